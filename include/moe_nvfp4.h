@@ -1,0 +1,205 @@
+/*
+ * moe_nvfp4.h -- C ABI of libmoe_nvfp4.so: the forward pass of a routed mixture-of-experts layer
+ * in NVIDIA's NVFP4 format with NVFP4 activations (W4A4), on one sm_103a GPU.
+ *
+ * The layer (shape of Qwen3.8-Flash-Next's MoE: hidden H = 2048, E = 512 routed experts, k = 10
+ * routed + 1 shared expert per token, SwiGLU experts of width I = 768):
+ *
+ *   logits  = x W_r^T                      (bf16 inputs, FP32 accumulation; + optional bias)
+ *   ids, w  = top-k of softmax_FP32(logits), ties to the lowest expert id, w renormalised to sum 1
+ *   g       = sigmoid(x w_sg)              (w_sg = row E of W_r: the shared-expert gate)
+ *   xq      = NVFP4(x)                     (E2M1 codes, UE4M3 scale per 16 along H, FP32 tensor scale)
+ *   rows    = the (token, expert) pairs grouped by expert id (stable), then the shared expert
+ *   h_r     = NVFP4_static( silu(xq W_gate[e]^T) * (xq W_up[e]^T) )   per row r of expert e
+ *   y_r     = h_r W_down[e]^T
+ *   out_t   = bf16( [residual_t +] sum_j w_tj y_(t,j) + g_t y_shared,t )   (FP32 accumulation)
+ *
+ * Sources for the format and the shape: the article "capy-flash runs a 125B MoE in full NVFP4 on
+ * two 16 GB GPUs ..." (richland.au), section "What shipped": E2M1 codes, UE4M3 block scales and an
+ * FP32 per-expert scale; 512 experts, 10 routed + 1 shared per layer. The capy-flash README v0.5.4,
+ * "What it does": activations are quantized to NVFP4 on the GPU (W4A4). The same article, "Why it
+ * matters": partial sums accumulate in FP32 throughout. The remaining steps (softmax top-k with
+ * renormalised weights, SwiGLU, static requantisation of the intermediate, sigmoid-gated shared
+ * expert) are this library's layer definition; the pages print no formula for them.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers owned by the caller unless a parameter says otherwise. The
+ *     library never allocates device memory and keeps no state between calls (except the
+ *     per-process driver entry point it looks up once).
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - NVFP4 tensors, row-major ("ModelOpt layout"): codes [rows][K/2] bytes, two E2M1 codes per
+ *     byte, the even-K element in the low nibble; block scales [rows][K/16] UE4M3 bytes; one FP32
+ *     tensor scale. Value = e2m1(code) * ue4m3(sf) * S.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *     They return MOE_OK after a successful launch; argument errors are detected on the host
+ *     before any launch and return an error code (moe_last_error_detail() gives the numbers).
+ *   - Scratch comes from a caller workspace of moe_workspace_bytes() bytes (256-byte aligned).
+ *     Kernels record device-side failures (a bounded wait that ran out) in a status word in the
+ *     workspace; moe_read_device_status() synchronises `stream` and returns it.
+ *   - Shapes: H and I multiples of 128; 1 <= k <= min(E, 32); 1 <= E <= 1024; T >= 0.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad enum value */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,    /* a shape outside the limits above */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < the size the call needs */
+    MOE_ERR_MISALIGNED = 4,           /* a pointer below its required alignment */
+    MOE_ERR_CUDA = 5,                 /* a CUDA runtime / driver call or a launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = 6,       /* a kernel's bounded wait ran out (status word) */
+    MOE_ERR_UNSUPPORTED_DEVICE = 7    /* the current device is not sm_103 */
+} moe_status_t;
+
+typedef void* moe_stream_t; /* cudaStream_t */
+
+/* NVFP4 weights of G experts, each an [N][K] matrix, in the PREPACKED layout that
+ * moe_prepack_nvfp4() writes (see there). gscale: [G][nscale] FP32 per-expert tensor scales. */
+typedef struct {
+    const uint8_t* codes; /* [G][N][K/2], rows in prepacked order */
+    const uint8_t* sf;    /* [G][N/128][K/64][512] scale-factor tiles */
+    const float* gscale;  /* [G][nscale] */
+} moe_nvfp4_bank_t;
+
+/* One MoE layer. The shared expert is expert index E of both banks. */
+typedef struct {
+    int H, E, k, I;
+    const uint16_t* w_router;   /* bf16 [E+1][H]; row E = shared-expert gate vector */
+    const float* logit_bias;    /* nullable, FP32 [E], added to the routed logits */
+    moe_nvfp4_bank_t w_gate_up; /* G = E+1, N = 2I, K = H, prepacked with gate/up interleave; gscale [E+1][2] (gate, up) */
+    moe_nvfp4_bank_t w_down;    /* G = E+1, N = H, K = I, prepacked plain; gscale [E+1] */
+    const float* s_mid;         /* FP32 [E+1]: static tensor scale of the intermediate h per expert */
+} moe_layer_t;
+
+/* Epilogues of moe_grouped_gemm_nvfp4. */
+enum {
+    MOE_EPI_F32 = 0,         /* out: FP32 [P][N] */
+    MOE_EPI_BF16 = 1,        /* out: bf16 [P][N] */
+    MOE_EPI_SWIGLU_NVFP4 = 2 /* gate/up bank; out: h codes [P][N/4], out_sf [P][N/32], scale epi_scale[g] */
+};
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_quantize_nvfp4 -- NVFP4 encoding of activations (W4A4: "What it does", capy-flash README).
+ *   x: bf16 [rows][K], K % 16 == 0. s_in: nullable device FP32 scalar; when NULL the tensor scale
+ *   is S = amax(|x|) / (6 * 448) (S = 1 when x is all zero), written to *s_out; when given, S =
+ *   *s_in (static scale) and is copied to *s_out. Per 16-element block: sf = UE4M3 nearest-even of
+ *   amax_b / (6 S) saturating at 448; each element: E2M1 nearest-even of x / (ue4m3(sf) S),
+ *   saturating at 6, sign kept; a block whose sf decodes to 0 has all codes 0.
+ *   codes: [rows][K/2]; sf: [rows][K/16]; s_out: FP32 scalar. ws: >= 256 bytes.
+ *   Results are bit-exact (every FP32 step is rounded to nearest, no contraction).
+ * moe_quantize_nvfp4_f32 -- the same from FP32 input (used to quantize weights).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t K, const float* s_in,
+                                uint8_t* codes, uint8_t* sf, float* s_out, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, const float* s_in,
+                                    uint8_t* codes, uint8_t* sf, float* s_out, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_route_topk -- router GEMM, FP32 softmax, top-k with renormalised weights, shared gate.
+ *   The capy-flash README v0.5.4 ("Measured") notes that the summation order of the router can
+ *   flip exact ties; here ties are broken by the lowest expert id.
+ *   x: bf16 [T][H]; uses L->w_router, L->logit_bias, L->H, L->E, L->k.
+ *   topk_ids: int32 [T][k] (routing order: weight non-increasing); topk_w: FP32 [T][k];
+ *   shared_g: nullable FP32 [T]; logits_out: nullable FP32 [T][E] (bias included).
+ *   ws: >= moe_workspace_bytes(H, E, k, I, T).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids,
+                            float* topk_w, float* shared_g, float* logits_out, void* ws,
+                            size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_permute -- stable counting sort of the T*k assignments f = t*k + j by expert id.
+ *   expert_offsets: int32 [E+2]: rows of expert e are [off[e], off[e+1]) (e < E); the shared
+ *   expert's group is [off[E], off[E+1]) = [T*k, T*k + T) when with_shared, else empty.
+ *   perm_src: int32 [T*k], perm_src[p] = f; src_perm: int32 [T*k], src_perm[f] = p;
+ *   row_token: nullable int32 [T*k + T*with_shared], the token of every permuted row (f / k, then
+ *   t for the shared rows) -- the gather index of the gate/up GEMM. Bit-exact.
+ *   ws: >= moe_workspace_bytes(any H, E, k, any I, T).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared,
+                         int32_t* expert_offsets, int32_t* perm_src, int32_t* src_perm,
+                         int32_t* row_token, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_prepack_nvfp4 -- rewrite G row-major NVFP4 matrices [N][K] into the layout the grouped GEMM
+ *   streams with TMA: codes keep [G][N][K/2] (with gate_up_interleave = 1 the rows are reordered
+ *   in blocks of 128 = 64 gate rows n..n+63 followed by the 64 up rows N/2+n..N/2+n+63); block
+ *   scales become 512-byte tiles [G][N/128][K/64]: tile byte (r % 32) * 16 + (r / 32) * 4 + j
+ *   holds the scale of row r (of the 128) for K-block 4 * (tile index) + j.
+ *   N % 128 == 0, K % 64 == 0; outputs must not alias inputs.
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_prepack_nvfp4(const uint8_t* codes, const uint8_t* sf, int G, int N, int K,
+                               int gate_up_interleave, uint8_t* codes_out, uint8_t* sf_out,
+                               moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_grouped_gemm_nvfp4 -- block-scaled grouped GEMM on the tcgen05 tensor cores
+ *   (kind::mxf4nvf4: E2M1 x E2M1 products, UE4M3 scale per 16 along K, FP32 accumulation in TMEM).
+ *   For every group g < G and row p in [group_offsets[g], group_offsets[g+1]):
+ *     acc[p][n] = sum_k A_hat[src(p)][k] * B_hat[g][n][k],  src(p) = a_row_index ? a_row_index[p] : p
+ *   A: codes [*][K/2], sf [*][K/16] (row-major), tensor scale a_scale[a_scale_per_group ? g : 0].
+ *   B: a prepacked bank with N columns (natural column order n of the unpacked matrix).
+ *   Epilogues:
+ *     MOE_EPI_F32 / MOE_EPI_BF16: out[p][n] = acc * a_scale * gscale[g][half]; half = n >= N/2
+ *        for a gate/up bank (nscale 2, interleaved prepack), else 0.
+ *     MOE_EPI_SWIGLU_NVFP4 (gate/up bank): h[p][j] = silu(gate) * up (FP32), j < N/2, encoded
+ *        like moe_quantize_nvfp4 with the static scale epi_scale[g]: out = codes [P][N/4],
+ *        out_sf = [P][N/32].
+ *   gate_up: 1 when b is a gate/up bank (nscale 2, interleaved prepack), 0 for a plain bank.
+ *   N % 128 == 0, K % 64 == 0, K <= 16384. P = group_offsets[G] (read on the device);
+ *   p_max: an upper bound of P that the host knows (sizes the grid).
+ *   ws: >= moe_workspace_bytes(..).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                    int a_scale_per_group, const int32_t* a_row_index,
+                                    const int32_t* group_offsets, int G, int64_t p_max,
+                                    const moe_nvfp4_bank_t* b, int N, int K, int gate_up, int epilogue,
+                                    const float* epi_scale, void* out, uint8_t* out_sf, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_combine -- weighted un-permute with FP32 accumulation ("Why it matters": FP32 partials):
+ *   out[t] = bf16( [residual[t] +] sum_j topk_w[t][j] * y[src_perm[t*k+j]]
+ *                  + (shared_g ? shared_g[t] * y[T*k + t] : 0) )
+ *   y: bf16 [T*k (+T)][H]; residual nullable bf16 [T][H]; out bf16 [T][H]. Each product is rounded
+ *   to FP32 before it is added (the README's rounding-order note: a product, then a sum).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_combine(const uint16_t* y, const float* topk_w, const float* shared_g,
+                         const int32_t* src_perm, int T, int k, int H, const uint16_t* residual,
+                         uint16_t* out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_layer_forward -- the whole layer (all steps above) on `stream`.
+ *   x: bf16 [T][H]; residual: nullable bf16 [T][H] (added to the output: a stack of MoE layers);
+ *   out: bf16 [T][H], must not alias x. ws: >= moe_workspace_bytes(H, E, k, I, T).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
+                               uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Workspace bytes for any call above with these sizes (T tokens). */
+size_t moe_workspace_bytes(int H, int E, int k, int I, int T);
+
+/* Synchronise `stream`, read and clear the device status word of `ws`: MOE_OK or
+ * MOE_ERR_DEVICE_TIMEOUT. */
+moe_status_t moe_read_device_status(void* ws, moe_stream_t stream);
+
+const char* moe_status_string(moe_status_t s);
+
+/* Thread-local text of the last host-side error, with the offending numbers. */
+const char* moe_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

@@ -1,0 +1,428 @@
+// api.cu -- the C ABI of libmoe_nvfp4 (include/moe_nvfp4.h): argument validation on the host,
+// workspace layout, and the launch sequence of the layer forward.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "../../include/moe_nvfp4.h"
+#include "kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+thread_local std::string g_detail;
+
+moe_status_t fail(moe_status_t s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_detail = buf;
+    return s;
+}
+
+moe_status_t cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+moe_status_t check_device()
+{
+    static int ok = -1;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ok < 0) {
+        int dev = 0, major = 0, minor = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(MOE_ERR_UNSUPPORTED_DEVICE, "no CUDA device");
+        }
+        ok = (major == 10 && minor == 3) ? 1 : 0;
+        if (!ok) return fail(MOE_ERR_UNSUPPORTED_DEVICE, "device is sm_%d%d, this library is built for sm_103a", major, minor);
+    }
+    return ok ? MOE_OK : fail(MOE_ERR_UNSUPPORTED_DEVICE, "device is not sm_103");
+}
+
+struct WsLayout {
+    size_t hdr, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, tile_off, perm_src, src_perm, row_token,
+        hist, h_codes, h_sf, y, total;
+};
+
+WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
+{
+    WsLayout L{};
+    size_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const size_t o = off;
+        off += (static_cast<size_t>(bytes < 0 ? 0 : bytes) + 255) & ~size_t(255);
+        return o;
+    };
+    const int64_t n = T * k, P = T * k + T;
+    L.hdr = take(sizeof(WsHeader));
+    L.topk_ids = take(n * 4);
+    L.topk_w = take(n * 4);
+    L.shared_g = take(T * 4);
+    L.logits = take(T * (E + 1) * 4);
+    L.x_codes = take(T * H / 2);
+    L.x_sf = take(T * H / 16);
+    L.offsets = take((E + 2) * 4);
+    L.tile_off = take((E + 2) * 4);
+    L.perm_src = take(n * 4);
+    L.src_perm = take(n * 4);
+    L.row_token = take(P * 4);
+    L.hist = take(perm_chunks(n) * E * 4);
+    L.h_codes = take(P * I / 2);
+    L.h_sf = take(P * I / 16);
+    L.y = take(P * H * 2);
+    L.total = off;
+    return L;
+}
+
+moe_status_t check_layer_shape(int H, int E, int k, int I)
+{
+    if (H < 128 || H > 8192 || H % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "H=%d not a multiple of 128 in [128, 8192]", H);
+    if (I < 128 || I > 8192 || I % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "I=%d not a multiple of 128 in [128, 8192]", I);
+    if (E < 1 || E > 1024) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "E=%d outside [1, 1024]", E);
+    if (k < 1 || k > 32 || k > E) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "k=%d outside [1, min(E=%d, 32)]", k, E);
+    return MOE_OK;
+}
+
+moe_status_t check_ws(const void* ws, size_t ws_bytes, size_t need)
+{
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(MOE_ERR_MISALIGNED, "workspace %p not 256-byte aligned", ws);
+    if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE_TOO_SMALL, "workspace %zu bytes < %zu needed", ws_bytes, need);
+    return MOE_OK;
+}
+
+#define MOE_TRY(x)                              \
+    do {                                        \
+        moe_status_t s_ = (x);                  \
+        if (s_ != MOE_OK) return s_;            \
+    } while (0)
+
+#define MOE_CUDA(x, what)                       \
+    do {                                        \
+        cudaError_t e_ = (x);                   \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+}  // namespace
+
+int device_sm_count()
+{
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                           uint32_t box1)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0, d0 * d1};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s)
+{
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE: unsupported shape";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL: workspace too small";
+        case MOE_ERR_MISALIGNED: return "MOE_ERR_MISALIGNED: misaligned pointer";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: CUDA error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a device-side wait ran out";
+        case MOE_ERR_UNSUPPORTED_DEVICE: return "MOE_ERR_UNSUPPORTED_DEVICE: not an sm_103 device";
+    }
+    return "unknown moe_status_t";
+}
+
+const char* moe_last_error_detail(void) { return g_detail.c_str(); }
+
+size_t moe_workspace_bytes(int H, int E, int k, int I, int T)
+{
+    if (H < 0 || E < 0 || k < 0 || I < 0 || T < 0) return 0;
+    return ws_layout(H, E, k, I, T).total;
+}
+
+moe_status_t moe_read_device_status(void* ws, moe_stream_t stream)
+{
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MOE_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    int status = 0;
+    MOE_CUDA(cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost), "read status");
+    MOE_CUDA(cudaMemset(ws, 0, sizeof(int)), "clear status");
+    if (status & kDevTimeoutGemm) return fail(MOE_ERR_DEVICE_TIMEOUT, "device status 0x%x: grouped GEMM wait timed out", status);
+    if (status & kDevBadExpertId) return fail(MOE_ERR_INVALID_ARG, "device status 0x%x: expert id outside [0, E)", status);
+    return MOE_OK;
+}
+
+static moe_status_t quantize_common(const void* x, bool f32, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
+                                    uint8_t* sf, float* s_out, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (rows < 0 || K <= 0 || K % 16) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "rows=%lld K=%lld: K must be a positive multiple of 16", (long long)rows, (long long)K);
+    if (!x || !codes || !sf || !s_out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(s_out, 4) || (s_in && !aligned(s_in, 4)))
+        return fail(MOE_ERR_MISALIGNED, "x must be 16-byte, codes 8-byte aligned");
+    MOE_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
+    MOE_TRY(check_device());
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = device_sm_count();
+    cudaError_t e = f32 ? launch_quantize_f32(static_cast<const float*>(x), rows, K, s_in, codes, sf, s_out, &hdr->amax_bits, sms, s)
+                        : launch_quantize(static_cast<const uint16_t*>(x), rows, K, s_in, codes, sf, s_out, &hdr->amax_bits, sms, s);
+    MOE_CUDA(e, "quantize launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_quantize_nvfp4(const uint16_t* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
+                                uint8_t* sf, float* s_out, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    return quantize_common(x, false, rows, K, s_in, codes, sf, s_out, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
+                                    uint8_t* sf, float* s_out, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    return quantize_common(x, true, rows, K, s_in, codes, sf, s_out, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids, float* topk_w,
+                            float* shared_g, float* logits_out, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    MOE_TRY(check_layer_shape(L->H, L->E, L->k, L->I));
+    if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    if (!x || !L->w_router || !topk_ids || !topk_w) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(x, 16) || !aligned(L->w_router, 16)) return fail(MOE_ERR_MISALIGNED, "x and w_router must be 16-byte aligned");
+    const WsLayout W = ws_layout(L->H, L->E, L->k, L->I, T);
+    MOE_TRY(check_ws(ws, ws_bytes, W.logits + static_cast<size_t>(T) * (L->E + 1) * 4));
+    MOE_TRY(check_device());
+    if (T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* logits = reinterpret_cast<float*>(static_cast<char*>(ws) + W.logits);
+    MOE_CUDA(launch_router_logits(x, T, L->H, L->E, L->w_router, L->logit_bias, logits, s), "router launch");
+    MOE_CUDA(launch_topk(logits, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s), "top-k launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* expert_offsets,
+                         int32_t* perm_src, int32_t* src_perm, int32_t* row_token, void* ws, size_t ws_bytes,
+                         moe_stream_t stream)
+{
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d k=%d E=%d outside the supported range", T, k, E);
+    if (!topk_ids || !expert_offsets || !perm_src || !src_perm) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    const size_t need = 256 + static_cast<size_t>(perm_chunks(static_cast<int64_t>(T) * k)) * E * 4;
+    MOE_TRY(check_ws(ws, ws_bytes, need));
+    MOE_TRY(check_device());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
+    MOE_CUDA(launch_permute(topk_ids, T, k, E, with_shared ? 1 : 0, expert_offsets, nullptr, perm_src, src_perm, row_token,
+                            hist, &hdr->status, s),
+             "permute launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_prepack_nvfp4(const uint8_t* codes, const uint8_t* sf, int G, int N, int K, int gate_up_interleave,
+                               uint8_t* codes_out, uint8_t* sf_out, moe_stream_t stream)
+{
+    if (G < 1 || N < 128 || N % 128 || K < 64 || K % 64)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "G=%d N=%d K=%d: N must be a multiple of 128 and K of 64", G, N, K);
+    if (!codes || !sf || !codes_out || !sf_out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(codes, 16) || !aligned(codes_out, 16) || !aligned(sf, 4) || !aligned(sf_out, 16))
+        return fail(MOE_ERR_MISALIGNED, "codes 16-byte, sf 4-byte, sf_out 16-byte alignment required");
+    MOE_TRY(check_device());
+    MOE_CUDA(launch_prepack(codes, sf, G, N, K, gate_up_interleave ? 1 : 0, codes_out, sf_out,
+                            static_cast<cudaStream_t>(stream)),
+             "prepack launch");
+    return MOE_OK;
+}
+
+static moe_status_t check_bank(const moe_nvfp4_bank_t* b, const char* name)
+{
+    if (!b || !b->codes || !b->sf || !b->gscale) return fail(MOE_ERR_INVALID_ARG, "bank %s has a NULL pointer", name);
+    if (!aligned(b->codes, 16) || !aligned(b->sf, 16) || !aligned(b->gscale, 4))
+        return fail(MOE_ERR_MISALIGNED, "bank %s: codes and sf must be 16-byte aligned", name);
+    return MOE_OK;
+}
+
+moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
+                                    int a_scale_per_group, const int32_t* a_row_index, const int32_t* group_offsets,
+                                    int G, int64_t p_max, const moe_nvfp4_bank_t* b, int N, int K, int gate_up,
+                                    int epilogue, const float* epi_scale, void* out, uint8_t* out_sf, void* ws,
+                                    size_t ws_bytes, moe_stream_t stream)
+{
+    if (G < 1 || G > kGemmMaxG) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "G=%d outside [1, %d]", G, kGemmMaxG);
+    if (N < 128 || N % 128 || K < 64 || K % 64 || K > 16384)
+        return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d: N must be a multiple of 128, K of 64 (<= 16384)", N, K);
+    if (p_max < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "p_max=%lld < 0", (long long)p_max);
+    if (epilogue < MOE_EPI_F32 || epilogue > MOE_EPI_SWIGLU_NVFP4) return fail(MOE_ERR_INVALID_ARG, "epilogue=%d", epilogue);
+    if (epilogue == MOE_EPI_SWIGLU_NVFP4 && (!gate_up || !epi_scale || !out_sf))
+        return fail(MOE_ERR_INVALID_ARG, "the SwiGLU epilogue needs a gate/up bank, epi_scale and out_sf");
+    if (!a_codes || !a_sf || !a_scale || !group_offsets || !out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(a_codes, 16) || !aligned(a_sf, 4) || !aligned(out, 16) || (out_sf && !aligned(out_sf, 4)))
+        return fail(MOE_ERR_MISALIGNED, "a_codes / out must be 16-byte, a_sf / out_sf 4-byte aligned");
+    MOE_TRY(check_bank(b, "b"));
+    const size_t need = 256 + ((static_cast<size_t>(G + 1) * 4 + 255) & ~size_t(255));
+    MOE_TRY(check_ws(ws, ws_bytes, need));
+    MOE_TRY(check_device());
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader* hdr = static_cast<WsHeader*>(ws);
+    int32_t* tile_off = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
+    MOE_CUDA(launch_tile_offsets(group_offsets, G, tile_off, s), "tile offsets launch");
+    GemmArgs ga{};
+    ga.a_codes = a_codes;
+    ga.a_sf = a_sf;
+    ga.a_scale = a_scale;
+    ga.a_scale_per_group = a_scale_per_group ? 1 : 0;
+    ga.a_row = a_row_index;
+    ga.offsets = group_offsets;
+    ga.tile_off = tile_off;
+    ga.G = G;
+    ga.b_codes = b->codes;
+    ga.b_sf = b->sf;
+    ga.b_scale = b->gscale;
+    ga.gate_up = gate_up ? 1 : 0;
+    ga.N = N;
+    ga.K = K;
+    ga.epilogue = epilogue;
+    ga.epi_scale = epi_scale;
+    ga.out = out;
+    ga.out_sf = out_sf;
+    ga.status = &hdr->status;
+    MOE_CUDA(launch_grouped_gemm(ga, p_max, device_sm_count(), s), "grouped GEMM launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_combine(const uint16_t* y, const float* topk_w, const float* shared_g, const int32_t* src_perm, int T,
+                         int k, int H, const uint16_t* residual, uint16_t* out, moe_stream_t stream)
+{
+    if (T < 0 || k < 1 || k > 32 || H < 8 || H % 8) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d k=%d H=%d", T, k, H);
+    if (!y || !topk_w || !src_perm || !out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(y, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
+        return fail(MOE_ERR_MISALIGNED, "y, out and residual must be 16-byte aligned");
+    MOE_TRY(check_device());
+    MOE_CUDA(launch_combine(y, topk_w, shared_g, src_perm, T, k, H, residual, out, static_cast<cudaStream_t>(stream)),
+             "combine launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual, uint16_t* out,
+                               void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    const int H = L->H, E = L->E, k = L->k, I = L->I;
+    MOE_TRY(check_layer_shape(H, E, k, I));
+    if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    if (!x || !out || !L->w_router || !L->s_mid) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(x, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)) || !aligned(L->w_router, 16))
+        return fail(MOE_ERR_MISALIGNED, "x, out, residual and w_router must be 16-byte aligned");
+    if (x == out) return fail(MOE_ERR_INVALID_ARG, "out must not alias x");
+    MOE_TRY(check_bank(&L->w_gate_up, "w_gate_up"));
+    MOE_TRY(check_bank(&L->w_down, "w_down"));
+    const WsLayout W = ws_layout(H, E, k, I, T);
+    MOE_TRY(check_ws(ws, ws_bytes, W.total));
+    MOE_TRY(check_device());
+    if (T == 0) return MOE_OK;
+
+    char* base = static_cast<char*>(ws);
+    WsHeader* hdr = reinterpret_cast<WsHeader*>(base + W.hdr);
+    auto P32 = [&](size_t o) { return reinterpret_cast<int32_t*>(base + o); };
+    auto PF = [&](size_t o) { return reinterpret_cast<float*>(base + o); };
+    auto P8 = [&](size_t o) { return reinterpret_cast<uint8_t*>(base + o); };
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = device_sm_count();
+    const int64_t P = static_cast<int64_t>(T) * k + T;
+
+    // W4A4: quantize the layer input once per token (dynamic tensor scale)
+    MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s), "quantize");
+    // router, softmax, top-k, shared gate
+    MOE_CUDA(launch_router_logits(x, T, H, E, L->w_router, L->logit_bias, PF(W.logits), s), "router");
+    MOE_CUDA(launch_topk(PF(W.logits), T, E, k, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), nullptr, s), "top-k");
+    // permutation by expert id, the shared expert appended as group E
+    MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), P32(W.tile_off), P32(W.perm_src),
+                            P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
+             "permute");
+    // gate/up GEMM with the fused SwiGLU + NVFP4 requantisation
+    GemmArgs g1{};
+    g1.a_codes = P8(W.x_codes);
+    g1.a_sf = P8(W.x_sf);
+    g1.a_scale = &hdr->s_x;
+    g1.a_row = P32(W.row_token);
+    g1.offsets = P32(W.offsets);
+    g1.tile_off = P32(W.tile_off);
+    g1.G = E + 1;
+    g1.b_codes = L->w_gate_up.codes;
+    g1.b_sf = L->w_gate_up.sf;
+    g1.b_scale = L->w_gate_up.gscale;
+    g1.gate_up = 1;
+    g1.N = 2 * I;
+    g1.K = H;
+    g1.epilogue = kEpiSwiGLU;
+    g1.epi_scale = L->s_mid;
+    g1.out = P8(W.h_codes);
+    g1.out_sf = P8(W.h_sf);
+    g1.status = &hdr->status;
+    MOE_CUDA(launch_grouped_gemm(g1, P, sms, s), "gate/up GEMM");
+    // down GEMM, bf16 rows in permuted order
+    GemmArgs g2 = g1;
+    g2.a_codes = P8(W.h_codes);
+    g2.a_sf = P8(W.h_sf);
+    g2.a_scale = L->s_mid;
+    g2.a_scale_per_group = 1;
+    g2.a_row = nullptr;
+    g2.b_codes = L->w_down.codes;
+    g2.b_sf = L->w_down.sf;
+    g2.b_scale = L->w_down.gscale;
+    g2.gate_up = 0;
+    g2.N = H;
+    g2.K = I;
+    g2.epilogue = kEpiBF16;
+    g2.epi_scale = nullptr;
+    g2.out = base + W.y;
+    g2.out_sf = nullptr;
+    MOE_CUDA(launch_grouped_gemm(g2, P, sms, s), "down GEMM");
+    // weighted combine (+ residual)
+    MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), P32(W.src_perm), T,
+                            k, H, residual, out, s),
+             "combine");
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,75 @@
+// kernels.cuh -- internal launchers of libmoe_nvfp4 (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---- quantize.cu
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes, uint8_t* sf,
+                            float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream);
+cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
+                                uint8_t* sf, float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream);
+
+// ---- router.cu
+// logits: FP32 [T][E+1] (column E = shared-gate logit, no bias).
+cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
+                                 float* logits, cudaStream_t stream);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w, float* shared_g,
+                        float* logits_out, cudaStream_t stream);
+
+// ---- permute.cu
+constexpr int kPermChunk = 512;  // assignments per warp-chunk
+constexpr int kGemmBM = 128;     // rows per GEMM M-tile (the permutation also writes tile offsets)
+inline int64_t perm_chunks(int64_t n) { return n <= 0 ? 1 : (n + kPermChunk - 1) / kPermChunk; }
+// offsets: [E+2]; tile_off: [E+2] prefix of ceil(rows_g / kGemmBM) over the E+1 groups (nullable).
+cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* offsets,
+                           int32_t* tile_off, int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist,
+                           int* status, cudaStream_t stream);
+// tile_off[g] = sum_{g' < g} ceil((offsets[g'+1] - offsets[g']) / kGemmBM), g = 0..G.
+cudaError_t launch_tile_offsets(const int32_t* offsets, int G, int32_t* tile_off, cudaStream_t stream);
+
+// ---- prepack.cu
+cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* sf, int G, int N, int K, int interleave,
+                           uint8_t* codes_out, uint8_t* sf_out, cudaStream_t stream);
+
+// ---- grouped_gemm.cu
+enum EpiKind : int { kEpiF32 = 0, kEpiBF16 = 1, kEpiSwiGLU = 2 };
+
+struct GemmArgs {
+    const uint8_t* a_codes;   // [*][K/2]
+    const uint8_t* a_sf;      // [*][K/16]
+    const float* a_scale;     // [1] or [G]
+    int a_scale_per_group;
+    const int32_t* a_row;     // nullable gather index, [P]
+    const int32_t* offsets;   // [G+1]
+    const int32_t* tile_off;  // [G+1]
+    int G;
+    const uint8_t* b_codes;   // prepacked [G][N][K/2] (described by the tensor map)
+    const uint8_t* b_sf;      // prepacked tiles [G][N/128][K/64][512]
+    const float* b_scale;     // [G][gate_up ? 2 : 1]
+    int gate_up;
+    int N, K;
+    int epilogue;
+    const float* epi_scale;   // [G] static scale of h (SwiGLU epilogue)
+    void* out;
+    uint8_t* out_sf;
+    int* status;
+};
+constexpr int kGemmMaxG = 1025;
+cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream);
+size_t grouped_gemm_smem_bytes();
+
+// ---- combine.cu
+cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* shared_g, const int32_t* src_perm, int T,
+                           int k, int H, const uint16_t* residual, uint16_t* out, cudaStream_t stream);
+
+// ---- api.cu
+int device_sm_count();
+CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                           uint32_t box1);
+
+}  // namespace moe

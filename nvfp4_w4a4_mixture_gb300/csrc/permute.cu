@@ -1,0 +1,185 @@
+// permute.cu -- stable counting sort of the T*k (token, slot) assignments by expert id.
+//
+// The flat assignment list f = t*k + j is cut into warp-chunks of kPermChunk entries.
+//   1. histogram: each warp counts its chunk per expert (warp match: one shared-memory add per
+//      run of equal ids, no atomics) -> hist[chunk][E];
+//   2. scan (one CTA): per expert, an exclusive scan over the chunks, then an exclusive scan over
+//      experts -> expert offsets, the global base of every (chunk, expert) and the GEMM tile
+//      offsets (ceil(rows / 128) per group, the shared expert appended as group E);
+//   3. scatter: each warp walks its chunk in order; an entry's position is its chunk base plus
+//      the number of earlier entries of the same expert in the chunk. Ascending f within every
+//      expert (stable), independent of scheduling: bit-exact.
+#include <cub/block/block_scan.cuh>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kPermWarps = 8;
+
+__global__ void __launch_bounds__(kPermWarps * 32)
+    k_perm_hist(const int32_t* __restrict__ ids, int64_t n, int E, int64_t nchunks, int32_t* __restrict__ hist,
+                int* status)
+{
+    extern __shared__ int32_t cnt[];  // [kPermWarps][E]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    int32_t* my = cnt + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp;
+    if (c >= nchunks) return;
+    const int64_t beg = c * kPermChunk, end = min(n, beg + kPermChunk);
+    for (int64_t base = beg; base < end; base += 32) {
+        const int64_t i = base + lane;
+        int e = -1;
+        if (i < end) {
+            e = ids[i];
+            if (e < 0 || e >= E) {
+                record_status(status, kDevBadExpertId);
+                e = -1;
+            }
+        }
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
+        __syncwarp();
+    }
+    for (int e = lane; e < E; e += 32) hist[c * E + e] = my[e];
+}
+
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    k_perm_scan(int32_t* __restrict__ hist, int64_t nchunks, int E, int T, int k, int with_shared,
+                int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off)
+{
+    using Scan = cub::BlockScan<int32_t, kScanThreads>;
+    __shared__ typename Scan::TempStorage tmp;
+    __shared__ int32_t total_s;
+    // items per thread: E <= 1024 experts (+ the shared group)
+    const int e = threadIdx.x;
+    int32_t cnt = 0;
+    if (e < E) {
+        for (int64_t c = 0; c < nchunks; ++c) {
+            const int32_t v = hist[c * E + e];
+            hist[c * E + e] = cnt;
+            cnt += v;
+        }
+    }
+    int32_t off;
+    Scan(tmp).ExclusiveSum(cnt, off);
+    if (e < E) offsets[e] = off;
+    if (e == E - 1) total_s = off + cnt;
+    __syncthreads();
+    const int32_t total = total_s;  // == T*k
+    if (e == 0) {
+        offsets[E] = total;
+        offsets[E + 1] = total + (with_shared ? T : 0);
+    }
+    if (e < E)
+        for (int64_t c = 0; c < nchunks; ++c) hist[c * E + e] += off;
+    if (tile_off) {
+        __syncthreads();
+        // groups 0..E-1 (routed) and E (shared): ceil(rows / BM)
+        int32_t mt = e < E ? (cnt + kGemmBM - 1) / kGemmBM : 0;
+        Scan(tmp).ExclusiveSum(mt, off);
+        if (e < E) tile_off[e] = off;
+        __syncthreads();
+        if (e == E - 1) total_s = off + mt;
+        __syncthreads();
+        if (e == 0) {
+            const int32_t shared_rows = with_shared ? T : 0;
+            tile_off[E] = total_s;
+            tile_off[E + 1] = total_s + (shared_rows + kGemmBM - 1) / kGemmBM;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPermWarps * 32)
+    k_perm_scatter(const int32_t* __restrict__ ids, int64_t n, int E, int k, int T, int with_shared, int64_t nchunks,
+                   const int32_t* __restrict__ hist, int32_t* __restrict__ perm_src, int32_t* __restrict__ src_perm,
+                   int32_t* __restrict__ row_token)
+{
+    extern __shared__ int32_t base_s[];  // [kPermWarps][E]
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // the shared-expert rows: row T*k + t holds token t
+    if (row_token && with_shared) {
+        for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < T;
+             t += static_cast<int64_t>(gridDim.x) * blockDim.x)
+            row_token[n + t] = static_cast<int32_t>(t);
+    }
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp;
+    if (c >= nchunks) return;
+    int32_t* my = base_s + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = hist[c * E + e];
+    __syncwarp();
+    const int64_t beg = c * kPermChunk, end = min(n, beg + kPermChunk);
+    const unsigned lt = (1u << lane) - 1u;
+    for (int64_t b = beg; b < end; b += 32) {
+        const int64_t i = b + lane;
+        int e = -1;
+        if (i < end) {
+            e = ids[i];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0) {
+            const int32_t pos = my[e] + __popc(m & lt);
+            perm_src[pos] = static_cast<int32_t>(i);
+            src_perm[i] = pos;
+            if (row_token) row_token[pos] = static_cast<int32_t>(i / k);
+        }
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* offsets,
+                           int32_t* tile_off, int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist,
+                           int* status, cudaStream_t stream)
+{
+    const int64_t n = static_cast<int64_t>(T) * k;
+    const int64_t nchunks = perm_chunks(n);
+    const int blocks = static_cast<int>((nchunks + kPermWarps - 1) / kPermWarps);
+    const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
+    k_perm_hist<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, nchunks, hist, status);
+    k_perm_scan<<<1, kScanThreads, 0, stream>>>(hist, nchunks, E, T, k, with_shared, offsets, tile_off);
+    k_perm_scatter<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, k, T, with_shared, nchunks, hist,
+                                                              perm_src, src_perm, row_token);
+    return cudaGetLastError();
+}
+
+// tile_off[g] for caller-given group offsets (the public grouped GEMM).
+__global__ void __launch_bounds__(kScanThreads) k_tile_offsets(const int32_t* __restrict__ offsets, int G,
+                                                               int32_t* __restrict__ tile_off)
+{
+    using Scan = cub::BlockScan<int32_t, kScanThreads>;
+    __shared__ typename Scan::TempStorage tmp;
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    for (int g0 = 0; g0 < G; g0 += kScanThreads) {
+        const int g = g0 + threadIdx.x;
+        int32_t mt = 0;
+        if (g < G) {
+            const int32_t rows = offsets[g + 1] - offsets[g];
+            mt = rows > 0 ? (rows + kGemmBM - 1) / kGemmBM : 0;
+        }
+        int32_t off, agg;
+        Scan(tmp).ExclusiveSum(mt, off, agg);
+        const int32_t c = carry;
+        if (g < G) tile_off[g] = c + off;
+        __syncthreads();
+        if (threadIdx.x == 0) carry = c + agg;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) tile_off[G] = carry;
+}
+
+cudaError_t launch_tile_offsets(const int32_t* offsets, int G, int32_t* tile_off, cudaStream_t stream)
+{
+    k_tile_offsets<<<1, kScanThreads, 0, stream>>>(offsets, G, tile_off);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,110 @@
+// quantize.cu -- NVFP4 encoding of activations (W4A4) and weights.
+//
+// Two passes over the tensor: a max-reduction for the tensor scale (skipped with a static
+// scale), then one thread per 16-element block. Loads are 16-byte vectors, a warp reads 1 KiB of
+// bf16 contiguously and writes 256 contiguous bytes of codes and 32 bytes of block scales.
+#include "kernels.cuh"
+
+namespace moe {
+
+__device__ __forceinline__ void load16(const uint16_t* p, float (&v)[16])
+{
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(p));
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = bf16_to_f32(w[i] & 0xFFFFu);
+        v[2 * i + 1] = bf16_to_f32(w[i] >> 16);
+    }
+}
+
+__device__ __forceinline__ void load16(const float* p, float (&v)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p) + i);
+        v[4 * i] = a.x;
+        v[4 * i + 1] = a.y;
+        v[4 * i + 2] = a.z;
+        v[4 * i + 3] = a.w;
+    }
+}
+
+__device__ __forceinline__ uint32_t abs_bits_max(uint32_t m, float f) { return max(m, __float_as_uint(fabsf(f))); }
+
+// amax(|x|) over nblocks 16-element blocks, as the bit pattern of a non-negative float.
+template <typename Tin>
+__global__ void k_amax(const Tin* __restrict__ x, int64_t nblocks, unsigned* __restrict__ amax_bits)
+{
+    uint32_t m = 0;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
+        float v[16];
+        load16(x + b * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) m = abs_bits_max(m, v[i]);
+    }
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(amax_bits, m);
+}
+
+template <typename Tin>
+__global__ void k_quantize(const Tin* __restrict__ x, int64_t nblocks, const float* __restrict__ s_static,
+                           const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes,
+                           uint8_t* __restrict__ sf, float* __restrict__ s_out)
+{
+    float S;
+    if (s_static) {
+        S = *s_static;
+    } else {
+        const float amax = __uint_as_float(*amax_bits);
+        S = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    }
+    if (s_out && blockIdx.x == 0 && threadIdx.x == 0) *s_out = S;
+    const float six_s = __fmul_rn(6.0f, S);
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
+        float v[16];
+        load16(x + b * 16, v);
+        uint32_t lo, hi;
+        const uint32_t s = nvfp4_encode16(v, S, six_s, lo, hi);
+        *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(lo, hi);
+        sf[b] = static_cast<uint8_t>(s);
+    }
+}
+
+static int quant_grid(int64_t nblocks, int sms)
+{
+    const int64_t want = (nblocks + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    return static_cast<int>(want < 1 ? 1 : (want > cap ? cap : want));
+}
+
+template <typename Tin>
+cudaError_t launch_quantize_t(const Tin* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes, uint8_t* sf,
+                              float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
+{
+    const int64_t nblocks = rows * K / 16;
+    if (!s_in) {
+        cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), stream);
+        if (e != cudaSuccess) return e;
+        if (nblocks > 0) k_amax<Tin><<<quant_grid(nblocks, sms), 256, 0, stream>>>(x, nblocks, amax_scratch);
+    }
+    k_quantize<Tin><<<quant_grid(nblocks, sms), 256, 0, stream>>>(x, nblocks, s_in, amax_scratch, codes, sf, s_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes, uint8_t* sf,
+                            float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
+{
+    return launch_quantize_t<uint16_t>(x, rows, K, s_in, codes, sf, s_out, amax_scratch, sms, stream);
+}
+
+cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
+                                uint8_t* sf, float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
+{
+    return launch_quantize_t<float>(x, rows, K, s_in, codes, sf, s_out, amax_scratch, sms, stream);
+}
+
+}  // namespace moe

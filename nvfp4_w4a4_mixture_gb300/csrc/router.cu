@@ -1,0 +1,157 @@
+// router.cu -- router logits (x W_r^T, bf16 inputs, FP32 accumulation) and the FP32 softmax top-k.
+//
+// Logits: one warp per router row, a tile of kRouterTT tokens staged in shared memory, 16-byte
+// loads of the router row (each row of W_r is read once per token tile). Every product of two
+// bf16 values is exact in FP32; the sum runs in a fixed order (per-lane strided partial sums,
+// then a butterfly), so the result is deterministic.
+// Top-k: one warp per token; k rounds of a warp arg-max on (logit desc, expert id asc), which
+// is the lowest-index tie rule; the renormalised weights are the softmax over the selected
+// logits (the full softmax denominator cancels), the shared gate is sigmoid(logit E).
+#include <cfloat>
+
+#include "kernels.cuh"
+
+namespace moe {
+
+constexpr int kRouterTT = 8;     // tokens per CTA
+constexpr int kRouterWarps = 8;  // router rows per CTA
+
+__global__ void __launch_bounds__(kRouterWarps * 32)
+    k_router_logits(const uint16_t* __restrict__ x, int T, int H, int E, const uint16_t* __restrict__ w,
+                    const float* __restrict__ bias, float* __restrict__ logits)
+{
+    extern __shared__ __align__(16) uint16_t xs[];  // [kRouterTT][H]
+    const int t0 = blockIdx.y * kRouterTT;
+    const int nt = min(kRouterTT, T - t0);
+    // stage the token tile (16-byte vectors)
+    const int vec_per_row = H / 8;
+    for (int i = threadIdx.x; i < kRouterTT * vec_per_row; i += blockDim.x) {
+        const int t = i / vec_per_row, c = i % vec_per_row;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < nt) v = __ldg(reinterpret_cast<const uint4*>(x + static_cast<int64_t>(t0 + t) * H) + c);
+        reinterpret_cast<uint4*>(xs + t * H)[c] = v;
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int e = blockIdx.x * kRouterWarps + warp;
+    if (e > E) return;
+    float acc[kRouterTT];
+#pragma unroll
+    for (int t = 0; t < kRouterTT; ++t) acc[t] = 0.0f;
+    const uint16_t* wr = w + static_cast<int64_t>(e) * H;
+    for (int h0 = lane * 8; h0 < H; h0 += 256) {
+        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + h0));
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int t = 0; t < kRouterTT; ++t) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h0);
+            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu)));
+                acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16)));
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kRouterTT; ++t) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xFFFFFFFFu, acc[t], o));
+    }
+    if (lane < nt) {
+        float v = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kRouterTT; ++t)
+            if (t == lane) v = acc[t];
+        if (bias && e < E) v = __fadd_rn(v, bias[e]);
+        logits[static_cast<int64_t>(t0 + lane) * (E + 1) + e] = v;
+    }
+}
+
+constexpr int kTopkMaxPerLane = 32;  // E <= 1024
+
+__global__ void k_topk(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
+                       float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
+{
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
+    if (warp >= T) return;
+    const int t = warp;
+    const float* l = logits + static_cast<int64_t>(t) * (E + 1);
+    float v[kTopkMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kTopkMaxPerLane; ++i) {
+        const int e = i * 32 + lane;
+        v[i] = e < E ? l[e] : -FLT_MAX;
+        if (logits_out && e < E) logits_out[static_cast<int64_t>(t) * E + e] = v[i];
+    }
+    float sel_l0 = 0.0f, wsum = 0.0f;
+    float my_l = 0.0f;  // lane j keeps the j-th selected logit
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        float best = -FLT_MAX;
+        int bid = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < kTopkMaxPerLane; ++i) {
+            const int e = i * 32 + lane;
+            if (e < E && (v[i] > best || (v[i] == best && e < bid))) {
+                best = v[i];
+                bid = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
+            if (ob > best || (ob == best && oi < bid)) {
+                best = ob;
+                bid = oi;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kTopkMaxPerLane; ++i)
+            if (i * 32 + lane == bid) v[i] = -FLT_MAX;
+        if (j == 0) sel_l0 = best;
+        if (lane == j) {
+            my_l = best;
+            my_id = bid;
+        }
+    }
+    // softmax over the selected logits (max = first selected)
+    float p = 0.0f;
+    if (lane < k) p = expf(my_l - sel_l0);
+    wsum = p;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
+    if (lane < k) {
+        topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
+        topk_w[static_cast<int64_t>(t) * k + lane] = p / wsum;
+    }
+    if (shared_g && lane == 0) shared_g[t] = 1.0f / (1.0f + expf(-l[E]));
+}
+
+cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
+                                 float* logits, cudaStream_t stream)
+{
+    if (T <= 0) return cudaSuccess;
+    const size_t smem = static_cast<size_t>(kRouterTT) * H * sizeof(uint16_t);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(k_router_logits, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr_set = true;
+    }
+    dim3 grid((E + 1 + kRouterWarps - 1) / kRouterWarps, (T + kRouterTT - 1) / kRouterTT);
+    k_router_logits<<<grid, kRouterWarps * 32, smem, stream>>>(x, T, H, E, w_router, bias, logits);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w, float* shared_g,
+                        float* logits_out, cudaStream_t stream)
+{
+    if (T <= 0) return cudaSuccess;
+    const int warps_per_block = 8;
+    const int blocks = (T + warps_per_block - 1) / warps_per_block;
+    k_topk<<<blocks, warps_per_block * 32, 0, stream>>>(logits, T, E, k, topk_ids, topk_w, shared_g, logits_out);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

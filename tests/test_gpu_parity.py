@@ -1,0 +1,341 @@
+"""GPU parity: every call of the C ABI against the CPU oracle on the same seeded inputs.
+
+Bars: bit-exact for codes, block scales, tensor scales, expert ids and routing order, offsets and
+permutation indices; the gate/up GEMM (FP32 out) within 1e-5 relative Frobenius error (overall and
+per expert); the layer output within 2e-2 relative Frobenius error; >= 99.9 % of the requantized
+intermediate codes identical; routing weights within 1e-6.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_w4a4_mixture_gb300 import workloads as wl
+from tests import inputs as I_
+
+pytestmark = pytest.mark.gpu
+
+GEMM_TOL = 1e-5
+LAYER_TOL = 2e-2
+CODE_MATCH = 0.999
+W_TOL = 1e-6
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import nvfp4_w4a4_mixture_gb300 as m
+    from nvfp4_w4a4_mixture_gb300 import build
+
+    build.build()
+    m.lib()
+    return m
+
+
+def dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def bf16_dev(x32):
+    return torch.from_numpy(np.ascontiguousarray(x32, np.float32)).to(torch.bfloat16).cuda()
+
+
+def nibbles(codes):
+    c = np.asarray(codes)
+    out = np.empty(c.shape[:-1] + (c.shape[-1] * 2,), np.uint8)
+    out[..., 0::2] = c & 15
+    out[..., 1::2] = c >> 4
+    return out
+
+
+def gpu_layer(m, case):
+    E, H, I, k = case["E"], case["H"], case["I"], case["k"]
+    gu, dn = case["gu"], case["dn"]
+    layer = m.MoeLayer(H, E, k, I, bf16_dev(case["w_r"]),
+                       (dev(gu[0]), dev(gu[1]), dev(gu[2])), (dev(dn[0]), dev(dn[1]), dev(dn[2])),
+                       dev(case["s_mid"]), logit_bias=None if case["bias"] is None else dev(case["bias"]))
+    return layer
+
+
+# ------------------------------------------------------------------------------------------------
+# quantize
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,K", [(64, 256), (1, 16), (3, 48), (1000, 2064), (4, 2048)])
+def test_quantize_bf16_bitexact(moe, rows, K):
+    x = wl.gen_x(rows * 7 + K, rows, K)
+    c_ref, s_ref, S_ref = oracle.quantize_nvfp4(x)
+    codes, sf, S = moe.moe_quantize_nvfp4(bf16_dev(x))
+    assert np.float32(S.item()) == S_ref
+    np.testing.assert_array_equal(sf.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(codes.cpu().numpy(), c_ref)
+
+
+def test_quantize_fp32_weights_bitexact(moe):
+    g, u, d = wl.gen_expert(0, 3, 2048, 768)
+    for w in (g, d):
+        c_ref, s_ref, S_ref = oracle.quantize_nvfp4(w)
+        codes, sf, S = moe.moe_quantize_nvfp4(dev(w))
+        assert np.float32(S.item()) == S_ref
+        np.testing.assert_array_equal(sf.cpu().numpy(), s_ref)
+        np.testing.assert_array_equal(codes.cpu().numpy(), c_ref)
+
+
+def test_quantize_golden_examples(moe):
+    from tests.test_oracle_pins import _load_golden
+
+    for ex in _load_golden():
+        row = ex["row"][None, :]
+        s_in = None if ex["scale"] is None else dev(np.array([ex["scale"]], np.float32))
+        codes, sf, S = moe.moe_quantize_nvfp4(dev(row), s_in=s_in)
+        assert S.item() == ex["S"], ex["name"]
+        assert list(sf.cpu().numpy()[0]) == ex["sf"], ex["name"]
+        assert list(nibbles(codes.cpu().numpy())[0]) == ex["codes"], ex["name"]
+
+
+def test_quantize_static_scale_edge_values(moe):
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((32, 128)) * np.exp(rng.uniform(-12, 6, (32, 1)))).astype(np.float32)
+    x[0] = 0.0
+    x[1, :16] = 2.0 ** -20  # underflows to a zero block scale
+    x[2] = 1e4              # saturates
+    x[3, 5] = -0.0
+    for S in (2.0 ** -8, 0.013, 7.5):
+        c_ref, s_ref, _ = oracle.quantize_nvfp4(x, s_in=S)
+        codes, sf, Sd = moe.moe_quantize_nvfp4(dev(x), s_in=dev(np.array([S], np.float32)))
+        np.testing.assert_array_equal(sf.cpu().numpy(), s_ref)
+        np.testing.assert_array_equal(codes.cpu().numpy(), c_ref)
+
+
+# ------------------------------------------------------------------------------------------------
+# router
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("config", ["tiny", "decode", "prefill4k"])
+def test_route_topk(moe, config):
+    c = wl.CONFIGS[config]
+    H, E, k, T = c["H"], c["E"], c["k"], c["T"]
+    w_r = wl.gen_router(0, E, H)
+    bias = I_.bias_for(config)
+    b64 = None if bias is None else bias.astype(np.float64)
+    x, _ = I_.draw_x(0, T, H, w_r, k, bias=b64)
+    ids_ref, w_ref, g_ref, lg_ref = oracle.router(x, w_r, k, bias=b64, want_logits=True)
+    dummy = (torch.zeros(1, 1, 8, dtype=torch.uint8, device="cuda"),) * 2 + (torch.ones(1, 2, device="cuda"),)
+    layer = moe.MoeLayer(H, E, k, 128, bf16_dev(w_r), dummy, dummy, torch.ones(E + 1, device="cuda"),
+                         logit_bias=None if bias is None else dev(bias), prepacked=True)
+    ids, w, g, lg = moe.moe_route_topk(bf16_dev(x), layer, want_logits=True)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.max(np.abs(w.cpu().numpy() - w_ref)) <= W_TOL
+    assert np.max(np.abs(w.cpu().numpy().sum(1) - 1.0)) <= W_TOL
+    assert np.max(np.abs(g.cpu().numpy() - g_ref)) <= W_TOL
+    assert np.max(np.abs(lg.cpu().numpy() - lg_ref)) <= 1e-4
+
+
+def test_route_exact_ties_lowest_index(moe):
+    H, E, k, T = 256, 16, 4, 8
+    rng = np.random.default_rng(3)
+    w_r = wl.bf16_round(rng.standard_normal((E + 1, H)).astype(np.float32) * 0.05)
+    w_r[7] = w_r[3]
+    w_r[12] = w_r[3]
+    bias = np.zeros(E, np.float32)
+    bias[3] = bias[7] = bias[12] = 1e3  # the tied trio is always selected first
+    x = wl.gen_x(4, T, H)
+    ids_ref, _, _, _ = oracle.router(x, w_r, k, bias=bias.astype(np.float64))
+    dummy = (torch.zeros(1, 1, 8, dtype=torch.uint8, device="cuda"),) * 2 + (torch.ones(1, 2, device="cuda"),)
+    layer = moe.MoeLayer(H, E, k, 128, bf16_dev(w_r), dummy, dummy, torch.ones(E + 1, device="cuda"),
+                         logit_bias=dev(bias), prepacked=True)
+    ids, w, _, _ = moe.moe_route_topk(bf16_dev(x), layer)
+    ids = ids.cpu().numpy()
+    np.testing.assert_array_equal(ids, ids_ref)
+    assert np.all(ids[:, :3] == [3, 7, 12])
+    w = w.cpu().numpy()
+    assert np.all(w[:, 0] == w[:, 1]) and np.all(w[:, 1] == w[:, 2])
+
+
+# ------------------------------------------------------------------------------------------------
+# permute
+# ------------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,k,E,mode", [(64, 2, 16, "rand"), (4, 10, 512, "rand"), (1, 1, 1, "rand"),
+                                        (1000, 3, 7, "one"), (16384, 10, 512, "hot"), (300, 8, 1024, "rand"),
+                                        (0, 4, 16, "rand")])
+def test_permute_bitexact(moe, T, k, E, mode):
+    rng = np.random.default_rng(T + k + E)
+    if mode == "one":
+        ids = np.zeros((T, k), np.int32)
+        ids[:] = np.arange(k) % E
+        ids[:, 0] = 5
+    elif mode == "hot":
+        hot = rng.random((T, k)) < 0.5
+        ids = np.where(hot, rng.integers(0, 51, (T, k)), rng.integers(51, E, (T, k))).astype(np.int32)
+    else:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32) if T else np.zeros((0, k), np.int32)
+    off_ref, ps_ref, sp_ref = oracle.permute(ids, E) if T else (np.zeros(E + 2, np.int32), None, None)
+    if T == 0:
+        return  # nothing to launch; covered by the host tests
+    off, ps, sp, rt = moe.moe_permute(dev(ids), E)
+    np.testing.assert_array_equal(off.cpu().numpy(), off_ref)
+    np.testing.assert_array_equal(ps.cpu().numpy(), ps_ref)
+    np.testing.assert_array_equal(sp.cpu().numpy(), sp_ref)
+    rt = rt.cpu().numpy()
+    np.testing.assert_array_equal(rt[: T * k], ps_ref // k)
+    np.testing.assert_array_equal(rt[T * k:], np.arange(T))
+
+
+# ------------------------------------------------------------------------------------------------
+# grouped GEMM
+# ------------------------------------------------------------------------------------------------
+
+def _gemm_case(seed, counts, H, I, N_kind):
+    """Random activations + oracle-quantized weights for groups with the given row counts."""
+    G = len(counts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    P = int(offsets[-1])
+    rng = np.random.default_rng(seed)
+    src_rows = max(P, 1) + 5
+    K = H if N_kind == "gate_up" else I
+    a = wl.bf16_round(rng.standard_normal((src_rows, K)).astype(np.float32))
+    a_row = rng.integers(0, src_rows, P).astype(np.int32)
+    ac, asf, sa = oracle.quantize_nvfp4(a)
+    if N_kind == "gate_up":
+        N = 2 * I
+        bc = np.zeros((G, N, K // 2), np.uint8)
+        bs = np.zeros((G, N, K // 16), np.uint8)
+        bsc = np.zeros((G, 2), np.float32)
+        for g in range(G):
+            for h in range(2):
+                w = rng.standard_normal((I, K)).astype(np.float32) * 0.02
+                c, s, S = oracle.quantize_nvfp4(w)
+                bc[g, h * I:(h + 1) * I], bs[g, h * I:(h + 1) * I], bsc[g, h] = c, s, S
+    else:
+        N = H
+        bc = np.zeros((G, N, K // 2), np.uint8)
+        bs = np.zeros((G, N, K // 16), np.uint8)
+        bsc = np.zeros(G, np.float32)
+        for g in range(G):
+            c, s, S = oracle.quantize_nvfp4(rng.standard_normal((N, K)).astype(np.float32) * 0.02)
+            bc[g], bs[g], bsc[g] = c, s, S
+    return dict(offsets=offsets, P=P, ac=ac, asf=asf, sa=sa, a_row=a_row, bc=bc, bs=bs, bsc=bsc, N=N, K=K)
+
+
+@pytest.mark.parametrize("counts", [[3, 0, 130, 1, 128, 257], [1] * 40, [700], [0, 0, 5]])
+def test_gemm_gate_up_f32(moe, counts):
+    c = _gemm_case(len(counts), counts, 256, 128, "gate_up")
+    ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
+    bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
+    out = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
+                                     dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], True,
+                                     moe.EPI_F32, a_row_index=dev(c["a_row"]))
+    out = out.cpu().numpy()
+    assert I_.rel_frobenius(out, ref) <= GEMM_TOL
+    for g in range(len(counts)):
+        p0, p1 = c["offsets"][g], c["offsets"][g + 1]
+        if p1 > p0:
+            assert I_.rel_frobenius(out[p0:p1], ref[p0:p1]) <= GEMM_TOL, g
+
+
+def test_gemm_gate_up_f32_flash_shape(moe):
+    c = _gemm_case(11, [2, 130, 1], 2048, 768, "gate_up")
+    ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
+    bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
+    out = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
+                                     dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], True,
+                                     moe.EPI_F32, a_row_index=dev(c["a_row"])).cpu().numpy()
+    assert I_.rel_frobenius(out, ref) <= GEMM_TOL
+    for g in range(3):
+        p0, p1 = c["offsets"][g], c["offsets"][g + 1]
+        assert I_.rel_frobenius(out[p0:p1], ref[p0:p1]) <= GEMM_TOL
+
+
+@pytest.mark.parametrize("H,I", [(256, 128), (2048, 768)])
+def test_gemm_down_bf16(moe, H, I):
+    c = _gemm_case(5, [5, 129, 0, 2], H, I, "down")
+    ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
+    bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), False)
+    out = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
+                                     dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], False,
+                                     moe.EPI_BF16, a_row_index=dev(c["a_row"]))
+    out = out.float().cpu().numpy()
+    # bf16 output: one rounding of each element (relative 2^-9)
+    assert I_.rel_frobenius(out, ref) <= 4e-3
+
+
+@pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 130, 1, 128]), (2048, 768, [1, 40, 3])])
+def test_gemm_swiglu_requant(moe, H, I, counts):
+    c = _gemm_case(7, counts, H, I, "gate_up")
+    G = len(counts)
+    gu_ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
+    h_ref = oracle.swiglu(gu_ref)
+    s_mid = np.full(G, np.float32(np.abs(h_ref).max() / 2688.0 * 0.8), np.float32)  # some values saturate
+    hc_ref, hs_ref = oracle.requantize_groups(h_ref, c["offsets"], s_mid)
+    bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
+    hc, hs = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
+                                        dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], True,
+                                        moe.EPI_SWIGLU_NVFP4, a_row_index=dev(c["a_row"]), epi_scale=dev(s_mid))
+    n_g, n_r = nibbles(hc.cpu().numpy()), nibbles(hc_ref)
+    match = np.mean(n_g == n_r)
+    assert match >= CODE_MATCH, match
+    assert np.mean(hs.cpu().numpy() == hs_ref) >= CODE_MATCH
+
+
+# ------------------------------------------------------------------------------------------------
+# combine and the whole layer
+# ------------------------------------------------------------------------------------------------
+
+def test_combine(moe):
+    rng = np.random.default_rng(8)
+    T, k, H = 37, 3, 256
+    P = T * k + T
+    y = wl.bf16_round(rng.standard_normal((P, H)).astype(np.float32))
+    tw = rng.random((T, k)).astype(np.float32)
+    g = rng.random(T).astype(np.float32)
+    src_perm = rng.permutation(T * k).astype(np.int32)
+    res = wl.bf16_round(rng.standard_normal((T, H)).astype(np.float32))
+    o64, o16 = oracle.combine(y.astype(np.float64), tw.astype(np.float64), src_perm, shared_g=g.astype(np.float64),
+                              shared_row0=T * k, residual=res)
+    out = moe.moe_combine(bf16_dev(y), dev(tw), dev(src_perm), shared_g=dev(g), residual=bf16_dev(res))
+    out = out.float().cpu().numpy()
+    assert np.max(np.abs(out - o64) / (np.abs(o64) + 1e-3)) <= 2 ** -8
+
+
+def _check_layer(moe, case, residual=False):
+    layer = gpu_layer(moe, case)
+    x = case["x"]
+    res = wl.bf16_round(np.random.default_rng(1).standard_normal(x.shape).astype(np.float32)) if residual else None
+    out = moe.moe_layer_forward(layer, bf16_dev(x), residual=None if res is None else bf16_dev(res))
+    moe.moe_read_device_status()
+    out = out.float().cpu().numpy()
+    rows = case["rows"]
+    b64 = None if case["bias"] is None else case["bias"].astype(np.float64)
+    Sx = oracle.tensor_scale(x)
+    ref = oracle.layer_forward(x[rows], case["w_r"], case["k"], case["gu"], case["dn"], case["s_mid"], bias=b64,
+                               residual=None if res is None else res[rows], x_scale=Sx)
+    err = I_.rel_frobenius(out[rows], ref["out_f64"])
+    assert err <= LAYER_TOL, err
+    return err
+
+
+def test_layer_tiny(moe):
+    case = I_.layer_case("tiny")
+    err = _check_layer(moe, case)
+    assert err < 5e-3  # requantized codes agree, so the error is the bf16 rounding of y and out
+
+
+def test_layer_tiny_residual(moe):
+    _check_layer(moe, I_.layer_case("tiny"), residual=True)
+
+
+def test_layer_decode_full_size(moe):
+    _check_layer(moe, I_.layer_case("decode"))
+
+
+def test_layer_prefill4k_sampled(moe):
+    _check_layer(moe, I_.layer_case("prefill4k", sample=12))
+
+
+def test_device_status_clean(moe):
+    moe.moe_read_device_status()
