@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 W4A4 routed-MoE layer forward (tokens/s per layer on one GB300).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|prefill4k|prefill16k|stack48|tiny]
+                    [--impl ours|reference] [--no-graph] [--no-cpu-baseline]
+
+A step is one whole layer forward (router, W4A4 quantisation, permutation, gate/up GEMM with fused
+SwiGLU + requantisation, down GEMM, combine) over one batch of synthetic tokens whose inputs are
+resident in HBM. The default workload is the Flash-Next-shaped decode call: hidden 2048, 512
+experts, top-10 + 1 shared, intermediate 768, 4 tokens (an MTP K=3 verify window). L2 is flushed
+(a 256 MiB write) before every timed step, outside the timed interval. Each step is timed with
+CUDA events on the launching stream. Under torchrun every rank runs an independent replica
+(weak scaling: per-GPU work fixed); rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (the plain FP64 reference of the same layer) on the host
+cores, one bounded sample of the workload per step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_w4a4_mixture_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (NVFP4 W4A4) at 1 GB300; % of FP4-TC / HBM roofline"
+DEFAULT_STEPS = {"tiny": 2000, "decode": 3000, "prefill4k": 300, "prefill16k": 100, "stack48": 10}
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor-core ratio
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-graph", action="store_true", help="launch the layer directly instead of a CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.config]
+    a.warmup = max(a.warmup, 3)
+    return a
+
+
+def workload_name(c, name):
+    s = "%s: MoE layer H%d E%d top-%d + 1 shared, I%d, %d tokens" % (name, c["H"], c["E"], c["k"], c["I"], c["T"])
+    if c["router"] == "zipf":
+        s += ", Zipf(1.1) expert prior"
+    elif c["router"] == "hot":
+        s += ", 10% of experts take 50% of assignments"
+    if c["layers"] > 1:
+        s += ", %d layers + residual" % c["layers"]
+    return s
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ------------------------------------------------------------------------------------------------
+
+class Dist:
+    def __init__(self):
+        import torch
+        import torch.distributed as dist
+
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.dist = dist if self.world > 1 else None
+        if torch.cuda.is_available():
+            torch.cuda.set_device(self.local)
+        if self.dist:
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    def barrier(self):
+        if self.dist:
+            self.dist.barrier()
+
+    def max(self, v):
+        if not self.dist:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist:
+            self.dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+
+        self.proc = None
+        sel = []
+        try:
+            p = torch.cuda.get_device_properties(device)
+            bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            sel = ["-i", bus]
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "50"] + sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out = self.proc.communicate(timeout=10)[0]
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# synthetic layer on the device
+# ------------------------------------------------------------------------------------------------
+
+def make_device_layer(m, c, seed, layer_idx, s_mid):
+    """Weights drawn on the device (seeded torch RNG, the workload's distributions), expert matrices
+    quantised to NVFP4 with the library's quantizer (one FP32 scale per expert matrix), prepacked."""
+    import torch
+
+    H, E, I = c["H"], c["E"], c["I"]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1_000_003 * seed + 7919 * layer_idx + 1)
+    w_r = (torch.randn(E + 1, H, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    gu_codes = torch.empty(E + 1, 2 * I, H // 2, dtype=torch.uint8, device="cuda")
+    gu_sf = torch.empty(E + 1, 2 * I, H // 16, dtype=torch.uint8, device="cuda")
+    gu_scale = torch.empty(E + 1, 2, dtype=torch.float32, device="cuda")
+    dn_codes = torch.empty(E + 1, H, I // 2, dtype=torch.uint8, device="cuda")
+    dn_sf = torch.empty(E + 1, H, I // 16, dtype=torch.uint8, device="cuda")
+    dn_scale = torch.empty(E + 1, dtype=torch.float32, device="cuda")
+    ws = m.Workspace(4096)
+    for e in range(E + 1):
+        w = torch.randn(2 * I, H, generator=g, device="cuda") * 0.02
+        for h in range(2):
+            m.moe_quantize_nvfp4(w[h * I:(h + 1) * I], ws=ws,
+                                 out=(gu_codes[e, h * I:(h + 1) * I], gu_sf[e, h * I:(h + 1) * I], gu_scale[e, h:h + 1]))
+        wd = torch.randn(H, I, generator=g, device="cuda") * 0.02
+        m.moe_quantize_nvfp4(wd, ws=ws, out=(dn_codes[e], dn_sf[e], dn_scale[e:e + 1]))
+    bias = wl.router_bias(c["router"], E)
+    bias_t = None if bias is None else torch.tensor(bias.astype("float32"), device="cuda")
+    s_mid_t = torch.full((E + 1,), s_mid, dtype=torch.float32, device="cuda")
+    layer = m.MoeLayer(H, E, c["k"], I, w_r, (gu_codes, gu_sf, gu_scale), (dn_codes, dn_sf, dn_scale), s_mid_t,
+                       logit_bias=bias_t)
+    del gu_codes, gu_sf, dn_codes, dn_sf
+    return layer
+
+
+def distinct_experts(m, layer, x):
+    ids, _, _, _ = m.moe_route_topk(x, layer)
+    return int(ids.unique().numel())
+
+
+def gemm_sources_hash():
+    h = hashlib.sha256()
+    for f in ("grouped_gemm.cu", "ptx.cuh", "common.cuh", "kernels.cuh"):
+        with open(os.path.join(ROOT, "nvfp4_w4a4_mixture_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(key):
+    """DRAM bytes per launch from a committed ncu summary, only while the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(key)
+    if not e or e.get("source_hash") != gemm_sources_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ------------------------------------------------------------------------------------------------
+
+class OracleSample:
+    """The oracle layer forward on a few tokens of the workload (inputs from the workload generator;
+    the expert weights the sample routes to are quantised by the oracle itself, untimed)."""
+
+    def __init__(self, c, seed, n_tokens):
+        import numpy as np
+
+        import oracle
+
+        self.oracle = oracle
+        H, E, k, I = c["H"], c["E"], c["k"], c["I"]
+        self.k = k
+        self.x = wl.gen_x(seed, n_tokens, H)
+        self.w_r = wl.gen_router(seed, E, H)
+        b = wl.router_bias(c["router"], E)
+        self.bias = None if b is None else b.astype(np.float32).astype(np.float64)
+        ids, _, _, _ = oracle.router(self.x, self.w_r, k, bias=self.bias)
+        experts = sorted(set(ids.ravel().tolist()) | {E})
+        self.gu = [np.zeros((E + 1, 2 * I, H // 2), np.uint8), np.zeros((E + 1, 2 * I, H // 16), np.uint8),
+                   np.ones((E + 1, 2), np.float32)]
+        self.dn = [np.zeros((E + 1, H, I // 2), np.uint8), np.zeros((E + 1, H, I // 16), np.uint8),
+                   np.ones(E + 1, np.float32)]
+        for e in experts:
+            g, u, d = wl.gen_expert(seed, e, H, I)
+            for h, w in enumerate((g, u)):
+                cc, s, S = oracle.quantize_nvfp4(w)
+                self.gu[0][e, h * I:(h + 1) * I], self.gu[1][e, h * I:(h + 1) * I], self.gu[2][e, h] = cc, s, S
+            cc, s, S = oracle.quantize_nvfp4(d)
+            self.dn[0][e], self.dn[1][e], self.dn[2][e] = cc, s, S
+        self.s_mid = np.full(E + 1, s_mid_value(c), np.float32)
+        self.n_tokens = n_tokens
+        self.cores = oracle.num_threads()
+
+    def run(self, rows=None):
+        x = self.x if rows is None else self.x[rows]
+        self.oracle.layer_forward(x, self.w_r, self.k, self.gu, self.dn, self.s_mid, bias=self.bias)
+        return x.shape[0]
+
+
+def s_mid_value(c):
+    cfg = "tiny" if c["H"] == 256 else "decode"
+    return wl.s_mid_for(cfg)
+
+
+def cpu_baseline(c, seed, budget_s=12.0):
+    n = min(c["T"], 4)
+    smp = OracleSample(c, seed, n)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        done += smp.run()
+        el = time.perf_counter() - t0
+        if el >= budget_s or done >= 64 * n:
+            break
+    return {"value": done / el, "unit": "tokens/s", "cores": smp.cores, "kind": "oracle",
+            "sample": "%d tokens of the workload per oracle call (their %d-expert weights prepared untimed), "
+                      "%d tokens timed over %.1f s" % (n, c["k"] + 1, done, el)}
+
+
+def run_reference(args, c, d):
+    if d.rank != 0:
+        return
+    smp = OracleSample(c, args.seed, min(c["T"], 4))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        smp.run(rows=[i % smp.n_tokens])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1000.0 * statistics.mean(times)
+    value = 1000.0 / ms
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(c, args.config), "sample_per_step": "1 token (its k routed + 1 shared experts)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": smp.cores, "kind": "oracle",
+                             "sample": "1 token per step through the FP64 CPU oracle"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def run_ours(args, c, d):
+    import torch
+
+    import nvfp4_w4a4_mixture_gb300 as m
+    from nvfp4_w4a4_mixture_gb300 import build
+
+    if d.local == 0 or not os.path.exists(m.LIB_PATH):
+        build.build()
+    d.barrier()
+    m.lib()
+    H, E, k, I, T, L = c["H"], c["E"], c["k"], c["I"], c["T"], c["layers"]
+    s_mid = s_mid_value(c)
+    layers = [make_device_layer(m, c, args.seed + 1000 * d.rank, li, s_mid) for li in range(L)]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(12345 + d.rank)
+    x = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16)
+    bufs = [torch.empty(T, H, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ws = m.Workspace(layers[0].workspace_bytes(T))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def forward():
+        cur = x
+        for li, lay in enumerate(layers):
+            o = bufs[li % 2]
+            m.moe_layer_forward(lay, cur, residual=cur if L > 1 else None, out=o, ws=ws)
+            cur = o
+        return cur
+
+    use_graph = not args.no_graph
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        forward()
+        forward()
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    m.moe_read_device_status(ws)
+    if use_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            forward()
+        run = graph.replay
+    else:
+        run = forward
+
+    # ---- timed region: K steps, L2 flushed before each, CUDA events on the launching stream
+    K, W = args.steps, args.warmup
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            flush.zero_()
+            run()
+    torch.cuda.synchronize()
+    d.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(d.local)
+    t_wall = time.perf_counter()
+    torch.cuda.nvtx.range_push("timed")
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.zero_()
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+    t_wall = time.perf_counter() - t_wall
+    d.barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    m.moe_read_device_status(ws)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms_local = statistics.mean(step_ms)
+    ms = d.max(ms_local)
+    value = d.world * T / (ms / 1000.0)
+
+    # ---- per-stage durations of the same launch sequence (CUDA events at the stage boundaries)
+    Kp = min(K, 500)
+    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(Kp)]
+    with torch.cuda.stream(stream):
+        for i in range(Kp):
+            flush.zero_()
+            m.moe_layer_forward_profiled(layers[0], x, st_ev[i], residual=x if L > 1 else None, out=bufs[0], ws=ws)
+    torch.cuda.synchronize()
+    stage_us = {}
+    for j, name in enumerate(m.LAYER_STAGES):
+        stage_us[name] = 1000.0 * statistics.mean(e[j].elapsed_time(e[j + 1]) for e in st_ev)
+
+    # ---- end to end through the public call: pinned host input -> layer -> pinned host output
+    x_h = x.cpu().pin_memory()
+    out_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    Ke = min(K, 1000)
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+    x_dev = torch.empty_like(x)
+    with torch.cuda.stream(stream):
+        for i in range(Ke):
+            flush.zero_()
+            ee[i][0].record(stream)
+            x_dev.copy_(x_h, non_blocking=True)
+            cur = x_dev
+            for li, lay in enumerate(layers):
+                o = bufs[li % 2]
+                m.moe_layer_forward(lay, cur, residual=cur if L > 1 else None, out=o, ws=ws)
+                cur = o
+            out_h.copy_(cur, non_blocking=True)
+            ee[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = d.max(statistics.mean(a.elapsed_time(b) for a, b in ee))
+    m.moe_read_device_status(ws)
+
+    # ---- roofline of the dominant kernel (gate/up GEMM) and of the whole layer
+    hbm, bf16_burst, bf16_sus, peak_src = measured_peaks()
+    U = distinct_experts(m, layers[0], x)  # routed experts touched by this batch
+    per_gu = 2 * I * H // 2 + 2 * I * H // 16 + 8
+    per_dn = H * I // 2 + H * I // 16 + 4
+    P = T * k + T
+    gemm1_bytes = (U + 1) * per_gu + T * H * (1 / 2 + 1 / 16) + P * I * (1 / 2 + 1 / 16)
+    gemm1_us = stage_us["gemm_gate_up"]
+    achieved = gemm1_bytes / (gemm1_us * 1e-6) / 1e9
+    layer_bytes = L * ((U + 1) * (per_gu + per_dn) + (E + 1) * H * 2 + 2 * T * H * 2 + (T * H * 2 if L > 1 else 0))
+    layer_flops = L * 2.0 * T * (k + 1) * 3 * H * I
+    fp4_peak = bf16_burst * FP4_OVER_BF16
+    t_s = ms / 1000.0  # per-replica step time
+    hbm_frac = layer_bytes / t_s / 1e9 / hbm
+    fp4_frac = layer_flops / t_s / 1e12 / fp4_peak
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": d.world, "steps": K, "warmup": W,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
+        "data": "synthetic: seeded torch RNG on the device; x ~ N(0,1) bf16, router N(0,0.02) bf16, experts "
+                "N(0,0.02) fp32 quantised to NVFP4 by the library",
+        "config": {"workload": workload_name(c, args.config), "tokens": T, "layers": L,
+                   "distinct_routed_experts": U, "cuda_graph": use_graph,
+                   "l2": "flushed before every timed step (256 MiB write, outside the timed interval)",
+                   "parallelism": "replicas" if d.world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": recorded_traffic("gemm_gate_up/" + args.config),
+                     "kernel": "k_grouped_gemm_nvf4 (gate/up, fused SwiGLU + NVFP4 requant)",
+                     "algorithmic_bytes_per_launch": gemm1_bytes, "avg_launch_us": gemm1_us,
+                     "peak_source": peak_src + " hbm_gbs"},
+        "layer_roofline": {"bytes": layer_bytes, "flops_fp4": layer_flops, "hbm_frac": hbm_frac,
+                           "fp4_tc_frac": fp4_frac, "fp4_peak_tflops": fp4_peak,
+                           "fp4_peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (peak_src, FP4_OVER_BF16)},
+        "stages_us": stage_us,
+        "step_ms_median": statistics.median(step_ms),
+        "e2e": {"value": d.world * T / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms, "cuda_graph": False},
+        "gpu_launches": K * L * 10,
+        "clocks": clk,
+    }
+    return line
+
+
+def main():
+    args = parse_args()
+    c = wl.CONFIGS[args.config]
+    d = Dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, c, d)
+            return
+        line = run_ours(args, c, d)
+        if d.rank == 0:
+            if not args.no_cpu_baseline and d.world == 1:
+                line["cpu_baseline"] = cpu_baseline(c, args.seed)
+            print(json.dumps(line), flush=True)
+    finally:
+        d.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -16,7 +16,7 @@ EPI_F32, EPI_BF16, EPI_SWIGLU_NVFP4 = 0, 1, 2
 
 ENTRY_POINTS = (
     "moe_quantize_nvfp4", "moe_quantize_nvfp4_f32", "moe_route_topk", "moe_permute", "moe_prepack_nvfp4",
-    "moe_grouped_gemm_nvfp4", "moe_combine", "moe_layer_forward", "moe_workspace_bytes",
+    "moe_grouped_gemm_nvfp4", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled", "moe_workspace_bytes",
     "moe_read_device_status", "moe_status_string", "moe_last_error_detail",
 )
 
@@ -73,6 +73,9 @@ def lib():
         L.moe_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.moe_layer_forward.restype = i32
         L.moe_layer_forward.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp]
+        L.moe_layer_forward_profiled.restype = i32
+        L.moe_layer_forward_profiled.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp,
+                                                 ctypes.POINTER(vp), i32]
         _lib = L
     return _lib
 
@@ -132,13 +135,19 @@ def _bf16_bits(t):
     return t
 
 
-def moe_quantize_nvfp4(x, s_in=None, ws=None):
-    """x: bf16 or fp32 [rows, K] CUDA tensor -> (codes u8 [rows, K/2], sf u8 [rows, K/16], S f32 [1])."""
+def moe_quantize_nvfp4(x, s_in=None, ws=None, out=None):
+    """x: bf16 or fp32 [rows, K] CUDA tensor -> (codes u8 [rows, K/2], sf u8 [rows, K/16], S f32 [1]).
+    out: optional preallocated (codes, sf, s) contiguous views to write into."""
     assert x.is_cuda and x.is_contiguous() and x.dim() == 2
     rows, K = x.shape
-    codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
-    sf = torch.empty(rows, K // 16, dtype=torch.uint8, device=x.device)
-    s_out = torch.empty(1, dtype=torch.float32, device=x.device)
+    if out is None:
+        codes = torch.empty(rows, K // 2, dtype=torch.uint8, device=x.device)
+        sf = torch.empty(rows, K // 16, dtype=torch.uint8, device=x.device)
+        s_out = torch.empty(1, dtype=torch.float32, device=x.device)
+    else:
+        codes, sf, s_out = out
+        assert codes.is_contiguous() and sf.is_contiguous() and codes.numel() == rows * K // 2
+        assert sf.numel() == rows * K // 16
     ws = ws or _ws(4096)
     f = lib().moe_quantize_nvfp4 if x.dtype == torch.bfloat16 else lib().moe_quantize_nvfp4_f32
     if x.dtype not in (torch.bfloat16, torch.float32):
@@ -253,4 +262,23 @@ def moe_layer_forward(layer, x, residual=None, out=None, ws=None):
     ws = ws or _ws(layer.workspace_bytes(T))
     _check(lib().moe_layer_forward(ctypes.byref(layer.desc), _p(_bf16_bits(x)), T, _p(residual), _p(out), ws.ptr,
                                    ws.nbytes, _stream()))
+    return out
+
+
+LAYER_STAGES = ("quantize", "route", "permute", "gemm_gate_up", "gemm_down", "combine")
+
+
+def moe_layer_forward_profiled(layer, x, events, residual=None, out=None, ws=None):
+    """moe_layer_forward recording 7 torch.cuda.Event objects (already created, enable_timing) at the
+    stage boundaries of LAYER_STAGES."""
+    T = x.shape[0]
+    if out is None:
+        out = torch.empty(T, layer.H, dtype=torch.bfloat16, device=x.device)
+    ws = ws or _ws(layer.workspace_bytes(T))
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(lib().moe_layer_forward_profiled(ctypes.byref(layer.desc), _p(_bf16_bits(x)), T, _p(residual), _p(out),
+                                            ws.ptr, ws.nbytes, _stream(), handles, len(events)))
     return out

@@ -15,6 +15,7 @@ namespace moe {
 namespace {
 
 thread_local std::string g_detail;
+constexpr int kLayerStageEvents = 7;
 
 moe_status_t fail(moe_status_t s, const char* fmt, ...)
 {
@@ -343,9 +344,15 @@ moe_status_t moe_combine(const uint16_t* y, const float* topk_w, const float* sh
     return MOE_OK;
 }
 
-moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual, uint16_t* out,
-                               void* ws, size_t ws_bytes, moe_stream_t stream)
+moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
+                                        uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream,
+                                        void* const* events, int n_events)
 {
+    if (n_events != 0 && n_events != kLayerStageEvents)
+        return fail(MOE_ERR_INVALID_ARG, "n_events=%d: pass 0 or %d events", n_events, kLayerStageEvents);
+    if (n_events && !events) return fail(MOE_ERR_INVALID_ARG, "events is NULL");
+    for (int i = 0; i < n_events; ++i)
+        if (!events[i]) return fail(MOE_ERR_INVALID_ARG, "events[%d] is NULL", i);
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     const int H = L->H, E = L->E, k = L->k, I = L->I;
     MOE_TRY(check_layer_shape(H, E, k, I));
@@ -369,16 +376,23 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int sms = device_sm_count();
     const int64_t P = static_cast<int64_t>(T) * k + T;
+    auto mark = [&](int i) -> cudaError_t {
+        return n_events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+    };
 
+    MOE_CUDA(mark(0), "event record");
     // W4A4: quantize the layer input once per token (dynamic tensor scale)
     MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s), "quantize");
+    MOE_CUDA(mark(1), "event record");
     // router, softmax, top-k, shared gate
     MOE_CUDA(launch_router_logits(x, T, H, E, L->w_router, L->logit_bias, PF(W.logits), s), "router");
     MOE_CUDA(launch_topk(PF(W.logits), T, E, k, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), nullptr, s), "top-k");
+    MOE_CUDA(mark(2), "event record");
     // permutation by expert id, the shared expert appended as group E
     MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), P32(W.tile_off), P32(W.perm_src),
                             P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
              "permute");
+    MOE_CUDA(mark(3), "event record");
     // gate/up GEMM with the fused SwiGLU + NVFP4 requantisation
     GemmArgs g1{};
     g1.a_codes = P8(W.x_codes);
@@ -400,6 +414,7 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
     g1.out_sf = P8(W.h_sf);
     g1.status = &hdr->status;
     MOE_CUDA(launch_grouped_gemm(g1, P, sms, s), "gate/up GEMM");
+    MOE_CUDA(mark(4), "event record");
     // down GEMM, bf16 rows in permuted order
     GemmArgs g2 = g1;
     g2.a_codes = P8(W.h_codes);
@@ -418,11 +433,19 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
     g2.out = base + W.y;
     g2.out_sf = nullptr;
     MOE_CUDA(launch_grouped_gemm(g2, P, sms, s), "down GEMM");
+    MOE_CUDA(mark(5), "event record");
     // weighted combine (+ residual)
     MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), P32(W.src_perm), T,
                             k, H, residual, out, s),
              "combine");
+    MOE_CUDA(mark(6), "event record");
     return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual, uint16_t* out,
+                               void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    return moe_layer_forward_profiled(L, x, T, residual, out, ws, ws_bytes, stream, nullptr, 0);
 }
 
 }  // extern "C"
