@@ -197,6 +197,14 @@ def make_device_layer(m, c, seed, layer_idx, s_mid):
     return layer
 
 
+def launches_per_layer(c):
+    """Kernels of the library launched by one layer forward (see csrc/api.cu)."""
+    T, H, k = c["T"], c["H"], c["k"]
+    quant = 1 if T * H // 16 <= 4096 else 2
+    perm = 1 if T * k <= 512 else 3
+    return quant + 2 + perm + 2 + 1  # quantize, logits + top-k, permute, two GEMMs, combine
+
+
 def distinct_experts(m, layer, x):
     ids, _, _, _ = m.moe_route_topk(x, layer)
     return int(ids.unique().numel())
@@ -457,7 +465,7 @@ def run_ours(args, c, d):
         "step_ms_median": statistics.median(step_ms),
         "e2e": {"value": d.world * T / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms, "cuda_graph": False},
-        "gpu_launches": K * L * 10,
+        "gpu_launches": K * L * launches_per_layer(c),
         "clocks": clk,
     }
     return line

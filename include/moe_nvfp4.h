@@ -79,11 +79,15 @@ typedef struct {
     const float* s_mid;         /* FP32 [E+1]: static tensor scale of the intermediate h per expert */
 } moe_layer_t;
 
-/* Epilogues of moe_grouped_gemm_nvfp4. */
+/* Epilogues of moe_grouped_gemm_nvfp4, optionally OR-ed with one schedule flag. */
 enum {
     MOE_EPI_F32 = 0,         /* out: FP32 [P][N] */
     MOE_EPI_BF16 = 1,        /* out: bf16 [P][N] */
-    MOE_EPI_SWIGLU_NVFP4 = 2 /* gate/up bank; out: h codes [P][N/4], out_sf [P][N/32], scale epi_scale[g] */
+    MOE_EPI_SWIGLU_NVFP4 = 2, /* gate/up bank; out: h codes [P][N/4], out_sf [P][N/32], scale epi_scale[g] */
+    /* Tile schedule (default: weights on M when p_max <= 64, else activations on M). Results agree
+     * to FP32 summation order. */
+    MOE_GEMM_SCHED_ACT_ON_M = 0x100,     /* 128 token rows x 128 weight rows per tile */
+    MOE_GEMM_SCHED_WEIGHTS_ON_M = 0x200  /* 128 weight rows x 32 token rows per tile (small groups) */
 };
 
 /* ---------------------------------------------------------------------------------------------
@@ -158,7 +162,7 @@ moe_status_t moe_prepack_nvfp4(const uint8_t* codes, const uint8_t* sf, int G, i
  *   gate_up: 1 when b is a gate/up bank (nscale 2, interleaved prepack), 0 for a plain bank.
  *   N % 128 == 0, K % 64 == 0, K <= 16384. P = group_offsets[G] (read on the device);
  *   p_max: an upper bound of P that the host knows (sizes the grid).
- *   ws: >= moe_workspace_bytes(..).
+ *   ws: >= 256 bytes (status word).
  * ------------------------------------------------------------------------------------------- */
 moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_scale,
                                     int a_scale_per_group, const int32_t* a_row_index,

@@ -13,6 +13,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_nvfp4.so")
 
 EPI_F32, EPI_BF16, EPI_SWIGLU_NVFP4 = 0, 1, 2
+SCHED_AUTO, SCHED_ACT_ON_M, SCHED_WEIGHTS_ON_M = 0, 0x100, 0x200
 
 ENTRY_POINTS = (
     "moe_quantize_nvfp4", "moe_quantize_nvfp4_f32", "moe_route_topk", "moe_permute", "moe_prepack_nvfp4",
@@ -224,7 +225,7 @@ def moe_permute(topk_ids, E, with_shared=True, ws=None):
 
 
 def moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, group_offsets, p_max, b_codes, b_sf, b_scale, N, K, gate_up,
-                           epilogue, a_row_index=None, epi_scale=None, ws=None):
+                           epilogue, a_row_index=None, epi_scale=None, ws=None, schedule=SCHED_AUTO):
     """Grouped GEMM over a prepacked bank. Returns out (and out_sf for the SwiGLU epilogue)."""
     G = group_offsets.numel() - 1
     dev = a_codes.device
@@ -241,7 +242,8 @@ def moe_grouped_gemm_nvfp4(a_codes, a_sf, a_scale, group_offsets, p_max, b_codes
     ws = ws or _ws(256 + 4 * (G + 1) + 4096)
     per_group = int(a_scale.numel() > 1)
     _check(lib().moe_grouped_gemm_nvfp4(_p(a_codes), _p(a_sf), _p(a_scale), per_group, _p(a_row_index),
-                                        _p(group_offsets), G, P, ctypes.byref(bank), N, K, int(gate_up), epilogue,
+                                        _p(group_offsets), G, P, ctypes.byref(bank), N, K, int(gate_up),
+                                        epilogue | schedule,
                                         _p(epi_scale), _p(out), _p(out_sf), ws.ptr, ws.nbytes, _stream()))
     return (out, out_sf) if epilogue == EPI_SWIGLU_NVFP4 else out
 

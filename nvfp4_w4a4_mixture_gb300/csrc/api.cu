@@ -55,7 +55,7 @@ moe_status_t check_device()
 }
 
 struct WsLayout {
-    size_t hdr, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, tile_off, perm_src, src_perm, row_token,
+    size_t hdr, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, perm_src, src_perm, row_token,
         hist, h_codes, h_sf, y, total;
 };
 
@@ -77,7 +77,6 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     L.x_codes = take(T * H / 2);
     L.x_sf = take(T * H / 16);
     L.offsets = take((E + 2) * 4);
-    L.tile_off = take((E + 2) * 4);
     L.perm_src = take(n * 4);
     L.src_perm = take(n * 4);
     L.row_token = take(P * 4);
@@ -293,6 +292,12 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     if (N < 128 || N % 128 || K < 64 || K % 64 || K > 16384)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d: N must be a multiple of 128, K of 64 (<= 16384)", N, K);
     if (p_max < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "p_max=%lld < 0", (long long)p_max);
+    const int sched_bits = epilogue & (MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M);
+    if (sched_bits == (MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M))
+        return fail(MOE_ERR_INVALID_ARG, "epilogue=0x%x: pick one schedule flag", epilogue);
+    const int schedule = sched_bits == MOE_GEMM_SCHED_ACT_ON_M ? kSchedActOnM
+                         : sched_bits == MOE_GEMM_SCHED_WEIGHTS_ON_M ? kSchedWeightsOnM : kSchedAuto;
+    epilogue &= ~(MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M);
     if (epilogue < MOE_EPI_F32 || epilogue > MOE_EPI_SWIGLU_NVFP4) return fail(MOE_ERR_INVALID_ARG, "epilogue=%d", epilogue);
     if (epilogue == MOE_EPI_SWIGLU_NVFP4 && (!gate_up || !epi_scale || !out_sf))
         return fail(MOE_ERR_INVALID_ARG, "the SwiGLU epilogue needs a gate/up bank, epi_scale and out_sf");
@@ -300,13 +305,10 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     if (!aligned(a_codes, 16) || !aligned(a_sf, 4) || !aligned(out, 16) || (out_sf && !aligned(out_sf, 4)))
         return fail(MOE_ERR_MISALIGNED, "a_codes / out must be 16-byte, a_sf / out_sf 4-byte aligned");
     MOE_TRY(check_bank(b, "b"));
-    const size_t need = 256 + ((static_cast<size_t>(G + 1) * 4 + 255) & ~size_t(255));
-    MOE_TRY(check_ws(ws, ws_bytes, need));
+    MOE_TRY(check_ws(ws, ws_bytes, sizeof(WsHeader)));
     MOE_TRY(check_device());
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
-    int32_t* tile_off = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
-    MOE_CUDA(launch_tile_offsets(group_offsets, G, tile_off, s), "tile offsets launch");
     GemmArgs ga{};
     ga.a_codes = a_codes;
     ga.a_sf = a_sf;
@@ -314,7 +316,6 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     ga.a_scale_per_group = a_scale_per_group ? 1 : 0;
     ga.a_row = a_row_index;
     ga.offsets = group_offsets;
-    ga.tile_off = tile_off;
     ga.G = G;
     ga.b_codes = b->codes;
     ga.b_sf = b->sf;
@@ -327,7 +328,7 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     ga.out = out;
     ga.out_sf = out_sf;
     ga.status = &hdr->status;
-    MOE_CUDA(launch_grouped_gemm(ga, p_max, device_sm_count(), s), "grouped GEMM launch");
+    MOE_CUDA(launch_grouped_gemm(ga, p_max, schedule, device_sm_count(), s), "grouped GEMM launch");
     return MOE_OK;
 }
 
@@ -389,7 +390,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     MOE_CUDA(launch_topk(PF(W.logits), T, E, k, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), nullptr, s), "top-k");
     MOE_CUDA(mark(2), "event record");
     // permutation by expert id, the shared expert appended as group E
-    MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), P32(W.tile_off), P32(W.perm_src),
+    MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), nullptr, P32(W.perm_src),
                             P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
              "permute");
     MOE_CUDA(mark(3), "event record");
@@ -400,7 +401,6 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     g1.a_scale = &hdr->s_x;
     g1.a_row = P32(W.row_token);
     g1.offsets = P32(W.offsets);
-    g1.tile_off = P32(W.tile_off);
     g1.G = E + 1;
     g1.b_codes = L->w_gate_up.codes;
     g1.b_sf = L->w_gate_up.sf;
@@ -413,7 +413,9 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     g1.out = P8(W.h_codes);
     g1.out_sf = P8(W.h_sf);
     g1.status = &hdr->status;
-    MOE_CUDA(launch_grouped_gemm(g1, P, sms, s), "gate/up GEMM");
+    // few rows per expert (decode): weights on the MMA's M side; otherwise activations on M
+    const int sched = static_cast<int64_t>(T) * k <= 16LL * E ? kSchedWeightsOnM : kSchedActOnM;
+    MOE_CUDA(launch_grouped_gemm(g1, P, sched, sms, s), "gate/up GEMM");
     MOE_CUDA(mark(4), "event record");
     // down GEMM, bf16 rows in permuted order
     GemmArgs g2 = g1;
@@ -432,7 +434,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     g2.epi_scale = nullptr;
     g2.out = base + W.y;
     g2.out_sf = nullptr;
-    MOE_CUDA(launch_grouped_gemm(g2, P, sms, s), "down GEMM");
+    MOE_CUDA(launch_grouped_gemm(g2, P, sched, sms, s), "down GEMM");
     MOE_CUDA(mark(5), "event record");
     // weighted combine (+ residual)
     MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), P32(W.src_perm), T,

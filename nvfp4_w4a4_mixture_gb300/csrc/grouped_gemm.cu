@@ -1,318 +1,540 @@
 // grouped_gemm.cu -- block-scaled NVFP4 grouped GEMM on the 5th-generation tensor cores.
 //
-// One persistent CTA per SM walks a list of 128 x 128 output tiles (group, M-tile, N-tile),
-// N-tile fastest so that consecutive CTAs share the same gathered activation rows and the same
-// expert's weights stay hot in L2. Warp roles (256 threads):
-//   warp 0     B producer: TMA of the expert's weight codes (128 rows x 128 bytes, 128-byte swizzle)
-//              and one bulk copy of the matching scale-factor tiles, per K-stage of 256 elements;
-//   warp 1     TMEM owner and MMA issuer: per stage, tcgen05.cp of the scale factors into tensor
-//              memory, then 4 x tcgen05.mma kind::mxf4nvf4 (M = 128, N = 128, K = 64) into an FP32
-//              accumulator in TMEM (two accumulator buffers);
-//   warps 2-3  A producers: gather the activation rows of the tile (row index list) with
-//              cp.async into the swizzled layout, and their scale factors into tile layout;
-//   warps 4-7  epilogue: tcgen05.ld the accumulator (one 32-lane quarter per warp), apply the
-//              tensor scales and write FP32 / bf16 rows, or SwiGLU + NVFP4 requantisation.
-// Stages are handed over with mbarriers (full: producers -> MMA; empty: MMA commit ->
-// producers; acc_full / acc_empty: MMA <-> epilogue). Every wait is bounded (ptx::mbar_wait): on
-// timeout the CTA records kDevTimeoutGemm in the status word, stops all roles and frees TMEM.
+// out[p][n] = a_scale * b_scale[g] * sum_k act[src(p)][k] * w[g][n][k] for the rows p of group g,
+// computed by tcgen05.mma kind::mxf4nvf4 (E2M1 x E2M1 products, one UE4M3 scale per 16 along K,
+// FP32 accumulation in tensor memory).
+//
+// One persistent CTA per SM walks a list of output tiles (token block of a group, 128 weight rows),
+// weight blocks fastest, so consecutive CTAs share the token block's activation rows and one
+// expert's weights stay in L2 across its token blocks. Two schedules:
+//   activations on M (large groups): 128 token rows x 128 weight rows per tile, MMA 128 x 128;
+//   weights on M (small groups, "swap"): 128 weight rows x 32 token rows per tile, MMA 128 x 32, so a
+//     decode step with one or two tokens per expert does not pay for 128-row tiles.
+// Warp roles:
+//   warp 0       weight producer: TMA of the 128 x 128-byte weight box (128-byte swizzle) and one
+//                bulk copy of its scale-factor tiles, per K-stage of 256 elements;
+//   warp 1       TMEM owner and MMA issuer: per stage, tcgen05.cp of both scale-factor sets into
+//                tensor memory, then 4 x tcgen05.mma (K = 64 each) into a double-buffered accumulator;
+//   warps 2-3    activation producers: gather the tile's activation rows (row index list) with
+//                cp.async into the swizzled layout, and their scale factors into tile layout;
+//   warps 4..    epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31), apply
+//                the tensor scales and write FP32 / bf16 rows, or SwiGLU + NVFP4 requantisation.
+// Stage hand-over uses mbarriers (full: producers -> MMA; empty: MMA commit -> producers;
+// acc_full / acc_empty: MMA <-> epilogue). Every wait is bounded (ptx::mbar_wait): on timeout the
+// CTA records kDevTimeoutGemm in the status word, all roles stop, and TMEM is freed after the
+// tensor cores drain.
 #include "kernels.cuh"
 
 namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 128;
-constexpr int BK_BYTES = 128;                 // one swizzle row = 256 E2M1 values
-constexpr int STAGES = 6;
-constexpr int THREADS = 256;
-constexpr int A_BYTES = BM * BK_BYTES;        // 16 KiB
-constexpr int B_BYTES = BN * BK_BYTES;        // 16 KiB
-constexpr int SF_BYTES = 4 * 512;             // 4 scale tiles (K = 4 x 64)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + 2 * SF_BYTES;
-constexpr int TMEM_COLS = 512;
-constexpr int ACC_COL = 0;                    // accumulators: columns [0, 256), 2 x 128
-constexpr int SF_COL = 256;                   // scale factors: 32 columns per stage
-constexpr int kNumAProducers = 64;
+constexpr int BK_BYTES = 128;              // K-stage: one 128-byte swizzle row = 256 E2M1 values
+constexpr int W_ROWS = 128;                // weight rows per tile (one TMA box)
+constexpr int SF_TILE = 512;               // scale factors of 128 rows x 4 K-blocks
+constexpr int SF_STAGE = 4 * SF_TILE;      // 4 MMA K-steps of 64 per stage
+constexpr int kNumActProducers = 64;  // warps 2-3; each arrives on every stage's full barrier
 
-struct SmemTail {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+template <bool kSwap>
+struct Cfg;
+template <>
+struct Cfg<false> {                        // activations on the MMA's M side
+    static constexpr int ACT_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128;
+    static constexpr int MMA_M = 128, MMA_N = 128;
+};
+template <>
+struct Cfg<true> {                         // weights on the MMA's M side
+    static constexpr int ACT_ROWS = 32, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32;
+    static constexpr int MMA_M = 128, MMA_N = 32;
+};
+
+template <bool kSwap>
+struct Lay {
+    using C = Cfg<kSwap>;
+    static constexpr int W_BYTES = W_ROWS * BK_BYTES;
+    static constexpr int ACT_BYTES = C::ACT_ROWS * BK_BYTES;
+    static constexpr int OFF_W = 0, OFF_ACT = W_BYTES, OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + SF_STAGE;
+    static constexpr int STAGE_BYTES = OFF_SFACT + SF_STAGE;
+    static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
+    static constexpr int SF_COL = 2 * C::ACC_COLS;  // first scale-factor column; 32 per stage
+    static constexpr int TMEM_COLS = 512;
+    static_assert(SF_COL + 32 * C::STAGES <= TMEM_COLS, "tensor memory budget");
+    static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
+};
+
+template <bool kSwap>
+struct Tail {
+    uint64_t full[Cfg<kSwap>::STAGES];
+    uint64_t empty[Cfg<kSwap>::STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t xchg_full;   // weights-on-M SwiGLU: up values written (64 arrivals)
+    uint64_t xchg_empty;  // weights-on-M SwiGLU: up values consumed (64 arrivals)
     uint32_t tmem_base;
     int abort;
-    int32_t tile_off[kGemmMaxG + 1];
+    int32_t wsum[32];
+    int32_t tb_off[kGemmMaxG + 1];
 };
 
-constexpr size_t kSmemBytes = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(SmemTail);
+// up-projection values handed from TMEM lanes 64..127 to lanes 0..63 (weights-on-M SwiGLU)
+struct SwapXchg {
+    float u[64][33];
+};
+
+template <bool kSwap>
+constexpr size_t smem_bytes()
+{
+    return 1024 + static_cast<size_t>(Cfg<kSwap>::STAGES) * Lay<kSwap>::STAGE_BYTES + sizeof(Tail<kSwap>) +
+           (kSwap ? sizeof(SwapXchg) : 0);
+}
 
 struct TileInfo {
-    int g, nt, row0, rows;
+    int g, nb, row0, rows;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const SmemTail& t, const GemmArgs& a, int n_tiles, int L)
+// tb_off[g] = sum_{g' < g} ceil(rows_g' / act_rows), g = 0..G (block-wide scan; contains barriers)
+__device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, int act_rows, int32_t* tb_off,
+                                  int32_t* wsum)
 {
-    const int mtg = L / n_tiles;
+    const int nt = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = nt >> 5;
+    const int per = (G + nt - 1) / nt;
+    const int g0 = min(G, t * per), g1 = min(G, g0 + per);
+    int32_t s = 0;
+    for (int g = g0; g < g1; ++g) {
+        const int32_t r = __ldg(offsets + g + 1) - __ldg(offsets + g);
+        s += r > 0 ? (r + act_rows - 1) / act_rows : 0;
+    }
+    int32_t x = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = lane < nwarps ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < nwarps) wsum[lane] = w;
+    }
+    __syncthreads();
+    int32_t run = x - s + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int g = g0; g < g1; ++g) {
+        tb_off[g] = run;
+        const int32_t r = __ldg(offsets + g + 1) - __ldg(offsets + g);
+        run += r > 0 ? (r + act_rows - 1) / act_rows : 0;
+    }
+    if (t == nt - 1) tb_off[G] = wsum[nwarps - 1];
+    __syncthreads();
+}
+
+__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmArgs& a, int n_wb, int act_rows, int L)
+{
+    const int tbg = L / n_wb;
     TileInfo ti;
-    ti.nt = L - mtg * n_tiles;
-    // largest g with tile_off[g] <= mtg (groups with no tiles have tile_off[g] == tile_off[g+1])
-    int lo = 0, hi = a.G;  // invariant: tile_off[lo] <= mtg < tile_off[hi]
+    ti.nb = L - tbg * n_wb;
+    int lo = 0, hi = a.G;  // tb_off[lo] <= tbg < tb_off[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (t.tile_off[mid] <= mtg) lo = mid; else hi = mid;
+        if (tb_off[mid] <= tbg) lo = mid; else hi = mid;
     }
     ti.g = lo;
-    const int mt = mtg - t.tile_off[lo];
     const int g0 = __ldg(a.offsets + lo), g1 = __ldg(a.offsets + lo + 1);
-    ti.row0 = g0 + mt * BM;
-    ti.rows = min(BM, g1 - ti.row0);
+    ti.row0 = g0 + (tbg - tb_off[lo]) * act_rows;
+    ti.rows = min(act_rows, g1 - ti.row0);
     return ti;
 }
 
-__device__ __forceinline__ void set_abort(SmemTail& t, int* status)
+template <bool kSwap>
+__device__ __forceinline__ void set_abort(Tail<kSwap>& t, int* status)
 {
     if (atomicExch(&t.abort, 1) == 0) record_status(status, kDevTimeoutGemm);
 }
 
-__device__ __forceinline__ bool aborted(const SmemTail& t) { return *reinterpret_cast<const volatile int*>(&t.abort) != 0; }
+template <bool kSwap>
+__device__ __forceinline__ bool aborted(const Tail<kSwap>& t)
+{
+    return *reinterpret_cast<const volatile int*>(&t.abort) != 0;
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// NVFP4 encoding of the intermediate h (16 values, static tensor scale S): the same rule as the
+// activation quantizer, with the two divisions replaced by multiplications with correctly rounded
+// reciprocals (the requantised intermediate is compared by agreement rate, not bit for bit).
+__device__ __forceinline__ uint32_t encode16_rcp(const float (&v)[16], float S, float inv_six_s, uint32_t& lo,
+                                                 uint32_t& hi)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const uint32_t sf = ptx::cvt_e4m3x2(amax * inv_six_s, 0.0f) & 0xFFu;
+    const float dsf = ue4m3_to_f32(sf);
+    lo = 0u;
+    hi = 0u;
+    if (dsf != 0.0f) {
+        const float r = __frcp_rn(dsf * S);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            lo |= ptx::cvt_e2m1x2(v[i] * r, v[i + 1] * r) << (4 * i);
+            hi |= ptx::cvt_e2m1x2(v[8 + i] * r, v[8 + i + 1] * r) << (4 * i);
+        }
+    }
+    return sf;
+}
 
 }  // namespace
 
-__global__ void __launch_bounds__(THREADS, 1)
-    k_grouped_gemm_nvf4(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs a)
+template <bool kSwap>
+__global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
+    k_grouped_gemm_nvf4(const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a)
 {
+    using C = Cfg<kSwap>;
+    using LY = Lay<kSwap>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + STAGES * STAGE_BYTES);
+    Tail<kSwap>& st = *reinterpret_cast<Tail<kSwap>*>(smem + C::STAGES * LY::STAGE_BYTES);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
     // ---- setup
-    for (int i = tid; i <= a.G; i += THREADS) st.tile_off[i] = __ldg(a.tile_off + i);
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(&st.full[s], 1 + kNumAProducers);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(&st.full[s], 1 + kNumActProducers);
             ptx::mbar_init(&st.empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&st.acc_full[s], 1);
-            ptx::mbar_init(&st.acc_empty[s], 128);
+            ptx::mbar_init(&st.acc_empty[s], 32 * C::EPI_WARPS);
         }
         ptx::mbar_init(&st.drain, 1);
+        ptx::mbar_init(&st.xchg_full, 64);
+        ptx::mbar_init(&st.xchg_empty, 64);
         st.abort = 0;
         ptx::fence_mbar_init();
-        ptx::prefetch_tmap(&tmap_b);
+        ptx::prefetch_tmap(&tmap_w);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(&st.tmem_base, TMEM_COLS);
+        ptx::tmem_alloc(&st.tmem_base, LY::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    block_tile_prefix(a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.wsum);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = st.tmem_base;
 
-    const int n_tiles = a.N / BN;
-    const int total = st.tile_off[a.G] * n_tiles;
+    const int n_wb = a.N / W_ROWS;
+    const int total = st.tb_off[a.G] * n_wb;
     const int k_stages = (a.K + 255) / 256;
     const int k_blocks64 = a.K / 64;
     const int64_t a_ld = a.K / 2, sf_ld = a.K / 16;
 
     if (warp == 0) {
-        // ================================ B producer
+        // ================================ weight producer
         if (lane == 0) {
-            uint32_t it = 0;
-            for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x) {
-                const TileInfo ti = tile_info(st, a, n_tiles, L);
-                const uint8_t* sf_base =
-                    a.b_sf + ((static_cast<int64_t>(ti.g) * (a.N / 128) + ti.nt) * k_blocks64) * 512;
-                for (int kt = 0; kt < k_stages; ++kt, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); break; }
-                    uint8_t* sbase = smem + s * STAGE_BYTES;
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
+                const TileInfo ti = tile_info(st.tb_off, a, n_wb, C::ACT_ROWS, L);
+                const uint8_t* sf_src = a.b_sf + ((static_cast<int64_t>(ti.g) * n_wb + ti.nb) * k_blocks64) * SF_TILE;
+                const int row = ti.nb * W_ROWS;
+                for (int kt = 0; kt < k_stages; ++kt) {
+                    if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                    uint8_t* sbase = smem + s * LY::STAGE_BYTES;
                     const int nat = min(4, k_blocks64 - kt * 4);
-                    ptx::mbar_arrive_expect_tx(&st.full[s], B_BYTES + nat * 512);
-                    ptx::tma_load_3d(sbase + A_BYTES, &tmap_b, &st.full[s], kt * BK_BYTES, ti.nt * BN, ti.g);
-                    ptx::bulk_load(sbase + A_BYTES + B_BYTES + SF_BYTES, sf_base + static_cast<int64_t>(kt) * 4 * 512,
-                                   nat * 512, &st.full[s]);
+                    ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + nat * SF_TILE);
+                    ptx::tma_load_3d(sbase + LY::OFF_W, &tmap_w, &st.full[s], kt * BK_BYTES, row, ti.g);
+                    ptx::bulk_load(sbase + LY::OFF_SFW, sf_src, nat * SF_TILE, &st.full[s]);
+                    sf_src += 4 * SF_TILE;
+                    if (++s == C::STAGES) { s = 0; ph ^= 1; }
                 }
             }
         }
     } else if (warp == 1) {
         // ================================ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_nvf4(BM, BN);
-            uint32_t it = 0, lt = 0;
-            for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x, ++lt) {
+            const uint32_t idesc = ptx::idesc_nvf4(C::MMA_M, C::MMA_N);
+            // descriptors of stage 0; stage s adds s * STAGE_BYTES to the start address field and
+            // K-step kk adds 32 bytes (operands) or one 512-byte scale tile
+            const uint32_t s0 = ptx::smem_u32(smem);
+            const uint64_t dw0 = ptx::sdesc_sw128(s0 + LY::OFF_W), dact0 = ptx::sdesc_sw128(s0 + LY::OFF_ACT);
+            const uint64_t dsfw0 = ptx::sdesc_sf(s0 + LY::OFF_SFW), dsfact0 = ptx::sdesc_sf(s0 + LY::OFF_SFACT);
+            constexpr uint64_t kStageAdv = LY::STAGE_BYTES >> 4, kOpAdv = 32 >> 4, kSfAdv = SF_TILE >> 4;
+            int s = 0;
+            uint32_t ph = 0, lt = 0;
+            bool ok = true;
+            for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x, ++lt) {
                 const uint32_t as = lt & 1, aph = (lt >> 1) & 1;
                 if (!ptx::mbar_wait(&st.acc_empty[as], aph ^ 1)) { set_abort(st, a.status); break; }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem + ACC_COL + as * BN;
-                for (int kt = 0; kt < k_stages; ++kt, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1;
-                    if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); break; }
-                    ptx::tc_fence_after();
-                    uint8_t* sbase = smem + s * STAGE_BYTES;
-                    const uint32_t sa = ptx::smem_u32(sbase), sb = ptx::smem_u32(sbase + A_BYTES);
-                    const uint32_t ssfa = ptx::smem_u32(sbase + A_BYTES + B_BYTES);
-                    const uint32_t ssfb = ssfa + SF_BYTES;
-                    const uint32_t tsfa = tmem + SF_COL + s * 32, tsfb = tsfa + 16;
+                const uint32_t d_tmem = tmem + as * C::ACC_COLS;
+                uint32_t acc = 0;
+                for (int kt = 0; kt < k_stages; ++kt) {
+                    if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
+                    const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
+                    const uint32_t tsfw = tmem + LY::SF_COL + s * 32, tsfact = tsfw + 16;
                     const int nk = min(4, k_blocks64 - kt * 4);
                     for (int kk = 0; kk < nk; ++kk) {
-                        ptx::tmem_cp_32x128b_x4(tsfa + kk * 4, ptx::sdesc_sf(ssfa + kk * 512));
-                        ptx::tmem_cp_32x128b_x4(tsfb + kk * 4, ptx::sdesc_sf(ssfb + kk * 512));
-                        ptx::mma_nvf4(d_tmem, ptx::sdesc_sw128(sa + kk * 32), ptx::sdesc_sw128(sb + kk * 32), idesc,
-                                      tsfa + kk * 4, tsfb + kk * 4, (kt | kk) != 0);
+                        ptx::tmem_cp_32x128b_x4(tsfw + kk * 4, dsfw0 + so + kk * kSfAdv);
+                        ptx::tmem_cp_32x128b_x4(tsfact + kk * 4, dsfact0 + so + kk * kSfAdv);
+                        const uint64_t dw = dw0 + so + kk * kOpAdv, dact = dact0 + so + kk * kOpAdv;
+                        if (kSwap)
+                            ptx::mma_nvf4(d_tmem, dw, dact, idesc, tsfw + kk * 4, tsfact + kk * 4, acc);
+                        else
+                            ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsfact + kk * 4, tsfw + kk * 4, acc);
+                        acc = 1;
                     }
                     ptx::tc_commit(&st.empty[s]);
+                    if (++s == C::STAGES) { s = 0; ph ^= 1; }
                 }
-                if (aborted(st)) break;
+                if (!ok) break;
                 ptx::tc_commit(&st.acc_full[as]);
             }
-            // wait until every issued tensor-core operation has finished before TMEM is freed
+            // every issued tensor-core operation finishes before TMEM is freed
             ptx::tc_commit(&st.drain);
             if (!ptx::mbar_wait(&st.drain, 0)) set_abort(st, a.status);
         }
     } else if (warp < 4) {
-        // ================================ A producers (gather)
-        const int pt = tid - 64;  // 0..63, rows pt and pt + 64
-        uint32_t it = 0;
-        int pending_stage = -1;
-        for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x) {
-            const TileInfo ti = tile_info(st, a, n_tiles, L);
-            int64_t src[2];
-            bool valid[2];
+        // ================================ activation producers (row gather)
+        // Warp w2 = warp - 2 fills rows [w2 * RW, w2 * RW + RW) of the tile. Lanes run along rows:
+        // 8 lanes copy the 8 16-byte chunks of one row's 128-byte K-slice (one cache line), 4 lanes
+        // the 4 scale words of one row, so each warp instruction touches few cache lines.
+        constexpr int RW = C::ACT_ROWS / 2;      // rows per producer warp
+        constexpr int NCR = RW / 4;              // code rows per lane (4 rows per warp instruction)
+        constexpr int NSR = RW / 8;              // scale rows per lane (8 rows per warp instruction)
+        constexpr int LAG = C::STAGES - 2;       // stages in flight before one is published
+        const int w2 = warp - 2;
+        const int chunk = lane & 7, word = lane & 3;
+        const uint8_t* cptr[NCR];
+        const uint8_t* sptr[NSR];
+        uint32_t cvalid = 0, svalid = 0;
+        int s = 0, pub = 0;
+        uint32_t ph = 0, issued = 0;
+        bool ok = true;
+        for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
+            const TileInfo ti = tile_info(st.tb_off, a, n_wb, C::ACT_ROWS, L);
+            // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row
+            int64_t srcv[(RW + 31) / 32];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int r = pt + h * 64;
-                valid[h] = r < ti.rows;
+            for (int h = 0; h < (RW + 31) / 32; ++h) {
+                const int r = w2 * RW + h * 32 + lane;
                 const int64_t p = ti.row0 + r;
-                src[h] = valid[h] ? (a.a_row ? static_cast<int64_t>(__ldg(a.a_row + p)) : p) : 0;
+                srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (a.a_row ? static_cast<int64_t>(__ldg(a.a_row + p)) : p) : -1;
             }
-            bool ok = true;
-            for (int kt = 0; kt < k_stages; ++kt, ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1;
+            cvalid = 0;
+            svalid = 0;
+#pragma unroll
+            for (int i = 0; i < NCR; ++i) {
+                const int rl = i * 4 + (lane >> 3);  // row within this warp's slice
+                const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
+                cptr[i] = src >= 0 ? a.a_codes + src * a_ld + chunk * 16 : a.a_codes;
+                if (src >= 0) cvalid |= 1u << i;
+            }
+#pragma unroll
+            for (int i = 0; i < NSR; ++i) {
+                const int rl = i * 8 + (lane >> 2);
+                const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
+                sptr[i] = src >= 0 ? a.a_sf + src * sf_ld + word * 4 : a.a_sf;
+                if (src >= 0) svalid |= 1u << i;
+            }
+            for (int kt = 0; kt < k_stages; ++kt) {
                 if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
-                uint8_t* sA = smem + s * STAGE_BYTES;
-                uint8_t* sSFA = sA + A_BYTES + B_BYTES;
+                uint8_t* sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
+                uint8_t* ssf = smem + s * LY::STAGE_BYTES + LY::OFF_SFACT;
+                const bool kin = static_cast<int64_t>(kt) * BK_BYTES + chunk * 16 < a_ld;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int r = pt + h * 64;
-                    const uint8_t* row = a.a_codes + src[h] * a_ld;
+                for (int i = 0; i < NCR; ++i) {
+                    const int r = w2 * RW + i * 4 + (lane >> 3);
+                    const bool v = ((cvalid >> i) & 1u) && kin;
+                    ptx::cp_async_16(sact + r * 128 + ((chunk ^ (r & 7)) * 16), v ? cptr[i] + kt * BK_BYTES : a.a_codes, v);
+                }
+                const bool kin_s = static_cast<int64_t>(kt) * 16 + word * 4 < sf_ld;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const int64_t kb = static_cast<int64_t>(kt) * BK_BYTES + c * 16;
-                        const bool v = valid[h] && kb < a_ld;
-                        ptx::cp_async_16(sA + r * 128 + ((c ^ (r & 7)) * 16), v ? row + kb : a.a_codes, v);
-                    }
-                    const uint8_t* srow = a.a_sf + src[h] * sf_ld;
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int64_t kb = static_cast<int64_t>(kt) * 16 + j * 4;
-                        const bool v = valid[h] && kb < sf_ld;
-                        ptx::cp_async_4(sSFA + j * 512 + (r % 32) * 16 + (r / 32) * 4, v ? srow + kb : a.a_sf, v);
-                    }
+                for (int i = 0; i < NSR; ++i) {
+                    const int r = w2 * RW + i * 8 + (lane >> 2);
+                    const bool v = ((svalid >> i) & 1u) && kin_s;
+                    ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : a.a_sf, v);
                 }
                 ptx::cp_async_commit();
-                // the previous stage's copies have landed: publish it
-                ptx::cp_async_wait<1>();
-                if (pending_stage >= 0) {
+                ++issued;
+                ptx::cp_async_wait<LAG>();
+                if (issued > static_cast<uint32_t>(LAG)) {
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&st.full[pending_stage]);
+                    ptx::mbar_arrive(&st.full[pub]);
+                    if (++pub == C::STAGES) pub = 0;
                 }
-                pending_stage = s;
+                if (++s == C::STAGES) { s = 0; ph ^= 1; }
             }
-            if (!ok) break;
         }
+        // publish the stages still in flight
         ptx::cp_async_wait<0>();
-        if (pending_stage >= 0) {
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&st.full[pending_stage]);
+        ptx::fence_proxy_async_smem();
+        for (uint32_t j = issued > static_cast<uint32_t>(LAG) ? issued - LAG : 0; j < issued; ++j) {
+            ptx::mbar_arrive(&st.full[pub]);
+            if (++pub == C::STAGES) pub = 0;
         }
     } else {
         // ================================ epilogue
-        const int q = warp - 4;            // TMEM lane quarter
-        const int r = q * 32 + lane;       // tile row
+        const int ew = warp - 4;
+        const int q = warp & 3;  // TMEM lane quarter of this warp
         uint32_t lt = 0;
         for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x, ++lt) {
-            const TileInfo ti = tile_info(st, a, n_tiles, L);
+            const TileInfo ti = tile_info(st.tb_off, a, n_wb, C::ACT_ROWS, L);
             const uint32_t as = lt & 1, aph = (lt >> 1) & 1;
             const bool got = ptx::mbar_wait(&st.acc_full[as], aph);
-            __syncwarp();  // tcgen05.ld below is warp-collective
+            __syncwarp();
             if (!__all_sync(0xFFFFFFFFu, got)) { set_abort(st, a.status); break; }
             ptx::tc_fence_after();
-            const uint32_t taddr = tmem + ACC_COL + as * BN + (static_cast<uint32_t>(q * 32) << 16);
-            const bool valid = r < ti.rows;
-            const int64_t p = ti.row0 + r;
+            const uint32_t tbase = tmem + as * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
             const float sa = __ldg(a.a_scale + (a.a_scale_per_group ? ti.g : 0));
-            if (a.epilogue == kEpiSwiGLU) {
-                const float sg = sa * __ldg(a.b_scale + 2 * ti.g), su = sa * __ldg(a.b_scale + 2 * ti.g + 1);
-                const float S = __ldg(a.epi_scale + ti.g);
-                const float six_s = __fmul_rn(6.0f, S);
-                const int I = a.N / 2;
-                uint8_t* hrow = static_cast<uint8_t*>(a.out) + p * (I / 2) + ti.nt * 32;
-                uint8_t* srow = a.out_sf + p * (I / 16) + ti.nt * 4;
-                uint32_t sfw = 0;
-                uint32_t cw[8];
+            if constexpr (!kSwap) {
+                // ---- TMEM lane = token row r; columns = weight rows of block nb
+                const int half = ew >> 2;
+                const int r = q * 32 + lane;
+                const bool valid = r < ti.rows;
+                const int64_t p = ti.row0 + r;
+                if (a.epilogue == kEpiSwiGLU) {
+                    const float sg = sa * __ldg(a.b_scale + 2 * ti.g), su = sa * __ldg(a.b_scale + 2 * ti.g + 1);
+                    const float S = __ldg(a.epi_scale + ti.g);
+                    const float inv_six_s = 1.0f / (6.0f * S);
+                    const int I = a.N / 2;
+                    uint32_t cw[4], sfw = 0;
 #pragma unroll
-                for (int blk = 0; blk < 4; ++blk) {
-                    uint32_t g[16], u[16];
-                    ptx::tmem_ld16(taddr + blk * 16, g);
-                    ptx::tmem_ld16(taddr + 64 + blk * 16, u);
-                    ptx::tmem_ld_wait();
-                    float h[16];
+                    for (int b = 0; b < 2; ++b) {
+                        const int blk = half * 2 + b;  // 16 h columns: gate cols blk*16, up cols 64 + blk*16
+                        uint32_t gr[16], ur[16];
+                        ptx::tmem_ld16(tbase + blk * 16, gr);
+                        ptx::tmem_ld16(tbase + 64 + blk * 16, ur);
+                        ptx::tmem_ld_wait();
+                        float h[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float gv = __uint_as_float(g[i]) * sg;
-                        const float uv = __uint_as_float(u[i]) * su;
-                        h[i] = gv / (1.0f + __expf(-gv)) * uv;
+                        for (int i = 0; i < 16; ++i) h[i] = silu(__uint_as_float(gr[i]) * sg) * (__uint_as_float(ur[i]) * su);
+                        uint32_t lo, hi;
+                        sfw |= encode16_rcp(h, S, inv_six_s, lo, hi) << (8 * b);
+                        cw[2 * b] = lo;
+                        cw[2 * b + 1] = hi;
                     }
-                    uint32_t lo, hi;
-                    sfw |= nvfp4_encode16(h, S, six_s, lo, hi) << (8 * blk);
-                    cw[2 * blk] = lo;
-                    cw[2 * blk + 1] = hi;
-                }
-                if (valid) {
-                    reinterpret_cast<uint4*>(hrow)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                    reinterpret_cast<uint4*>(hrow)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-                    *reinterpret_cast<uint32_t*>(srow) = sfw;
+                    if (valid) {
+                        uint8_t* hrow = static_cast<uint8_t*>(a.out) + p * (I / 2) + ti.nb * 32 + half * 16;
+                        *reinterpret_cast<uint4*>(hrow) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                        *reinterpret_cast<uint16_t*>(a.out_sf + p * (I / 16) + ti.nb * 4 + half * 2) =
+                            static_cast<uint16_t>(sfw);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
+                        uint32_t v[16];
+                        ptx::tmem_ld16(tbase + c0, v);
+                        ptx::tmem_ld_wait();
+                        int col;
+                        float sb;
+                        if (a.gate_up) {
+                            const int upper = c0 >= 64;
+                            col = (upper ? a.N / 2 : 0) + ti.nb * 64 + (c0 & 63);
+                            sb = __ldg(a.b_scale + 2 * ti.g + upper);
+                        } else {
+                            col = ti.nb * W_ROWS + c0;
+                            sb = __ldg(a.b_scale + ti.g);
+                        }
+                        const float s = sa * sb;
+                        if (valid) {
+                            if (a.epilogue == kEpiF32) {
+                                float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + p * a.N + col);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    o[i] = make_float4(__uint_as_float(v[4 * i]) * s, __uint_as_float(v[4 * i + 1]) * s,
+                                                       __uint_as_float(v[4 * i + 2]) * s, __uint_as_float(v[4 * i + 3]) * s);
+                            } else {
+                                uint32_t w[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    w[i] = f32_to_bf16(__uint_as_float(v[2 * i]) * s) |
+                                           (f32_to_bf16(__uint_as_float(v[2 * i + 1]) * s) << 16);
+                                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + p * a.N + col);
+                                o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                                o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                            }
+                        }
+                    }
                 }
             } else {
-#pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
-                    uint32_t v[16];
-                    ptx::tmem_ld16(taddr + c0, v);
-                    ptx::tmem_ld_wait();
+                // ---- TMEM lane = weight row m of block nb; columns = token slots of the tile
+                const int m = q * 32 + lane;
+                uint32_t v[32];
+                ptx::tmem_ld16(tbase, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                ptx::tmem_ld16(tbase + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+                ptx::tmem_ld_wait();
+                const int nv = ti.rows;
+                if (a.epilogue == kEpiSwiGLU) {
+                    // interleaved gate/up block: lanes 0..63 gate rows, 64..127 the matching up rows
+                    SwapXchg& xg = *reinterpret_cast<SwapXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kSwap>));
+                    const float sg = sa * __ldg(a.b_scale + 2 * ti.g), su = sa * __ldg(a.b_scale + 2 * ti.g + 1);
+                    const uint32_t xph = lt & 1;
+                    bool xok = true;
+                    if (q >= 2) {
+                        xok = ptx::mbar_wait(&st.xchg_empty, xph ^ 1);
+                        if (xok) {
+#pragma unroll
+                            for (int t = 0; t < 32; ++t)
+                                if (t < nv) xg.u[m - 64][t] = __uint_as_float(v[t]) * su;
+                        }
+                        ptx::mbar_arrive(&st.xchg_full);
+                    } else {
+                        xok = ptx::mbar_wait(&st.xchg_full, xph);
+                    }
+                    if (!xok) set_abort(st, a.status);
+                    if (q < 2 && xok) {
+                        const float S = __ldg(a.epi_scale + ti.g);
+                        const float inv_six_s = 1.0f / (6.0f * S);
+                        const int I = a.N / 2;
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) {
+                            if (t < nv) {  // warp-uniform
+                                const float h = silu(__uint_as_float(v[t]) * sg) * xg.u[m][t];
+                                float amax = fabsf(h);
+#pragma unroll
+                                for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+                                const uint32_t sf = ptx::cvt_e4m3x2(amax * inv_six_s, 0.0f) & 0xFFu;
+                                const float dsf = ue4m3_to_f32(sf);
+                                uint32_t code = 0;
+                                if (dsf != 0.0f) code = ptx::cvt_e2m1x2(h * __frcp_rn(dsf * S), 0.0f) & 15u;
+                                const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);
+                                const int64_t p = ti.row0 + t;
+                                if ((lane & 1) == 0)
+                                    static_cast<uint8_t*>(a.out)[p * (I / 2) + ti.nb * 32 + m / 2] =
+                                        static_cast<uint8_t>(code | (other << 4));
+                                if ((lane & 15) == 0) a.out_sf[p * (I / 16) + ti.nb * 4 + m / 16] = static_cast<uint8_t>(sf);
+                            }
+                        }
+                    }
+                    if (q < 2) ptx::mbar_arrive(&st.xchg_empty);
+                } else {
                     int col;
                     float sb;
                     if (a.gate_up) {
-                        const int half = c0 >= 64;
-                        col = (half ? a.N / 2 : 0) + ti.nt * 64 + (c0 & 63);
-                        sb = __ldg(a.b_scale + 2 * ti.g + half);
+                        const int upper = m >= 64;
+                        col = (upper ? a.N / 2 : 0) + ti.nb * 64 + (m & 63);
+                        sb = __ldg(a.b_scale + 2 * ti.g + upper);
                     } else {
-                        col = ti.nt * BN + c0;
+                        col = ti.nb * W_ROWS + m;
                         sb = __ldg(a.b_scale + ti.g);
                     }
                     const float s = sa * sb;
-                    if (valid) {
-                        if (a.epilogue == kEpiF32) {
-                            float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + p * a.N + col);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                o[i] = make_float4(__uint_as_float(v[4 * i]) * s, __uint_as_float(v[4 * i + 1]) * s,
-                                                   __uint_as_float(v[4 * i + 2]) * s, __uint_as_float(v[4 * i + 3]) * s);
-                        } else {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                w[i] = f32_to_bf16(__uint_as_float(v[2 * i]) * s) |
-                                       (f32_to_bf16(__uint_as_float(v[2 * i + 1]) * s) << 16);
-                            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + p * a.N + col);
-                            o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                            o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    for (int t = 0; t < 32; ++t) {
+                        if (t < nv) {
+                            const int64_t p = ti.row0 + t;
+                            const float val = __uint_as_float(v[t]) * s;
+                            if (a.epilogue == kEpiF32)
+                                static_cast<float*>(a.out)[p * a.N + col] = val;
+                            else
+                                static_cast<uint16_t*>(a.out)[p * a.N + col] = static_cast<uint16_t>(f32_to_bf16(val));
                         }
                     }
                 }
@@ -328,30 +550,38 @@ __global__ void __launch_bounds__(THREADS, 1)
     ptx::tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        ptx::tmem_dealloc(tmem, TMEM_COLS);
+        ptx::tmem_dealloc(tmem, LY::TMEM_COLS);
     }
 }
 
-size_t grouped_gemm_smem_bytes() { return kSmemBytes; }
+size_t grouped_gemm_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
 
-cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream)
+template <bool kSwap>
+static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_nvf4, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_nvf4<kSwap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_bytes<kSwap>()));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap tmap;
     CUresult cr = encode_tmap_3d_u8(&tmap, a.b_codes, static_cast<uint64_t>(a.K / 2), static_cast<uint64_t>(a.N),
-                                    static_cast<uint64_t>(a.G), BK_BYTES, BN);
+                                    static_cast<uint64_t>(a.G), BK_BYTES, W_ROWS);
     if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    const int64_t mtiles_ub = (p_max + BM - 1) / BM + a.G;
-    const int64_t tiles_ub = mtiles_ub * (a.N / BN);
+    const int act_rows = Cfg<kSwap>::ACT_ROWS;
+    const int64_t blocks_ub = (p_max + act_rows - 1) / act_rows + a.G;
+    const int64_t tiles_ub = blocks_ub * (a.N / W_ROWS);
     const int grid = static_cast<int>(tiles_ub < sms ? (tiles_ub < 1 ? 1 : tiles_ub) : sms);
-    k_grouped_gemm_nvf4<<<grid, THREADS, kSmemBytes, stream>>>(tmap, a);
+    k_grouped_gemm_nvf4<kSwap><<<grid, Lay<kSwap>::THREADS, smem_bytes<kSwap>(), stream>>>(tmap, a);
     return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream)
+{
+    const bool swap = schedule == kSchedWeightsOnM || (schedule == kSchedAuto && p_max <= 64);
+    return swap ? launch_t<true>(a, p_max, sms, stream) : launch_t<false>(a, p_max, sms, stream);
 }
 
 }  // namespace moe

@@ -46,7 +46,6 @@ struct GemmArgs {
     int a_scale_per_group;
     const int32_t* a_row;     // nullable gather index, [P]
     const int32_t* offsets;   // [G+1]
-    const int32_t* tile_off;  // [G+1]
     int G;
     const uint8_t* b_codes;   // prepacked [G][N][K/2] (described by the tensor map)
     const uint8_t* b_sf;      // prepacked tiles [G][N/128][K/64][512]
@@ -60,7 +59,10 @@ struct GemmArgs {
     int* status;
 };
 constexpr int kGemmMaxG = 1025;
-cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream);
+// Tile schedules: activations on the MMA's M side (128-row token blocks) or weights on M
+// (32-row token blocks, for small groups); auto picks weights-on-M when p_max <= 64.
+enum GemmSchedule : int { kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2 };
+cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream);
 size_t grouped_gemm_smem_bytes();
 
 // ---- combine.cu

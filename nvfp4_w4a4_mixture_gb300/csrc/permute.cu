@@ -134,11 +134,71 @@ __global__ void __launch_bounds__(kPermWarps * 32)
     }
 }
 
+// Small assignment lists (n <= kSmallPerm, e.g. a decode batch): one CTA, one launch. Counts by
+// shared-memory atomics (order-free), offsets by a block scan, and each entry's rank within its
+// expert = the number of earlier entries with the same id (a direct count): stable, bit-exact.
+constexpr int kSmallPerm = 512;
+
+__global__ void __launch_bounds__(kScanThreads)
+    k_perm_small(const int32_t* __restrict__ ids, int n, int E, int k, int T, int with_shared, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ perm_src, int32_t* __restrict__ src_perm, int32_t* __restrict__ row_token,
+                 int* status)
+{
+    using Scan = cub::BlockScan<int32_t, kScanThreads>;
+    __shared__ typename Scan::TempStorage tmp;
+    __shared__ int32_t ids_s[kSmallPerm];
+    __shared__ int32_t base_s[1024];
+    __shared__ int32_t total_s;
+    const int tid = threadIdx.x;
+    if (tid < E) base_s[tid] = 0;
+    __syncthreads();
+    for (int f = tid; f < n; f += kScanThreads) {
+        int e = ids[f];
+        if (e < 0 || e >= E) {
+            record_status(status, kDevBadExpertId);
+            e = -1;
+        }
+        ids_s[f] = e;
+        if (e >= 0) atomicAdd(&base_s[e], 1);
+    }
+    __syncthreads();
+    const int32_t cnt = tid < E ? base_s[tid] : 0;
+    int32_t off;
+    Scan(tmp).ExclusiveSum(cnt, off);
+    if (tid < E) {
+        offsets[tid] = off;
+        base_s[tid] = off;
+    }
+    if (tid == E - 1) total_s = off + cnt;
+    __syncthreads();
+    if (tid == 0) {
+        offsets[E] = total_s;
+        offsets[E + 1] = total_s + (with_shared ? T : 0);
+    }
+    for (int f = tid; f < n; f += kScanThreads) {
+        const int e = ids_s[f];
+        if (e < 0) continue;
+        int r = 0;
+        for (int q = 0; q < f; ++q) r += ids_s[q] == e;
+        const int pos = base_s[e] + r;
+        perm_src[pos] = f;
+        src_perm[f] = pos;
+        if (row_token) row_token[pos] = f / k;
+    }
+    if (row_token && with_shared)
+        for (int t = tid; t < T; t += kScanThreads) row_token[n + t] = t;
+}
+
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* offsets,
                            int32_t* tile_off, int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist,
                            int* status, cudaStream_t stream)
 {
     const int64_t n = static_cast<int64_t>(T) * k;
+    if (n <= kSmallPerm && !tile_off) {
+        k_perm_small<<<1, kScanThreads, 0, stream>>>(topk_ids, static_cast<int>(n), E, k, T, with_shared, offsets,
+                                                     perm_src, src_perm, row_token, status);
+        return cudaGetLastError();
+    }
     const int64_t nchunks = perm_chunks(n);
     const int blocks = static_cast<int>((nchunks + kPermWarps - 1) / kPermWarps);
     const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);

@@ -1,7 +1,8 @@
 // quantize.cu -- NVFP4 encoding of activations (W4A4) and weights.
 //
 // Two passes over the tensor: a max-reduction for the tensor scale (skipped with a static
-// scale), then one thread per 16-element block. Loads are 16-byte vectors, a warp reads 1 KiB of
+// scale), then one thread per 16-element block; a tensor of at most 4096 blocks is done by a
+// single CTA in one launch. Loads are 16-byte vectors, a warp reads 1 KiB of
 // bf16 contiguously and writes 256 contiguous bytes of codes and 32 bytes of block scales.
 #include "kernels.cuh"
 
@@ -74,6 +75,55 @@ __global__ void k_quantize(const Tin* __restrict__ x, int64_t nblocks, const flo
     }
 }
 
+// Small tensors (<= kSmallBlocks blocks, e.g. a decode batch): one CTA computes the max and encodes,
+// one launch instead of three.
+constexpr int64_t kSmallBlocks = 4096;
+constexpr int kSmallThreads = 512;
+
+template <typename Tin>
+__global__ void __launch_bounds__(kSmallThreads)
+    k_quantize_small(const Tin* __restrict__ x, int64_t nblocks, const float* __restrict__ s_static,
+                     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ s_out)
+{
+    __shared__ uint32_t wmax[kSmallThreads / 32];
+    __shared__ float S_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (s_static) {
+        if (tid == 0) S_s = *s_static;
+    } else {
+        uint32_t m = 0;
+        for (int64_t b = tid; b < nblocks; b += kSmallThreads) {
+            float v[16];
+            load16(x + b * 16, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = abs_bits_max(m, v[i]);
+        }
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0) wmax[warp] = m;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t w = lane < kSmallThreads / 32 ? wmax[lane] : 0u;
+            w = __reduce_max_sync(0xFFFFFFFFu, w);
+            if (lane == 0) {
+                const float amax = __uint_as_float(w);
+                S_s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+            }
+        }
+    }
+    __syncthreads();
+    const float S = S_s;
+    if (s_out && tid == 0) *s_out = S;
+    const float six_s = __fmul_rn(6.0f, S);
+    for (int64_t b = tid; b < nblocks; b += kSmallThreads) {
+        float v[16];
+        load16(x + b * 16, v);
+        uint32_t lo, hi;
+        const uint32_t s = nvfp4_encode16(v, S, six_s, lo, hi);
+        *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(lo, hi);
+        sf[b] = static_cast<uint8_t>(s);
+    }
+}
+
 static int quant_grid(int64_t nblocks, int sms)
 {
     const int64_t want = (nblocks + 255) / 256;
@@ -86,6 +136,10 @@ cudaError_t launch_quantize_t(const Tin* x, int64_t rows, int64_t K, const float
                               float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
 {
     const int64_t nblocks = rows * K / 16;
+    if (nblocks <= kSmallBlocks) {
+        k_quantize_small<Tin><<<1, kSmallThreads, 0, stream>>>(x, nblocks, s_in, codes, sf, s_out);
+        return cudaGetLastError();
+    }
     if (!s_in) {
         cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), stream);
         if (e != cudaSuccess) return e;

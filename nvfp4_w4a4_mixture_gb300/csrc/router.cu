@@ -4,9 +4,9 @@
 // loads of the router row (each row of W_r is read once per token tile). Every product of two
 // bf16 values is exact in FP32; the sum runs in a fixed order (per-lane strided partial sums,
 // then a butterfly), so the result is deterministic.
-// Top-k: one warp per token; k rounds of a warp arg-max on (logit desc, expert id asc), which
-// is the lowest-index tie rule; the renormalised weights are the softmax over the selected
-// logits (the full softmax denominator cancels), the shared gate is sigmoid(logit E).
+// Top-k: one CTA of 4 warps per token; k rounds of a block arg-max on (logit desc, expert id
+// asc), which is the lowest-index tie rule; the renormalised weights are the softmax over the
+// selected logits (the full softmax denominator cancels), the shared gate is sigmoid(logit E).
 #include <cfloat>
 
 #include "kernels.cuh"
@@ -39,17 +39,28 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
 #pragma unroll
     for (int t = 0; t < kRouterTT; ++t) acc[t] = 0.0f;
     const uint16_t* wr = w + static_cast<int64_t>(e) * H;
-    for (int h0 = lane * 8; h0 < H; h0 += 256) {
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wr + h0));
-        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    // the row's 16-byte vectors are loaded 8 at a time so their latencies overlap
+    for (int base = 0; base < H; base += 8 * 256) {
+        uint4 wv[8];
 #pragma unroll
-        for (int t = 0; t < kRouterTT; ++t) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h0);
-            const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+        for (int u = 0; u < 8; ++u) {
+            const int h0 = base + u * 256 + lane * 8;
+            wv[u] = h0 < H ? __ldg(reinterpret_cast<const uint4*>(wr + h0)) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu)));
-                acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16)));
+        for (int u = 0; u < 8; ++u) {
+            const int h0 = base + u * 256 + lane * 8;
+            if (h0 >= H) break;
+            const uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+            for (int t = 0; t < kRouterTT; ++t) {
+                const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h0);
+                const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu)));
+                    acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16)));
+                }
             }
         }
     }
@@ -68,65 +79,88 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     }
 }
 
-constexpr int kTopkMaxPerLane = 32;  // E <= 1024
+constexpr int kTopkThreads = 128;
+constexpr int kTopkPer = 8;  // E <= 1024 = kTopkThreads * kTopkPer
 
-__global__ void k_topk(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
-                       float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
+// (value desc, index asc) order: true when (a, ia) comes before (b, ib)
+__device__ __forceinline__ bool before(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+
+// One CTA (4 warps) per token: each thread holds 8 logits; k rounds of a block arg-max.
+__global__ void __launch_bounds__(kTopkThreads)
+    k_topk(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
+           float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
 {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) / 32, lane = threadIdx.x % 32;
-    if (warp >= T) return;
-    const int t = warp;
+    __shared__ float wb[kTopkThreads / 32];
+    __shared__ int wi[kTopkThreads / 32];
+    __shared__ float sel_l[32];
+    __shared__ int sel_i[32];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float* l = logits + static_cast<int64_t>(t) * (E + 1);
-    float v[kTopkMaxPerLane];
+    float v[kTopkPer];
+    unsigned live = 0;
 #pragma unroll
-    for (int i = 0; i < kTopkMaxPerLane; ++i) {
-        const int e = i * 32 + lane;
-        v[i] = e < E ? l[e] : -FLT_MAX;
-        if (logits_out && e < E) logits_out[static_cast<int64_t>(t) * E + e] = v[i];
+    for (int i = 0; i < kTopkPer; ++i) {
+        const int e = i * kTopkThreads + tid;
+        v[i] = e < E ? l[e] : 0.0f;
+        if (e < E) {
+            live |= 1u << i;
+            if (logits_out) logits_out[static_cast<int64_t>(t) * E + e] = v[i];
+        }
     }
-    float sel_l0 = 0.0f, wsum = 0.0f;
-    float my_l = 0.0f;  // lane j keeps the j-th selected logit
-    int my_id = 0;
     for (int j = 0; j < k; ++j) {
-        float best = -FLT_MAX;
-        int bid = 0x7FFFFFFF;
+        float b = -INFINITY;  // (-inf, INT_MAX) loses to every live (finite) logit
+        int bi = 0x7FFFFFFF;
 #pragma unroll
-        for (int i = 0; i < kTopkMaxPerLane; ++i) {
-            const int e = i * 32 + lane;
-            if (e < E && (v[i] > best || (v[i] == best && e < bid))) {
-                best = v[i];
-                bid = e;
+        for (int i = 0; i < kTopkPer; ++i) {
+            const int e = i * kTopkThreads + tid;
+            if (((live >> i) & 1u) && before(v[i], e, b, bi)) {
+                b = v[i];
+                bi = e;
             }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bid, o);
-            if (ob > best || (ob == best && oi < bid)) {
-                best = ob;
-                bid = oi;
+            const float ob = __shfl_xor_sync(0xFFFFFFFFu, b, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (before(ob, oi, b, bi)) {
+                b = ob;
+                bi = oi;
             }
         }
-#pragma unroll
-        for (int i = 0; i < kTopkMaxPerLane; ++i)
-            if (i * 32 + lane == bid) v[i] = -FLT_MAX;
-        if (j == 0) sel_l0 = best;
-        if (lane == j) {
-            my_l = best;
-            my_id = bid;
+        if (lane == 0) {
+            wb[warp] = b;
+            wi[warp] = bi;
         }
-    }
-    // softmax over the selected logits (max = first selected)
-    float p = 0.0f;
-    if (lane < k) p = expf(my_l - sel_l0);
-    wsum = p;
+        __syncthreads();
+        b = wb[0];
+        bi = wi[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xFFFFFFFFu, wsum, o);
-    if (lane < k) {
-        topk_ids[static_cast<int64_t>(t) * k + lane] = my_id;
-        topk_w[static_cast<int64_t>(t) * k + lane] = p / wsum;
+        for (int w = 1; w < kTopkThreads / 32; ++w)
+            if (before(wb[w], wi[w], b, bi)) {
+                b = wb[w];
+                bi = wi[w];
+            }
+        if (tid == 0) {
+            sel_l[j] = b;
+            sel_i[j] = bi;
+        }
+#pragma unroll
+        for (int i = 0; i < kTopkPer; ++i)
+            if (i * kTopkThreads + tid == bi) live &= ~(1u << i);
+        __syncthreads();
     }
-    if (shared_g && lane == 0) shared_g[t] = 1.0f / (1.0f + expf(-l[E]));
+    // renormalised weights: softmax over the selected logits (the first one is the largest)
+    if (warp == 0) {
+        const float p = lane < k ? expf(sel_l[lane] - sel_l[0]) : 0.0f;
+        float sum = p;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        if (lane < k) {
+            topk_ids[static_cast<int64_t>(t) * k + lane] = sel_i[lane];
+            topk_w[static_cast<int64_t>(t) * k + lane] = p / sum;
+        }
+        if (shared_g && lane == 0) shared_g[t] = 1.0f / (1.0f + expf(-l[E]));
+    }
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
@@ -148,9 +182,7 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* topk_
                         float* logits_out, cudaStream_t stream)
 {
     if (T <= 0) return cudaSuccess;
-    const int warps_per_block = 8;
-    const int blocks = (T + warps_per_block - 1) / warps_per_block;
-    k_topk<<<blocks, warps_per_block * 32, 0, stream>>>(logits, T, E, k, topk_ids, topk_w, shared_g, logits_out);
+    k_topk<<<T, kTopkThreads, 0, stream>>>(logits, T, E, k, topk_ids, topk_w, shared_g, logits_out);
     return cudaGetLastError();
 }
 

@@ -222,14 +222,22 @@ def _gemm_case(seed, counts, H, I, N_kind):
     return dict(offsets=offsets, P=P, ac=ac, asf=asf, sa=sa, a_row=a_row, bc=bc, bs=bs, bsc=bsc, N=N, K=K)
 
 
-@pytest.mark.parametrize("counts", [[3, 0, 130, 1, 128, 257], [1] * 40, [700], [0, 0, 5]])
-def test_gemm_gate_up_f32(moe, counts):
+SCHEDS = ["act_on_m", "weights_on_m"]
+
+
+def _sched(moe, name):
+    return moe.SCHED_ACT_ON_M if name == "act_on_m" else moe.SCHED_WEIGHTS_ON_M
+
+
+@pytest.mark.parametrize("sched", SCHEDS)
+@pytest.mark.parametrize("counts", [[3, 0, 130, 1, 128, 257], [1] * 40, [700], [0, 0, 5], [33, 32, 31, 64, 65]])
+def test_gemm_gate_up_f32(moe, counts, sched):
     c = _gemm_case(len(counts), counts, 256, 128, "gate_up")
     ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
     bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
     out = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
                                      dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], True,
-                                     moe.EPI_F32, a_row_index=dev(c["a_row"]))
+                                     moe.EPI_F32, a_row_index=dev(c["a_row"]), schedule=_sched(moe, sched))
     out = out.cpu().numpy()
     assert I_.rel_frobenius(out, ref) <= GEMM_TOL
     for g in range(len(counts)):
@@ -238,34 +246,38 @@ def test_gemm_gate_up_f32(moe, counts):
             assert I_.rel_frobenius(out[p0:p1], ref[p0:p1]) <= GEMM_TOL, g
 
 
-def test_gemm_gate_up_f32_flash_shape(moe):
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_gemm_gate_up_f32_flash_shape(moe, sched):
     c = _gemm_case(11, [2, 130, 1], 2048, 768, "gate_up")
     ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
     bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
     out = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
                                      dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], True,
-                                     moe.EPI_F32, a_row_index=dev(c["a_row"])).cpu().numpy()
+                                     moe.EPI_F32, a_row_index=dev(c["a_row"]),
+                                     schedule=_sched(moe, sched)).cpu().numpy()
     assert I_.rel_frobenius(out, ref) <= GEMM_TOL
     for g in range(3):
         p0, p1 = c["offsets"][g], c["offsets"][g + 1]
         assert I_.rel_frobenius(out[p0:p1], ref[p0:p1]) <= GEMM_TOL
 
 
+@pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("H,I", [(256, 128), (2048, 768)])
-def test_gemm_down_bf16(moe, H, I):
+def test_gemm_down_bf16(moe, H, I, sched):
     c = _gemm_case(5, [5, 129, 0, 2], H, I, "down")
     ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
     bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), False)
     out = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
                                      dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], False,
-                                     moe.EPI_BF16, a_row_index=dev(c["a_row"]))
+                                     moe.EPI_BF16, a_row_index=dev(c["a_row"]), schedule=_sched(moe, sched))
     out = out.float().cpu().numpy()
     # bf16 output: one rounding of each element (relative 2^-9)
     assert I_.rel_frobenius(out, ref) <= 4e-3
 
 
+@pytest.mark.parametrize("sched", SCHEDS)
 @pytest.mark.parametrize("H,I,counts", [(256, 128, [3, 0, 130, 1, 128]), (2048, 768, [1, 40, 3])])
-def test_gemm_swiglu_requant(moe, H, I, counts):
+def test_gemm_swiglu_requant(moe, H, I, counts, sched):
     c = _gemm_case(7, counts, H, I, "gate_up")
     G = len(counts)
     gu_ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
@@ -275,7 +287,8 @@ def test_gemm_swiglu_requant(moe, H, I, counts):
     bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
     hc, hs = moe.moe_grouped_gemm_nvfp4(dev(c["ac"]), dev(c["asf"]), dev(np.array([c["sa"]], np.float32)),
                                         dev(c["offsets"]), c["P"], bcp, bsp, dev(c["bsc"]), c["N"], c["K"], True,
-                                        moe.EPI_SWIGLU_NVFP4, a_row_index=dev(c["a_row"]), epi_scale=dev(s_mid))
+                                        moe.EPI_SWIGLU_NVFP4, a_row_index=dev(c["a_row"]), epi_scale=dev(s_mid),
+                                        schedule=_sched(moe, sched))
     n_g, n_r = nibbles(hc.cpu().numpy()), nibbles(hc_ref)
     match = np.mean(n_g == n_r)
     assert match >= CODE_MATCH, match
