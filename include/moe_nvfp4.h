@@ -201,6 +201,23 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
                                         uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream,
                                         void* const* events, int n_events);
 
+/* ---------------------------------------------------------------------------------------------
+ * moe_route_topk_noalloc -- moe_route_topk for callers that cannot give the library scratch
+ *   memory: an application whose device memory is owned by another allocator and may not grow
+ *   by extra cudaMalloc calls, or a decode loop that cannot afford cudaMalloc's implicit device
+ *   synchronisation. The capy-flash pages have no counterpart of this call; it is a convenience
+ *   of this library.
+ *   Same arguments and results as moe_route_topk, without the workspace. The logits scratch is a
+ *   fixed array inside the library (64 tokens x 1025 FP32 = 262,400 bytes of device memory on
+ *   every GPU that loads the library, held until the process exits); it allocates nothing.
+ *   Limits: T <= 64, E <= 1024; larger calls return MOE_ERR_UNSUPPORTED_SHAPE (use
+ *   moe_route_topk). The first call on a device looks up the array's device address (a host-side
+ *   set-up step); make that first call before capturing any stream. Every call shares the one
+ *   array: calls that overlap on the GPU (other streams or host threads) race on it.
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids,
+                                    float* topk_w, float* shared_g, float* logits_out, moe_stream_t stream);
+
 /* Workspace bytes for any call above with these sizes (T tokens). */
 size_t moe_workspace_bytes(int H, int E, int k, int I, int T);
 

@@ -18,7 +18,7 @@ SCHED_AUTO, SCHED_ACT_ON_M, SCHED_WEIGHTS_ON_M = 0, 0x100, 0x200
 ENTRY_POINTS = (
     "moe_quantize_nvfp4", "moe_quantize_nvfp4_f32", "moe_route_topk", "moe_permute", "moe_prepack_nvfp4",
     "moe_grouped_gemm_nvfp4", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled", "moe_workspace_bytes",
-    "moe_read_device_status", "moe_status_string", "moe_last_error_detail",
+    "moe_read_device_status", "moe_status_string", "moe_last_error_detail", "moe_route_topk_noalloc",
 )
 
 
@@ -63,6 +63,8 @@ def lib():
             f.argtypes = [vp, i64, i64, vp, vp, vp, vp, vp, sz, vp]
         L.moe_route_topk.restype = i32
         L.moe_route_topk.argtypes = [vp, i32, ctypes.POINTER(LayerDesc), vp, vp, vp, vp, vp, sz, vp]
+        L.moe_route_topk_noalloc.restype = i32
+        L.moe_route_topk_noalloc.argtypes = [vp, i32, ctypes.POINTER(LayerDesc), vp, vp, vp, vp, vp]
         L.moe_permute.restype = i32
         L.moe_permute.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
         L.moe_prepack_nvfp4.restype = i32

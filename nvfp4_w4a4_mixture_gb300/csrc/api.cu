@@ -119,6 +119,8 @@ moe_status_t check_ws(const void* ws, size_t ws_bytes, size_t need)
 
 }  // namespace
 
+void set_last_error_detail(const char* msg) { g_detail = msg ? msg : ""; }
+
 int device_sm_count()
 {
     int dev = 0, sms = 0;

@@ -71,6 +71,7 @@ cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* 
 
 // ---- api.cu
 int device_sm_count();
+void set_last_error_detail(const char* msg);  // text returned by moe_last_error_detail()
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                            uint32_t box1);
 
