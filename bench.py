@@ -202,7 +202,7 @@ def launches_per_layer(c):
     T, H, k = c["T"], c["H"], c["k"]
     quant = 1 if T * H // 16 <= 4096 else 2
     perm = 1 if T * k <= 512 else 3
-    return quant + 2 + perm + 2 + 1  # quantize, logits + top-k, permute, two GEMMs, combine
+    return quant + 2 + perm + 1 + 1  # quantize, logits + top-k, permute, expert GEMMs (one launch), combine
 
 
 def distinct_experts(m, layer, x):
@@ -397,7 +397,7 @@ def run_ours(args, c, d):
 
     # ---- per-stage durations of the same launch sequence (CUDA events at the stage boundaries)
     Kp = min(K, 500)
-    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(Kp)]
+    st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(m.LAYER_STAGES) + 1)] for _ in range(Kp)]
     with torch.cuda.stream(stream):
         for i in range(Kp):
             flush.zero_()
@@ -429,15 +429,18 @@ def run_ours(args, c, d):
     e2e_ms = d.max(statistics.mean(a.elapsed_time(b) for a, b in ee))
     m.moe_read_device_status(ws)
 
-    # ---- roofline of the dominant kernel (gate/up GEMM) and of the whole layer
+    # ---- roofline of the dominant kernel (the expert GEMMs, one launch) and of the whole layer
     hbm, bf16_burst, bf16_sus, peak_src = measured_peaks()
     U = distinct_experts(m, layers[0], x)  # routed experts touched by this batch
     per_gu = 2 * I * H // 2 + 2 * I * H // 16 + 8
     per_dn = H * I // 2 + H * I // 16 + 4
     P = T * k + T
-    gemm1_bytes = (U + 1) * per_gu + T * H * (1 / 2 + 1 / 16) + P * I * (1 / 2 + 1 / 16)
-    gemm1_us = stage_us["gemm_gate_up"]
-    achieved = gemm1_bytes / (gemm1_us * 1e-6) / 1e9
+    # weights of the touched experts + shared expert, x codes read once, h written and read once,
+    # y written once
+    exp_bytes = ((U + 1) * (per_gu + per_dn) + T * H * (1 / 2 + 1 / 16) + 2 * P * I * (1 / 2 + 1 / 16)
+                 + P * H * 2)
+    exp_us = stage_us["experts"]
+    achieved = exp_bytes / (exp_us * 1e-6) / 1e9
     layer_bytes = L * ((U + 1) * (per_gu + per_dn) + (E + 1) * H * 2 + 2 * T * H * 2 + (T * H * 2 if L > 1 else 0))
     layer_flops = L * 2.0 * T * (k + 1) * 3 * H * I
     fp4_peak = bf16_burst * FP4_OVER_BF16
@@ -454,9 +457,9 @@ def run_ours(args, c, d):
                    "l2": "flushed before every timed step (256 MiB write, outside the timed interval)",
                    "parallelism": "replicas" if d.world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": recorded_traffic("gemm_gate_up/" + args.config),
-                     "kernel": "k_grouped_gemm_nvf4 (gate/up, fused SwiGLU + NVFP4 requant)",
-                     "algorithmic_bytes_per_launch": gemm1_bytes, "avg_launch_us": gemm1_us,
+                     "traffic": recorded_traffic("experts/" + args.config),
+                     "kernel": "k_grouped_gemm_nvf4 (gate/up + SwiGLU + NVFP4 requant + down, one launch)",
+                     "algorithmic_bytes_per_launch": exp_bytes, "avg_launch_us": exp_us,
                      "peak_source": peak_src + " hbm_gbs"},
         "layer_roofline": {"bytes": layer_bytes, "flops_fp4": layer_flops, "hbm_frac": hbm_frac,
                            "fp4_tc_frac": fp4_frac, "fp4_peak_tflops": fp4_peak,

@@ -194,8 +194,8 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
  * moe_layer_forward_profiled -- moe_layer_forward that also records caller-created CUDA events
  *   (cudaEvent_t handles) on `stream` at the stage boundaries: events[0] before the activation
  *   quantizer, [1] after it, [2] after routing (logits + top-k), [3] after the permutation, [4]
- *   after the gate/up GEMM, [5] after the down GEMM, [6] after the combine. n_events: 0 (plain
- *   forward) or 7. The library creates and destroys no event.
+ *   after the expert GEMMs (gate/up + SwiGLU + requantisation + down, one launch), [5] after the
+ *   combine. n_events: 0 (plain forward) or 6. The library creates and destroys no event.
  * ------------------------------------------------------------------------------------------- */
 moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
                                         uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream,

@@ -269,11 +269,11 @@ def moe_layer_forward(layer, x, residual=None, out=None, ws=None):
     return out
 
 
-LAYER_STAGES = ("quantize", "route", "permute", "gemm_gate_up", "gemm_down", "combine")
+LAYER_STAGES = ("quantize", "route", "permute", "experts", "combine")
 
 
 def moe_layer_forward_profiled(layer, x, events, residual=None, out=None, ws=None):
-    """moe_layer_forward recording 7 torch.cuda.Event objects (already created, enable_timing) at the
+    """moe_layer_forward recording 6 torch.cuda.Event objects (already created, enable_timing) at the
     stage boundaries of LAYER_STAGES."""
     T = x.shape[0]
     if out is None:

@@ -15,7 +15,7 @@ namespace moe {
 namespace {
 
 thread_local std::string g_detail;
-constexpr int kLayerStageEvents = 7;
+constexpr int kLayerStageEvents = 6;
 
 moe_status_t fail(moe_status_t s, const char* fmt, ...)
 {
@@ -56,7 +56,7 @@ moe_status_t check_device()
 
 struct WsLayout {
     size_t hdr, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, perm_src, src_perm, row_token,
-        hist, h_codes, h_sf, y, total;
+        hist, h_codes, h_sf, ready, y, total;
 };
 
 WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
@@ -81,8 +81,11 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     L.src_perm = take(n * 4);
     L.row_token = take(P * 4);
     L.hist = take(perm_chunks(n) * E * 4);
+    // token blocks of the expert GEMMs: at most ceil(P / 32) + E + 1 (32-row blocks in the smallest schedule)
+    const int64_t nblk = (P + 31) / 32 + E + 1;
     L.h_codes = take(P * I / 2);
-    L.h_sf = take(P * I / 16);
+    L.h_sf = take(nblk * (I / 64) * 512);  // h block scales in token-block tiles
+    L.ready = take(nblk * 4);
     L.y = take(P * H * 2);
     L.total = off;
     return L;
@@ -312,23 +315,25 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     GemmArgs ga{};
-    ga.a_codes = a_codes;
-    ga.a_sf = a_sf;
-    ga.a_scale = a_scale;
-    ga.a_scale_per_group = a_scale_per_group ? 1 : 0;
-    ga.a_row = a_row_index;
+    GemmProblem& P = ga.p[0];
+    P.a_codes = a_codes;
+    P.a_sf = a_sf;
+    P.a_scale = a_scale;
+    P.a_scale_per_group = a_scale_per_group ? 1 : 0;
+    P.a_row = a_row_index;
+    P.b_codes = b->codes;
+    P.b_sf = b->sf;
+    P.b_scale = b->gscale;
+    P.gate_up = gate_up ? 1 : 0;
+    P.N = N;
+    P.K = K;
+    P.epilogue = epilogue;
+    P.epi_scale = epi_scale;
+    P.out = out;
+    P.out_sf = out_sf;
+    ga.nphase = 1;
     ga.offsets = group_offsets;
     ga.G = G;
-    ga.b_codes = b->codes;
-    ga.b_sf = b->sf;
-    ga.b_scale = b->gscale;
-    ga.gate_up = gate_up ? 1 : 0;
-    ga.N = N;
-    ga.K = K;
-    ga.epilogue = epilogue;
-    ga.epi_scale = epi_scale;
-    ga.out = out;
-    ga.out_sf = out_sf;
     ga.status = &hdr->status;
     MOE_CUDA(launch_grouped_gemm(ga, p_max, schedule, device_sm_count(), s), "grouped GEMM launch");
     return MOE_OK;
@@ -396,14 +401,14 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
                             P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
              "permute");
     MOE_CUDA(mark(3), "event record");
-    // gate/up GEMM with the fused SwiGLU + NVFP4 requantisation
-    GemmArgs g1{};
+    // expert GEMMs in one launch: gate/up with the fused SwiGLU + NVFP4 requantisation of h,
+    // then down (bf16 rows in permuted order); a down tile waits for its token block's h
+    GemmArgs ga{};
+    GemmProblem& g1 = ga.p[0];
     g1.a_codes = P8(W.x_codes);
     g1.a_sf = P8(W.x_sf);
     g1.a_scale = &hdr->s_x;
     g1.a_row = P32(W.row_token);
-    g1.offsets = P32(W.offsets);
-    g1.G = E + 1;
     g1.b_codes = L->w_gate_up.codes;
     g1.b_sf = L->w_gate_up.sf;
     g1.b_scale = L->w_gate_up.gscale;
@@ -414,35 +419,35 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     g1.epi_scale = L->s_mid;
     g1.out = P8(W.h_codes);
     g1.out_sf = P8(W.h_sf);
-    g1.status = &hdr->status;
-    // few rows per expert (decode): weights on the MMA's M side; otherwise activations on M
-    const int sched = static_cast<int64_t>(T) * k <= 16LL * E ? kSchedWeightsOnM : kSchedActOnM;
-    MOE_CUDA(launch_grouped_gemm(g1, P, sched, sms, s), "gate/up GEMM");
-    MOE_CUDA(mark(4), "event record");
-    // down GEMM, bf16 rows in permuted order
-    GemmArgs g2 = g1;
+    g1.out_sf_tiled = 1;
+    GemmProblem& g2 = ga.p[1];
     g2.a_codes = P8(W.h_codes);
     g2.a_sf = P8(W.h_sf);
+    g2.a_sf_tiled = 1;
     g2.a_scale = L->s_mid;
     g2.a_scale_per_group = 1;
-    g2.a_row = nullptr;
     g2.b_codes = L->w_down.codes;
     g2.b_sf = L->w_down.sf;
     g2.b_scale = L->w_down.gscale;
-    g2.gate_up = 0;
     g2.N = H;
     g2.K = I;
     g2.epilogue = kEpiBF16;
-    g2.epi_scale = nullptr;
     g2.out = base + W.y;
-    g2.out_sf = nullptr;
-    MOE_CUDA(launch_grouped_gemm(g2, P, sched, sms, s), "down GEMM");
-    MOE_CUDA(mark(5), "event record");
+    ga.nphase = 2;
+    ga.offsets = P32(W.offsets);
+    ga.G = E + 1;
+    ga.ready = P32(W.ready);
+    ga.status = &hdr->status;
+    // few rows per expert (decode): weights on the MMA's M side; otherwise activations on M
+    const int sched = static_cast<int64_t>(T) * k <= 16LL * E ? kSchedWeightsOnM : kSchedActOnM;
+    MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, ((P + 31) / 32 + E + 1) * 4, s), "clear ready counters");
+    MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");
+    MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)
     MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), P32(W.src_perm), T,
                             k, H, residual, out, s),
              "combine");
-    MOE_CUDA(mark(6), "event record");
+    MOE_CUDA(mark(5), "event record");
     return MOE_OK;
 }
 

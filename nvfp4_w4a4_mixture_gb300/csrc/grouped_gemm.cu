@@ -4,25 +4,31 @@
 // computed by tcgen05.mma kind::mxf4nvf4 (E2M1 x E2M1 products, one UE4M3 scale per 16 along K,
 // FP32 accumulation in tensor memory).
 //
-// One persistent CTA per SM walks a list of output tiles (token block of a group, 128 weight rows),
-// weight blocks fastest, so consecutive CTAs share the token block's activation rows and one
-// expert's weights stay in L2 across its token blocks. Two schedules:
+// One persistent CTA per SM walks a list of output tiles (token block of a group, 128 weight
+// rows), weight blocks fastest, so consecutive CTAs share the token block's activation rows and
+// one expert's weights stay in L2 across its token blocks. Two schedules:
 //   activations on M (large groups): 128 token rows x 128 weight rows per tile, MMA 128 x 128;
-//   weights on M (small groups, "swap"): 128 weight rows x 32 token rows per tile, MMA 128 x 32, so a
-//     decode step with one or two tokens per expert does not pay for 128-row tiles.
+//   weights on M (small groups): 128 weight rows x 32 token rows per tile, MMA 128 x 32, so a decode
+//     step with one or two tokens per expert does not pay for 128-row tiles.
+// A launch can hold two problems (phases) over the same groups: the gate/up GEMM with its SwiGLU
+// epilogue, then the down GEMM reading the intermediate h. A down tile of token block b waits
+// (bounded) until every gate/up tile of block b has stored its part of h: the gate/up epilogue
+// threads publish with a fence and an atomic count per token block. The two-phase launch is
+// cooperative, so all CTAs are resident and such a wait ends. h's block scales are written in
+// 512-byte token-block tiles, the layout the down GEMM copies straight into shared memory.
 // Warp roles:
 //   warp 0       weight producer: TMA of the 128 x 128-byte weight box (128-byte swizzle) and one
 //                bulk copy of its scale-factor tiles, per K-stage of 256 elements;
-//   warp 1       TMEM owner and MMA issuer: per stage, tcgen05.cp of both scale-factor sets into
-//                tensor memory, then 4 x tcgen05.mma (K = 64 each) into a double-buffered accumulator;
+//   warp 1       TMEM owner and MMA issuer: per K-step of 64, tcgen05.cp of both scale-factor
+//                tiles into tensor memory and one tcgen05.mma into a double-buffered accumulator;
 //   warps 2-3    activation producers: gather the tile's activation rows (row index list) with
 //                cp.async into the swizzled layout, and their scale factors into tile layout;
 //   warps 4..    epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31), apply
 //                the tensor scales and write FP32 / bf16 rows, or SwiGLU + NVFP4 requantisation.
 // Stage hand-over uses mbarriers (full: producers -> MMA; empty: MMA commit -> producers;
-// acc_full / acc_empty: MMA <-> epilogue). Every wait is bounded (ptx::mbar_wait): on timeout the
-// CTA records kDevTimeoutGemm in the status word, all roles stop, and TMEM is freed after the
-// tensor cores drain.
+// acc_full / acc_empty: MMA <-> epilogue). Every wait is bounded (ptx::mbar_wait, spin_until): on
+// timeout the CTA records kDevTimeoutGemm in the status word, all roles stop, and TMEM is freed
+// after the tensor cores drain.
 #include "kernels.cuh"
 
 namespace moe {
@@ -33,7 +39,7 @@ constexpr int BK_BYTES = 128;              // K-stage: one 128-byte swizzle row 
 constexpr int W_ROWS = 128;                // weight rows per tile (one TMA box)
 constexpr int SF_TILE = 512;               // scale factors of 128 rows x 4 K-blocks
 constexpr int SF_STAGE = 4 * SF_TILE;      // 4 MMA K-steps of 64 per stage
-constexpr int kNumActProducers = 64;  // warps 2-3; each arrives on every stage's full barrier
+constexpr int kNumActProducers = 64;       // warps 2-3; each arrives on every stage's full barrier
 
 template <bool kSwap>
 struct Cfg;
@@ -58,6 +64,7 @@ struct Lay {
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
     static constexpr int SF_COL = 2 * C::ACC_COLS;  // first scale-factor column; 32 per stage
     static constexpr int TMEM_COLS = 512;
+    static constexpr int READY_PER_TILE = C::EPI_WARPS;  // epilogue warp arrivals per gate/up tile
     static_assert(SF_COL + 32 * C::STAGES <= TMEM_COLS, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
@@ -90,7 +97,7 @@ constexpr size_t smem_bytes()
 }
 
 struct TileInfo {
-    int g, nb, row0, rows;
+    int ph, g, nb, tbg, row0, rows;
 };
 
 // tb_off[g] = sum_{g' < g} ceil(rows_g' / act_rows), g = 0..G (block-wide scan; contains barriers)
@@ -133,19 +140,23 @@ __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, in
     __syncthreads();
 }
 
-__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmArgs& a, int n_wb, int act_rows, int L)
+// Tile L of the launch: phase-0 tiles first (token block major, weight block minor), then phase 1.
+__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmArgs& a, int act_rows, int tiles0, int L)
 {
-    const int tbg = L / n_wb;
     TileInfo ti;
-    ti.nb = L - tbg * n_wb;
+    ti.ph = L >= tiles0 ? 1 : 0;
+    const int Lp = L - (ti.ph ? tiles0 : 0);
+    const int n_wb = a.p[ti.ph].N / W_ROWS;
+    ti.tbg = Lp / n_wb;
+    ti.nb = Lp - ti.tbg * n_wb;
     int lo = 0, hi = a.G;  // tb_off[lo] <= tbg < tb_off[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (tb_off[mid] <= tbg) lo = mid; else hi = mid;
+        if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
     }
     ti.g = lo;
     const int g0 = __ldg(a.offsets + lo), g1 = __ldg(a.offsets + lo + 1);
-    ti.row0 = g0 + (tbg - tb_off[lo]) * act_rows;
+    ti.row0 = g0 + (ti.tbg - tb_off[lo]) * act_rows;
     ti.rows = min(act_rows, g1 - ti.row0);
     return ti;
 }
@@ -160,6 +171,25 @@ template <bool kSwap>
 __device__ __forceinline__ bool aborted(const Tail<kSwap>& t)
 {
     return *reinterpret_cast<const volatile int*>(&t.abort) != 0;
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *p >= target; false on timeout.
+__device__ __forceinline__ bool spin_until(const int32_t* p, int target)
+{
+    if (ld_acquire(p) >= target) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (ld_acquire(p) < target) {
+        if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+    return true;
 }
 
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
@@ -192,7 +222,8 @@ __device__ __forceinline__ uint32_t encode16_rcp(const float (&v)[16], float S, 
 
 template <bool kSwap>
 __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
-    k_grouped_gemm_nvf4(const __grid_constant__ CUtensorMap tmap_w, const GemmArgs a)
+    k_grouped_gemm_nvf4(const __grid_constant__ CUtensorMap tmap_w0, const __grid_constant__ CUtensorMap tmap_w1,
+                        const GemmArgs a)
 {
     using C = Cfg<kSwap>;
     using LY = Lay<kSwap>;
@@ -216,7 +247,8 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         ptx::mbar_init(&st.xchg_empty, 64);
         st.abort = 0;
         ptx::fence_mbar_init();
-        ptx::prefetch_tmap(&tmap_w);
+        ptx::prefetch_tmap(&tmap_w0);
+        if (a.nphase > 1) ptx::prefetch_tmap(&tmap_w1);
     }
     if (warp == 1) {
         ptx::tmem_alloc(&st.tmem_base, LY::TMEM_COLS);
@@ -228,11 +260,9 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = st.tmem_base;
 
-    const int n_wb = a.N / W_ROWS;
-    const int total = st.tb_off[a.G] * n_wb;
-    const int k_stages = (a.K + 255) / 256;
-    const int k_blocks64 = a.K / 64;
-    const int64_t a_ld = a.K / 2, sf_ld = a.K / 16;
+    const int nblk = st.tb_off[a.G];
+    const int tiles0 = nblk * (a.p[0].N / W_ROWS);
+    const int total = tiles0 + (a.nphase > 1 ? nblk * (a.p[1].N / W_ROWS) : 0);
 
     if (warp == 0) {
         // ================================ weight producer
@@ -241,15 +271,18 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
-                const TileInfo ti = tile_info(st.tb_off, a, n_wb, C::ACT_ROWS, L);
-                const uint8_t* sf_src = a.b_sf + ((static_cast<int64_t>(ti.g) * n_wb + ti.nb) * k_blocks64) * SF_TILE;
+                const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, tiles0, L);
+                const GemmProblem& P = a.p[ti.ph];
+                const CUtensorMap* tm = ti.ph ? &tmap_w1 : &tmap_w0;
+                const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256, n_wb = P.N / W_ROWS;
+                const uint8_t* sf_src = P.b_sf + ((static_cast<int64_t>(ti.g) * n_wb + ti.nb) * kb64) * SF_TILE;
                 const int row = ti.nb * W_ROWS;
                 for (int kt = 0; kt < k_stages; ++kt) {
                     if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
                     uint8_t* sbase = smem + s * LY::STAGE_BYTES;
-                    const int nat = min(4, k_blocks64 - kt * 4);
+                    const int nat = min(4, kb64 - kt * 4);
                     ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + nat * SF_TILE);
-                    ptx::tma_load_3d(sbase + LY::OFF_W, &tmap_w, &st.full[s], kt * BK_BYTES, row, ti.g);
+                    ptx::tma_load_3d(sbase + LY::OFF_W, tm, &st.full[s], kt * BK_BYTES, row, ti.g);
                     ptx::bulk_load(sbase + LY::OFF_SFW, sf_src, nat * SF_TILE, &st.full[s]);
                     sf_src += 4 * SF_TILE;
                     if (++s == C::STAGES) { s = 0; ph ^= 1; }
@@ -270,6 +303,8 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
             uint32_t ph = 0, lt = 0;
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x, ++lt) {
+                const int kK = a.p[L >= tiles0 ? 1 : 0].K;
+                const int kb64 = kK / 64, k_stages = (kK + 255) / 256;
                 const uint32_t as = lt & 1, aph = (lt >> 1) & 1;
                 if (!ptx::mbar_wait(&st.acc_empty[as], aph ^ 1)) { set_abort(st, a.status); break; }
                 ptx::tc_fence_after();
@@ -279,7 +314,7 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                     if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
                     const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
                     const uint32_t tsfw = tmem + LY::SF_COL + s * 32, tsfact = tsfw + 16;
-                    const int nk = min(4, k_blocks64 - kt * 4);
+                    const int nk = min(4, kb64 - kt * 4);
                     for (int kk = 0; kk < nk; ++kk) {
                         ptx::tmem_cp_32x128b_x4(tsfw + kk * 4, dsfw0 + so + kk * kSfAdv);
                         ptx::tmem_cp_32x128b_x4(tsfact + kk * 4, dsfact0 + so + kk * kSfAdv);
@@ -304,12 +339,13 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         // ================================ activation producers (row gather)
         // Warp w2 = warp - 2 fills rows [w2 * RW, w2 * RW + RW) of the tile. Lanes run along rows:
         // 8 lanes copy the 8 16-byte chunks of one row's 128-byte K-slice (one cache line), 4 lanes
-        // the 4 scale words of one row, so each warp instruction touches few cache lines.
+        // the 4 scale words of one row, so each warp instruction touches few cache lines. Scales
+        // stored in token-block tiles are copied as whole 512-byte tiles (both warps share them).
         constexpr int RW = C::ACT_ROWS / 2;      // rows per producer warp
         constexpr int NCR = RW / 4;              // code rows per lane (4 rows per warp instruction)
         constexpr int NSR = RW / 8;              // scale rows per lane (8 rows per warp instruction)
         constexpr int LAG = C::STAGES - 2;       // stages in flight before one is published
-        const int w2 = warp - 2;
+        const int w2 = warp - 2, pt = tid - 64;
         const int chunk = lane & 7, word = lane & 3;
         const uint8_t* cptr[NCR];
         const uint8_t* sptr[NSR];
@@ -318,31 +354,40 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         uint32_t ph = 0, issued = 0;
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
-            const TileInfo ti = tile_info(st.tb_off, a, n_wb, C::ACT_ROWS, L);
+            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, tiles0, L);
+            const GemmProblem& P = a.p[ti.ph];
+            const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
+            const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
+            if (ti.ph == 1) {
+                // the down GEMM reads h: wait until every gate/up tile of this token block stored it
+                const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS);
+                if (!spin_until(a.ready + ti.tbg, target)) { set_abort(st, a.status); break; }
+            }
             // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row
             int64_t srcv[(RW + 31) / 32];
 #pragma unroll
             for (int h = 0; h < (RW + 31) / 32; ++h) {
                 const int r = w2 * RW + h * 32 + lane;
                 const int64_t p = ti.row0 + r;
-                srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (a.a_row ? static_cast<int64_t>(__ldg(a.a_row + p)) : p) : -1;
+                srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (P.a_row ? static_cast<int64_t>(__ldg(P.a_row + p)) : p) : -1;
             }
             cvalid = 0;
             svalid = 0;
 #pragma unroll
             for (int i = 0; i < NCR; ++i) {
-                const int rl = i * 4 + (lane >> 3);  // row within this warp's slice
+                const int rl = i * 4 + (lane >> 3);  // row within this warp's slice (same word of srcv in all lanes)
                 const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
-                cptr[i] = src >= 0 ? a.a_codes + src * a_ld + chunk * 16 : a.a_codes;
+                cptr[i] = src >= 0 ? P.a_codes + src * a_ld + chunk * 16 : P.a_codes;
                 if (src >= 0) cvalid |= 1u << i;
             }
 #pragma unroll
             for (int i = 0; i < NSR; ++i) {
                 const int rl = i * 8 + (lane >> 2);
                 const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
-                sptr[i] = src >= 0 ? a.a_sf + src * sf_ld + word * 4 : a.a_sf;
+                sptr[i] = src >= 0 ? P.a_sf + src * sf_ld + word * 4 : P.a_sf;
                 if (src >= 0) svalid |= 1u << i;
             }
+            const uint8_t* sf_tiles = P.a_sf + static_cast<int64_t>(ti.tbg) * kb64 * SF_TILE;
             for (int kt = 0; kt < k_stages; ++kt) {
                 if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
                 uint8_t* sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
@@ -352,14 +397,26 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                 for (int i = 0; i < NCR; ++i) {
                     const int r = w2 * RW + i * 4 + (lane >> 3);
                     const bool v = ((cvalid >> i) & 1u) && kin;
-                    ptx::cp_async_16(sact + r * 128 + ((chunk ^ (r & 7)) * 16), v ? cptr[i] + kt * BK_BYTES : a.a_codes, v);
+                    ptx::cp_async_16(sact + r * 128 + ((chunk ^ (r & 7)) * 16), v ? cptr[i] + kt * BK_BYTES : P.a_codes, v);
                 }
-                const bool kin_s = static_cast<int64_t>(kt) * 16 + word * 4 < sf_ld;
+                if (P.a_sf_tiled) {
+                    // the stage's (up to) 4 scale tiles, 32 lines x 16 bytes each, 2 copies per thread
+                    const int nat = min(4, kb64 - kt * 4);
 #pragma unroll
-                for (int i = 0; i < NSR; ++i) {
-                    const int r = w2 * RW + i * 8 + (lane >> 2);
-                    const bool v = ((svalid >> i) & 1u) && kin_s;
-                    ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : a.a_sf, v);
+                    for (int c = pt; c < 4 * 32; c += kNumActProducers) {
+                        const int j = c >> 5, line = c & 31;
+                        const bool v = j < nat;
+                        ptx::cp_async_16(ssf + j * SF_TILE + line * 16,
+                                         v ? sf_tiles + (static_cast<int64_t>(kt) * 4 + j) * SF_TILE + line * 16 : P.a_sf, v);
+                    }
+                } else {
+                    const bool kin_s = static_cast<int64_t>(kt) * 16 + word * 4 < sf_ld;
+#pragma unroll
+                    for (int i = 0; i < NSR; ++i) {
+                        const int r = w2 * RW + i * 8 + (lane >> 2);
+                        const bool v = ((svalid >> i) & 1u) && kin_s;
+                        ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : P.a_sf, v);
+                    }
                 }
                 ptx::cp_async_commit();
                 ++issued;
@@ -383,27 +440,30 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         // ================================ epilogue
         const int ew = warp - 4;
         const int q = warp & 3;  // TMEM lane quarter of this warp
-        uint32_t lt = 0;
+        uint32_t lt = 0, xt = 0;
         for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x, ++lt) {
-            const TileInfo ti = tile_info(st.tb_off, a, n_wb, C::ACT_ROWS, L);
+            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, tiles0, L);
+            const GemmProblem& P = a.p[ti.ph];
             const uint32_t as = lt & 1, aph = (lt >> 1) & 1;
             const bool got = ptx::mbar_wait(&st.acc_full[as], aph);
             __syncwarp();
             if (!__all_sync(0xFFFFFFFFu, got)) { set_abort(st, a.status); break; }
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + as * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-            const float sa = __ldg(a.a_scale + (a.a_scale_per_group ? ti.g : 0));
+            const float sa = __ldg(P.a_scale + (P.a_scale_per_group ? ti.g : 0));
+            const int I = P.N / 2;  // h columns (SwiGLU)
+            // scale tile of h for this token block and weight block: [token block][I/64][512 bytes]
+            uint8_t* hsf_tile = P.out_sf_tiled ? P.out_sf + (static_cast<int64_t>(ti.tbg) * (I / 64) + ti.nb) * SF_TILE : nullptr;
             if constexpr (!kSwap) {
                 // ---- TMEM lane = token row r; columns = weight rows of block nb
                 const int half = ew >> 2;
                 const int r = q * 32 + lane;
                 const bool valid = r < ti.rows;
                 const int64_t p = ti.row0 + r;
-                if (a.epilogue == kEpiSwiGLU) {
-                    const float sg = sa * __ldg(a.b_scale + 2 * ti.g), su = sa * __ldg(a.b_scale + 2 * ti.g + 1);
-                    const float S = __ldg(a.epi_scale + ti.g);
+                if (P.epilogue == kEpiSwiGLU) {
+                    const float sg = sa * __ldg(P.b_scale + 2 * ti.g), su = sa * __ldg(P.b_scale + 2 * ti.g + 1);
+                    const float S = __ldg(P.epi_scale + ti.g);
                     const float inv_six_s = 1.0f / (6.0f * S);
-                    const int I = a.N / 2;
                     uint32_t cw[4], sfw = 0;
 #pragma unroll
                     for (int b = 0; b < 2; ++b) {
@@ -421,10 +481,14 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                         cw[2 * b + 1] = hi;
                     }
                     if (valid) {
-                        uint8_t* hrow = static_cast<uint8_t*>(a.out) + p * (I / 2) + ti.nb * 32 + half * 16;
+                        uint8_t* hrow = static_cast<uint8_t*>(P.out) + p * (I / 2) + ti.nb * 32 + half * 16;
                         *reinterpret_cast<uint4*>(hrow) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                        *reinterpret_cast<uint16_t*>(a.out_sf + p * (I / 16) + ti.nb * 4 + half * 2) =
-                            static_cast<uint16_t>(sfw);
+                        if (P.out_sf_tiled)
+                            *reinterpret_cast<uint16_t*>(hsf_tile + (r % 32) * 16 + (r / 32) * 4 + half * 2) =
+                                static_cast<uint16_t>(sfw);
+                        else
+                            *reinterpret_cast<uint16_t*>(P.out_sf + p * (I / 16) + ti.nb * 4 + half * 2) =
+                                static_cast<uint16_t>(sfw);
                     }
                 } else {
 #pragma unroll 1
@@ -434,18 +498,18 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                         ptx::tmem_ld_wait();
                         int col;
                         float sb;
-                        if (a.gate_up) {
+                        if (P.gate_up) {
                             const int upper = c0 >= 64;
-                            col = (upper ? a.N / 2 : 0) + ti.nb * 64 + (c0 & 63);
-                            sb = __ldg(a.b_scale + 2 * ti.g + upper);
+                            col = (upper ? P.N / 2 : 0) + ti.nb * 64 + (c0 & 63);
+                            sb = __ldg(P.b_scale + 2 * ti.g + upper);
                         } else {
                             col = ti.nb * W_ROWS + c0;
-                            sb = __ldg(a.b_scale + ti.g);
+                            sb = __ldg(P.b_scale + ti.g);
                         }
                         const float s = sa * sb;
                         if (valid) {
-                            if (a.epilogue == kEpiF32) {
-                                float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + p * a.N + col);
+                            if (P.epilogue == kEpiF32) {
+                                float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + p * P.N + col);
 #pragma unroll
                                 for (int i = 0; i < 4; ++i)
                                     o[i] = make_float4(__uint_as_float(v[4 * i]) * s, __uint_as_float(v[4 * i + 1]) * s,
@@ -456,7 +520,7 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                                 for (int i = 0; i < 8; ++i)
                                     w[i] = f32_to_bf16(__uint_as_float(v[2 * i]) * s) |
                                            (f32_to_bf16(__uint_as_float(v[2 * i + 1]) * s) << 16);
-                                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.out) + p * a.N + col);
+                                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + p * P.N + col);
                                 o[0] = make_uint4(w[0], w[1], w[2], w[3]);
                                 o[1] = make_uint4(w[4], w[5], w[6], w[7]);
                             }
@@ -471,11 +535,12 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                 ptx::tmem_ld16(tbase + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                 ptx::tmem_ld_wait();
                 const int nv = ti.rows;
-                if (a.epilogue == kEpiSwiGLU) {
+                if (P.epilogue == kEpiSwiGLU) {
                     // interleaved gate/up block: lanes 0..63 gate rows, 64..127 the matching up rows
                     SwapXchg& xg = *reinterpret_cast<SwapXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kSwap>));
-                    const float sg = sa * __ldg(a.b_scale + 2 * ti.g), su = sa * __ldg(a.b_scale + 2 * ti.g + 1);
-                    const uint32_t xph = lt & 1;
+                    const float sg = sa * __ldg(P.b_scale + 2 * ti.g), su = sa * __ldg(P.b_scale + 2 * ti.g + 1);
+                    const uint32_t xph = xt & 1;
+                    ++xt;
                     bool xok = true;
                     if (q >= 2) {
                         xok = ptx::mbar_wait(&st.xchg_empty, xph ^ 1);
@@ -490,9 +555,8 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                     }
                     if (!xok) set_abort(st, a.status);
                     if (q < 2 && xok) {
-                        const float S = __ldg(a.epi_scale + ti.g);
+                        const float S = __ldg(P.epi_scale + ti.g);
                         const float inv_six_s = 1.0f / (6.0f * S);
-                        const int I = a.N / 2;
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
                             if (t < nv) {  // warp-uniform
@@ -507,9 +571,14 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                                 const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);
                                 const int64_t p = ti.row0 + t;
                                 if ((lane & 1) == 0)
-                                    static_cast<uint8_t*>(a.out)[p * (I / 2) + ti.nb * 32 + m / 2] =
+                                    static_cast<uint8_t*>(P.out)[p * (I / 2) + ti.nb * 32 + m / 2] =
                                         static_cast<uint8_t>(code | (other << 4));
-                                if ((lane & 15) == 0) a.out_sf[p * (I / 16) + ti.nb * 4 + m / 16] = static_cast<uint8_t>(sf);
+                                if ((lane & 15) == 0) {
+                                    if (P.out_sf_tiled)
+                                        hsf_tile[t * 16 + m / 16] = static_cast<uint8_t>(sf);
+                                    else
+                                        P.out_sf[p * (I / 16) + ti.nb * 4 + m / 16] = static_cast<uint8_t>(sf);
+                                }
                             }
                         }
                     }
@@ -517,13 +586,13 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                 } else {
                     int col;
                     float sb;
-                    if (a.gate_up) {
+                    if (P.gate_up) {
                         const int upper = m >= 64;
-                        col = (upper ? a.N / 2 : 0) + ti.nb * 64 + (m & 63);
-                        sb = __ldg(a.b_scale + 2 * ti.g + upper);
+                        col = (upper ? P.N / 2 : 0) + ti.nb * 64 + (m & 63);
+                        sb = __ldg(P.b_scale + 2 * ti.g + upper);
                     } else {
                         col = ti.nb * W_ROWS + m;
-                        sb = __ldg(a.b_scale + ti.g);
+                        sb = __ldg(P.b_scale + ti.g);
                     }
                     const float s = sa * sb;
 #pragma unroll
@@ -531,16 +600,25 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                         if (t < nv) {
                             const int64_t p = ti.row0 + t;
                             const float val = __uint_as_float(v[t]) * s;
-                            if (a.epilogue == kEpiF32)
-                                static_cast<float*>(a.out)[p * a.N + col] = val;
+                            if (P.epilogue == kEpiF32)
+                                static_cast<float*>(P.out)[p * P.N + col] = val;
                             else
-                                static_cast<uint16_t*>(a.out)[p * a.N + col] = static_cast<uint16_t>(f32_to_bf16(val));
+                                static_cast<uint16_t*>(P.out)[p * P.N + col] = static_cast<uint16_t>(f32_to_bf16(val));
                         }
                     }
                 }
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&st.acc_empty[as]);
+            if (a.nphase > 1 && ti.ph == 0) {
+                // publish this warp's part of h for the down GEMM of the same token block: the warp
+                // barrier orders the lanes' stores before lane 0's (cumulative) fence and count
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    atomicAdd(a.ready + ti.tbg, 1);
+                }
+            }
         }
     }
 
@@ -556,6 +634,8 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
 
 size_t grouped_gemm_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
 
+int gemm_act_rows(bool weights_on_m) { return weights_on_m ? Cfg<true>::ACT_ROWS : Cfg<false>::ACT_ROWS; }
+
 template <bool kSwap>
 static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream)
 {
@@ -566,16 +646,34 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    CUtensorMap tmap;
-    CUresult cr = encode_tmap_3d_u8(&tmap, a.b_codes, static_cast<uint64_t>(a.K / 2), static_cast<uint64_t>(a.N),
-                                    static_cast<uint64_t>(a.G), BK_BYTES, W_ROWS);
-    if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    CUtensorMap tmap[2];
+    for (int i = 0; i < a.nphase; ++i) {
+        const GemmProblem& P = a.p[i];
+        CUresult cr = encode_tmap_3d_u8(&tmap[i], P.b_codes, static_cast<uint64_t>(P.K / 2), static_cast<uint64_t>(P.N),
+                                        static_cast<uint64_t>(a.G), BK_BYTES, W_ROWS);
+        if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    if (a.nphase == 1) tmap[1] = tmap[0];
     const int act_rows = Cfg<kSwap>::ACT_ROWS;
     const int64_t blocks_ub = (p_max + act_rows - 1) / act_rows + a.G;
-    const int64_t tiles_ub = blocks_ub * (a.N / W_ROWS);
+    const int64_t tiles_ub = blocks_ub * (a.p[0].N / W_ROWS);
     const int grid = static_cast<int>(tiles_ub < sms ? (tiles_ub < 1 ? 1 : tiles_ub) : sms);
-    k_grouped_gemm_nvf4<kSwap><<<grid, Lay<kSwap>::THREADS, smem_bytes<kSwap>(), stream>>>(tmap, a);
-    return cudaGetLastError();
+    if (a.nphase == 1) {
+        k_grouped_gemm_nvf4<kSwap><<<grid, Lay<kSwap>::THREADS, smem_bytes<kSwap>(), stream>>>(tmap[0], tmap[1], a);
+        return cudaGetLastError();
+    }
+    // two phases: CTAs wait on one another's results, so all of them must be resident
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Lay<kSwap>::THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<kSwap>();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_grouped_gemm_nvf4<kSwap>, tmap[0], tmap[1], a);
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream)

@@ -39,14 +39,14 @@ cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* sf, int G, int N
 // ---- grouped_gemm.cu
 enum EpiKind : int { kEpiF32 = 0, kEpiBF16 = 1, kEpiSwiGLU = 2 };
 
-struct GemmArgs {
+// One grouped GEMM over the groups of a launch (see grouped_gemm.cu).
+struct GemmProblem {
     const uint8_t* a_codes;   // [*][K/2]
-    const uint8_t* a_sf;      // [*][K/16]
+    const uint8_t* a_sf;      // [*][K/16] row-major, or token-block tiles when a_sf_tiled
     const float* a_scale;     // [1] or [G]
     int a_scale_per_group;
     const int32_t* a_row;     // nullable gather index, [P]
-    const int32_t* offsets;   // [G+1]
-    int G;
+    int a_sf_tiled;           // A scales in tiles [token block][K/64][512 B] (written by a SwiGLU phase)
     const uint8_t* b_codes;   // prepacked [G][N][K/2] (described by the tensor map)
     const uint8_t* b_sf;      // prepacked tiles [G][N/128][K/64][512]
     const float* b_scale;     // [G][gate_up ? 2 : 1]
@@ -55,7 +55,18 @@ struct GemmArgs {
     int epilogue;
     const float* epi_scale;   // [G] static scale of h (SwiGLU epilogue)
     void* out;
-    uint8_t* out_sf;
+    uint8_t* out_sf;          // SwiGLU: h scales, row-major [P][N/32] or tiles when out_sf_tiled
+    int out_sf_tiled;
+};
+
+// A launch: one problem, or the gate/up problem (phase 0) followed by the down problem (phase 1)
+// over the same groups; phase-1 tiles of a token block wait for that block's phase-0 tiles.
+struct GemmArgs {
+    GemmProblem p[2];
+    int nphase;
+    const int32_t* offsets;   // [G+1]
+    int G;
+    int32_t* ready;           // [token blocks], zeroed before a two-phase launch
     int* status;
 };
 constexpr int kGemmMaxG = 1025;
@@ -64,6 +75,7 @@ constexpr int kGemmMaxG = 1025;
 enum GemmSchedule : int { kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream);
 size_t grouped_gemm_smem_bytes();
+int gemm_act_rows(bool weights_on_m);  // token rows per tile of a schedule
 
 // ---- combine.cu
 cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* shared_g, const int32_t* src_perm, int T,
