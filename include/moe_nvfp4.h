@@ -34,6 +34,8 @@
  *     They return MOE_OK after a successful launch; argument errors are detected on the host
  *     before any launch and return an error code (moe_last_error_detail() gives the numbers).
  *   - Scratch comes from a caller workspace of moe_workspace_bytes() bytes (256-byte aligned).
+ *     Its first 256 bytes (status word and launch counters) must be zero before its first use;
+ *     the calls leave the counters at zero. One workspace serves one stream at a time.
  *     Kernels record device-side failures (a bounded wait that ran out) in a status word in the
  *     workspace; moe_read_device_status() synchronises `stream` and returns it.
  *   - Shapes: H and I multiples of 128; 1 <= k <= min(E, 32); 1 <= E <= 1024; T >= 0.
@@ -111,7 +113,8 @@ moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, con
 /* ---------------------------------------------------------------------------------------------
  * moe_route_topk -- router GEMM, FP32 softmax, top-k with renormalised weights, shared gate.
  *   The capy-flash README v0.5.4 ("Measured") notes that the summation order of the router can
- *   flip exact ties; here ties are broken by the lowest expert id.
+ *   flip exact ties; here ties are broken by the lowest expert id. A NaN logit ranks below every
+ *   number, so the ids are always in [0, E).
  *   x: bf16 [T][H]; uses L->w_router, L->logit_bias, L->H, L->E, L->k.
  *   topk_ids: int32 [T][k] (routing order: weight non-increasing); topk_w: FP32 [T][k];
  *   shared_g: nullable FP32 [T]; logits_out: nullable FP32 [T][E] (bias included).
@@ -195,7 +198,9 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
  *   (cudaEvent_t handles) on `stream` at the stage boundaries: events[0] before the activation
  *   quantizer, [1] after it, [2] after routing (logits + top-k), [3] after the permutation, [4]
  *   after the expert GEMMs (gate/up + SwiGLU + requantisation + down, one launch), [5] after the
- *   combine. n_events: 0 (plain forward) or 6. The library creates and destroys no event.
+ *   combine. For small batches (T <= 64 and T*k <= 512) quantisation, routing and permutation run
+ *   as one launch between events [0] and [1]; [2] and [3] then follow [1] directly.
+ *   n_events: 0 (plain forward) or 6. The library creates and destroys no event.
  * ------------------------------------------------------------------------------------------- */
 moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
                                         uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream,

@@ -389,17 +389,28 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     };
 
     MOE_CUDA(mark(0), "event record");
-    // W4A4: quantize the layer input once per token (dynamic tensor scale)
-    MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s), "quantize");
-    MOE_CUDA(mark(1), "event record");
-    // router, softmax, top-k, shared gate
-    MOE_CUDA(launch_router_logits(x, T, H, E, L->w_router, L->logit_bias, PF(W.logits), s), "router");
-    MOE_CUDA(launch_topk(PF(W.logits), T, E, k, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), nullptr, s), "top-k");
-    MOE_CUDA(mark(2), "event record");
-    // permutation by expert id, the shared expert appended as group E
-    MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), nullptr, P32(W.perm_src),
-                            P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
-             "permute");
+    if (front_fits(T, H, E, k)) {
+        // small batch: quantisation, router, top-k, shared gate and permutation in one launch
+        MOE_CUDA(launch_front(x, T, H, E, k, L->w_router, L->logit_bias, PF(W.logits), P8(W.x_codes), P8(W.x_sf),
+                              &hdr->s_x, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), P32(W.offsets),
+                              P32(W.perm_src), P32(W.src_perm), P32(W.row_token), &hdr->ticket, s),
+                 "front");
+        MOE_CUDA(mark(1), "event record");
+        MOE_CUDA(mark(2), "event record");
+    } else {
+        // W4A4: quantize the layer input once per token (dynamic tensor scale)
+        MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s),
+                 "quantize");
+        MOE_CUDA(mark(1), "event record");
+        // router, softmax, top-k, shared gate
+        MOE_CUDA(launch_router_logits(x, T, H, E, L->w_router, L->logit_bias, PF(W.logits), s), "router");
+        MOE_CUDA(launch_topk(PF(W.logits), T, E, k, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), nullptr, s), "top-k");
+        MOE_CUDA(mark(2), "event record");
+        // permutation by expert id, the shared expert appended as group E
+        MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), nullptr, P32(W.perm_src),
+                                P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
+                 "permute");
+    }
     MOE_CUDA(mark(3), "event record");
     // expert GEMMs in one launch: gate/up with the fused SwiGLU + NVFP4 requantisation of h,
     // then down (bf16 rows in permuted order); a down tile waits for its token block's h

@@ -20,7 +20,8 @@ struct WsHeader {
     int status;            // OR of kDev* bits
     unsigned amax_bits;    // bit pattern of amax(|x|) (non-negative floats order like integers)
     float s_x;             // tensor scale of the layer input
-    int pad[61];
+    unsigned ticket;       // CTAs of the one-launch front half that finished (zero between calls)
+    int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

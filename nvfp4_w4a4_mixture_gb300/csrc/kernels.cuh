@@ -32,6 +32,13 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int wit
 // tile_off[g] = sum_{g' < g} ceil((offsets[g'+1] - offsets[g']) / kGemmBM), g = 0..G.
 cudaError_t launch_tile_offsets(const int32_t* offsets, int G, int32_t* tile_off, cudaStream_t stream);
 
+// ---- front.cu (small batches: quantize + router + top-k + permute in one launch)
+bool front_fits(int T, int H, int E, int k);
+cudaError_t launch_front(const uint16_t* x, int T, int H, int E, int k, const uint16_t* w_router, const float* bias,
+                         float* logits, uint8_t* xq_codes, uint8_t* xq_sf, float* s_x, int32_t* topk_ids, float* topk_w,
+                         float* shared_g, int32_t* offsets, int32_t* perm_src, int32_t* src_perm, int32_t* row_token,
+                         unsigned* ticket, cudaStream_t stream);
+
 // ---- prepack.cu
 cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* sf, int G, int N, int K, int interleave,
                            uint8_t* codes_out, uint8_t* sf_out, cudaStream_t stream);

@@ -105,10 +105,11 @@ __global__ void __launch_bounds__(kTopkThreads)
         if (e < E) {
             live |= 1u << i;
             if (logits_out) logits_out[static_cast<int64_t>(t) * E + e] = v[i];
+            if (v[i] != v[i]) v[i] = -INFINITY;  // a NaN logit ranks below every number
         }
     }
     for (int j = 0; j < k; ++j) {
-        float b = -INFINITY;  // (-inf, INT_MAX) loses to every live (finite) logit
+        float b = -INFINITY;  // (-inf, INT_MAX) loses to every live logit
         int bi = 0x7FFFFFFF;
 #pragma unroll
         for (int i = 0; i < kTopkPer; ++i) {

@@ -60,11 +60,12 @@ def quantized_experts(seed, E, H, I, experts, layer=0):
 
 
 @functools.lru_cache(maxsize=4)
-def layer_case(config, seed=0, sample=None):
+def layer_case(config, seed=0, sample=None, T=None):
     """Inputs of one layer call. sample: number of tokens whose experts get real weights (None: all
-    tokens). Returns a dict of numpy arrays."""
+    tokens); T: token count other than the configuration's. Returns a dict of numpy arrays."""
     c = wl.CONFIGS[config]
-    H, E, k, I, T = c["H"], c["E"], c["k"], c["I"], c["T"]
+    H, E, k, I = c["H"], c["E"], c["k"], c["I"]
+    T = c["T"] if T is None else int(T)
     w_r = wl.gen_router(seed, E, H)
     bias = bias_for(config)
     x, redrawn = draw_x(seed, T, H, w_r, k, bias=None if bias is None else bias.astype(np.float64))

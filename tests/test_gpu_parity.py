@@ -350,5 +350,30 @@ def test_layer_prefill4k_sampled(moe):
     _check_layer(moe, I_.layer_case("prefill4k", sample=12))
 
 
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 63, 64, 65, 130])
+def test_layer_tiny_token_counts(moe, T):
+    # T <= 64 with T*k <= 512 takes the one-launch front half, larger T the separate kernels;
+    # 8 tokens are staged per router pass, so 7/8/9 and 63/64/65 straddle its edges
+    _check_layer(moe, I_.layer_case("tiny", seed=T, T=T))
+
+
+@pytest.mark.parametrize("T", [51, 52])
+def test_layer_decode_shape_front_edge(moe, T):
+    # T*k = 510 is the largest assignment count of the one-launch front half at k = 10; 520 is not
+    _check_layer(moe, I_.layer_case("decode", seed=3, sample=6, T=T))
+
+
+def test_layer_repeat_bit_identical(moe):
+    # the front half's completion counter must be back at zero after every call
+    case = I_.layer_case("decode", seed=5, sample=4)
+    layer = gpu_layer(moe, case)
+    x = bf16_dev(case["x"])
+    ws = moe.Workspace(moe.moe_workspace_bytes(case["H"], case["E"], case["k"], case["I"], case["T"]))
+    outs = [moe.moe_layer_forward(layer, x, ws=ws).clone() for _ in range(4)]
+    moe.moe_read_device_status(ws=ws)
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
 def test_device_status_clean(moe):
     moe.moe_read_device_status()
