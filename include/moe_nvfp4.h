@@ -89,7 +89,9 @@ enum {
     /* Tile schedule (default: weights on M when p_max <= 64, else activations on M). Results agree
      * to FP32 summation order. */
     MOE_GEMM_SCHED_ACT_ON_M = 0x100,     /* 128 token rows x 128 weight rows per tile */
-    MOE_GEMM_SCHED_WEIGHTS_ON_M = 0x200  /* 128 weight rows x 32 token rows per tile (small groups) */
+    MOE_GEMM_SCHED_WEIGHTS_ON_M = 0x200, /* 128 weight rows x 32 token rows per tile (small groups) */
+    MOE_GEMM_SCHED_WIDE = 0x400          /* 128 token rows x 256 weight rows per tile (N % 256 == 0,
+                                          * else activations on M) */
 };
 
 /* ---------------------------------------------------------------------------------------------

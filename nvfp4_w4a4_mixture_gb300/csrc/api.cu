@@ -4,10 +4,12 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
 #include "../../include/moe_nvfp4.h"
+
 #include "kernels.cuh"
 
 namespace moe {
@@ -130,6 +132,15 @@ int device_sm_count()
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     return sms > 0 ? sms : 1;
+}
+
+bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_NVFP4_NO_PDL");
+        return !(v && v[0] == '1');
+    }();
+    return on;
 }
 
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
@@ -297,12 +308,14 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     if (N < 128 || N % 128 || K < 64 || K % 64 || K > 16384)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d: N must be a multiple of 128, K of 64 (<= 16384)", N, K);
     if (p_max < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "p_max=%lld < 0", (long long)p_max);
-    const int sched_bits = epilogue & (MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M);
-    if (sched_bits == (MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M))
-        return fail(MOE_ERR_INVALID_ARG, "epilogue=0x%x: pick one schedule flag", epilogue);
-    const int schedule = sched_bits == MOE_GEMM_SCHED_ACT_ON_M ? kSchedActOnM
-                         : sched_bits == MOE_GEMM_SCHED_WEIGHTS_ON_M ? kSchedWeightsOnM : kSchedAuto;
-    epilogue &= ~(MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M);
+    constexpr int kSchedBits = MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M | MOE_GEMM_SCHED_WIDE;
+    const int sched_bits = epilogue & kSchedBits;
+    if (sched_bits & (sched_bits - 1)) return fail(MOE_ERR_INVALID_ARG, "epilogue=0x%x: pick one schedule flag", epilogue);
+    const int schedule = sched_bits == MOE_GEMM_SCHED_ACT_ON_M      ? kSchedActOnM
+                         : sched_bits == MOE_GEMM_SCHED_WEIGHTS_ON_M ? kSchedWeightsOnM
+                         : sched_bits == MOE_GEMM_SCHED_WIDE         ? kSchedWide
+                                                                     : kSchedAuto;
+    epilogue &= ~kSchedBits;
     if (epilogue < MOE_EPI_F32 || epilogue > MOE_EPI_SWIGLU_NVFP4) return fail(MOE_ERR_INVALID_ARG, "epilogue=%d", epilogue);
     if (epilogue == MOE_EPI_SWIGLU_NVFP4 && (!gate_up || !epi_scale || !out_sf))
         return fail(MOE_ERR_INVALID_ARG, "the SwiGLU epilogue needs a gate/up bank, epi_scale and out_sf");
@@ -388,12 +401,15 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         return n_events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
 
+    const int n_ready = static_cast<int>((P + 31) / 32 + E + 1);  // token blocks of the expert GEMMs
+    const bool one_launch_front = front_fits(T, H, E, k);
     MOE_CUDA(mark(0), "event record");
-    if (front_fits(T, H, E, k)) {
+    if (one_launch_front) {
         // small batch: quantisation, router, top-k, shared gate and permutation in one launch
         MOE_CUDA(launch_front(x, T, H, E, k, L->w_router, L->logit_bias, PF(W.logits), P8(W.x_codes), P8(W.x_sf),
                               &hdr->s_x, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), P32(W.offsets),
-                              P32(W.perm_src), P32(W.src_perm), P32(W.row_token), &hdr->ticket, s),
+                              P32(W.perm_src), P32(W.src_perm), P32(W.row_token), &hdr->ticket, P32(W.ready),
+                              n_ready, s),
                  "front");
         MOE_CUDA(mark(1), "event record");
         MOE_CUDA(mark(2), "event record");
@@ -449,9 +465,12 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     ga.G = E + 1;
     ga.ready = P32(W.ready);
     ga.status = &hdr->status;
-    // few rows per expert (decode): weights on the MMA's M side; otherwise activations on M
-    const int sched = static_cast<int64_t>(T) * k <= 16LL * E ? kSchedWeightsOnM : kSchedActOnM;
-    MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, ((P + 31) / 32 + E + 1) * 4, s), "clear ready counters");
+    // few rows per expert (decode): 256-row weight tiles when H allows, else weights on the MMA's M
+    // side; otherwise 128 x 128 tiles with activations on M
+    const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
+    const int sched = small ? (gemm_wide_fits(ga) ? kSchedWide : kSchedWeightsOnM) : kSchedActOnM;
+    if (!one_launch_front)  // (the one-launch front half clears them itself)
+        MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready) * 4, s), "clear ready counters");
     MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");
     MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(kCombineThreads)
 {
     __shared__ int64_t rows_s[kMaxK + 1];
     __shared__ float w_s[kMaxK + 1];
+    ptx::griddep_wait();  // y comes from the launch before this one
+    ptx::griddep_launch_dependents();
     const int t = blockIdx.x;
     const int64_t tk = static_cast<int64_t>(t) * k;
     if (threadIdx.x < k) {
@@ -68,8 +70,8 @@ cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* 
 {
     if (T <= 0) return cudaSuccess;
     dim3 grid(T, (H + kCombineThreads * 8 - 1) / (kCombineThreads * 8));
-    k_combine<<<grid, kCombineThreads, 0, stream>>>(y, topk_w, shared_g, src_perm, T, k, H, residual, out);
-    return cudaGetLastError();
+    return launch_pdl(k_combine, grid, dim3(kCombineThreads), 0, stream, y, topk_w, shared_g, src_perm, T, k, H, residual,
+                      out);
 }
 
 }  // namespace moe

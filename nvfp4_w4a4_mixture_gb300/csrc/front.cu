@@ -24,7 +24,50 @@ constexpr int kFrontMaxE = 1024;
 constexpr int kFrontMaxT = 64;
 constexpr int kSmallFrontAssign = 512;  // T * k
 
-__device__ __forceinline__ bool before(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+// Order-preserving key of a logit: a larger logit has a larger key; every logit, -inf included, has
+// a key >= 1, and NaN ranks with -inf (so the selected ids always lie in [0, E)).
+__device__ __forceinline__ uint32_t order_key(float v)
+{
+    if (v != v) v = -INFINITY;
+    if (v == 0.0f) v = 0.0f;  // -0 ties with +0
+    const uint32_t b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// A lane's four largest keys, largest first (equal keys: lowest slot first); unused entries hold 0.
+struct Top4 {
+    uint32_t k[4];
+    int s[4];
+};
+
+__device__ __forceinline__ void lane_top4(const uint32_t (&key)[32], Top4& c)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        c.k[q] = 0u;
+        c.s[q] = 31;
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        uint32_t kv = key[i];
+        int sv = i;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // insertion: a strictly larger key moves ahead
+            const bool gt = kv > c.k[q];
+            const uint32_t tk = gt ? c.k[q] : kv;
+            const int ts = gt ? c.s[q] : sv;
+            c.k[q] = gt ? kv : c.k[q];
+            c.s[q] = gt ? sv : c.s[q];
+            kv = tk;
+            sv = ts;
+        }
+    }
+}
 
 // Exclusive scan of cnt[0..n) (n <= 1024) in place by 256 threads; returns the total.
 __device__ int32_t block_exclusive_scan(int32_t* cnt, int n, int32_t* wsum)
@@ -86,6 +129,8 @@ struct FrontArgs {
     int32_t* src_perm;
     int32_t* row_token;    // [T*k + T]
     unsigned* ticket;      // zero between calls
+    int32_t* ready;        // [n_ready] token-block counters of the expert GEMMs, zeroed here
+    int n_ready;
 };
 
 __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs a)
@@ -100,29 +145,43 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, E = a.E, T = a.T, k = a.k;
     const int e = blockIdx.x * kFrontWarps + warp;  // this warp's router row (E = shared gate)
+    const int n_logit_ctas = (E + 1 + kFrontWarps - 1) / kFrontWarps;
 
-    // ---- logits of this CTA's router rows, kFrontTT tokens per pass
-    for (int t0 = 0; t0 < T; t0 += kFrontTT) {
+    // The router row does not depend on the previous launch on the stream: its first 2048 columns
+    // are loaded before waiting for that launch (x and the routing outputs may still be in use there).
+    const bool has_row = blockIdx.x < n_logit_ctas && e <= E;
+    const uint16_t* wr = a.w_router + static_cast<int64_t>(has_row ? e : 0) * H;
+    uint4 wv0[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int h0 = u * 256 + lane * 8;
+        wv0[u] = has_row && h0 < H ? __ldg(reinterpret_cast<const uint4*>(wr + h0)) : make_uint4(0, 0, 0, 0);
+    }
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
+
+    // ---- logits of this CTA's router rows, kFrontTT tokens per pass (CTAs 0 .. n_logit_ctas-1)
+    for (int t0 = 0; t0 < T && blockIdx.x < n_logit_ctas; t0 += kFrontTT) {
         const int nt = min(kFrontTT, T - t0);
         const int vec_per_row = H / 8;
-        for (int i = tid; i < kFrontTT * vec_per_row; i += kFrontThreads) {
+#pragma unroll 4
+        for (int i = tid; i < nt * vec_per_row; i += kFrontThreads) {
             const int t = i / vec_per_row, c = i % vec_per_row;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < nt) v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t0 + t) * H) + c);
-            reinterpret_cast<uint4*>(xs + t * H)[c] = v;
+            reinterpret_cast<uint4*>(xs + t * H)[c] =
+                __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t0 + t) * H) + c);
         }
         __syncthreads();
-        if (e <= E) {
+        if (has_row) {
             float acc[kFrontTT];
 #pragma unroll
             for (int t = 0; t < kFrontTT; ++t) acc[t] = 0.0f;
-            const uint16_t* wr = a.w_router + static_cast<int64_t>(e) * H;
             for (int base = 0; base < H; base += 8 * 256) {
                 uint4 wv[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int h0 = base + u * 256 + lane * 8;
-                    wv[u] = h0 < H ? __ldg(reinterpret_cast<const uint4*>(wr + h0)) : make_uint4(0, 0, 0, 0);
+                    wv[u] = base == 0 ? wv0[u]
+                                      : (h0 < H ? __ldg(reinterpret_cast<const uint4*>(wr + h0)) : make_uint4(0, 0, 0, 0));
                 }
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -158,8 +217,8 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
         __syncthreads();
     }
 
-    // ---- CTA 0: W4A4 quantisation of x (tensor max, then one thread per 16-element block)
-    if (blockIdx.x == 0) {
+    // ---- last CTA: W4A4 quantisation of x (tensor max, then one thread per 16-element block)
+    if (blockIdx.x == n_logit_ctas) {
         const int64_t nblocks = static_cast<int64_t>(T) * H / 16;
         uint32_t m = 0;
         for (int64_t b = tid; b < nblocks; b += kFrontThreads) {
@@ -206,50 +265,49 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     if (!last_s) return;
     __threadfence();
 
-    // top-k per token: warp w takes tokens w, w + 8, ...; each lane holds 32 logits (E <= 1024)
+    // top-k per token: warp w takes tokens w, w + 8, ...; lane l holds logits l, l + 32, ... as
+    // order-preserving integer keys (a removed or absent entry has key 0, below every logit) and a
+    // cache of its four largest. A round takes the warp's largest cached key with one reduction and
+    // the lowest expert id holding it with a second; the winning lane pops its cache and rebuilds it
+    // from its remaining keys only when it runs empty.
     for (int t = warp; t < T; t += kFrontWarps) {
         const float* l = a.logits + static_cast<int64_t>(t) * (E + 1);
-        float v[32];
-        unsigned live = 0;
+        uint32_t key[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const int ee = i * 32 + lane;
-            v[i] = ee < E ? __ldcg(l + ee) : 0.0f;
-            if (v[i] != v[i]) v[i] = -INFINITY;  // a NaN logit ranks below every number: ids stay in [0, E)
-            if (ee < E) live |= 1u << i;
+            key[i] = ee < E ? order_key(__ldcg(l + ee)) : 0u;
         }
-        float sel_l = 0.0f, l0 = 0.0f;
+        Top4 c;
+        lane_top4(key, c);
+        float sel_l = 0.0f;
         int sel_i = 0;
+        uint32_t k0 = 0;
         for (int j = 0; j < k; ++j) {
-            float b = -INFINITY;
-            int bi = 0x7FFFFFFF;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int ee = i * 32 + lane;
-                if (((live >> i) & 1u) && before(v[i], ee, b, bi)) {
-                    b = v[i];
-                    bi = ee;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ob = __shfl_xor_sync(0xFFFFFFFFu, b, o);
-                const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-                if (before(ob, oi, b, bi)) {
-                    b = ob;
-                    bi = oi;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i * 32 + lane == bi) live &= ~(1u << i);
-            if (j == 0) l0 = b;
+            const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, c.k[0]);
+            const int widx = static_cast<int>(__reduce_min_sync(
+                0xFFFFFFFFu, c.k[0] == wmax ? static_cast<unsigned>(c.s[0] * 32 + lane) : 0x7FFFFFFFu));
+            if (j == 0) k0 = wmax;
             if (lane == j) {
-                sel_l = b;
-                sel_i = bi;
+                sel_l = key_value(wmax);
+                sel_i = widx;
+            }
+            if ((widx & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (i == c.s[0]) key[i] = 0u;
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    c.k[q] = c.k[q + 1];
+                    c.s[q] = c.s[q + 1];
+                }
+                c.k[3] = 0u;
+                c.s[3] = 31;
+                if (c.k[0] == 0u) lane_top4(key, c);
             }
         }
         // renormalised weights: softmax over the selected logits (the first one is the largest)
+        const float l0 = key_value(k0);
         const float p = lane < k ? expf(sel_l - l0) : 0.0f;
         float sum = p;
 #pragma unroll
@@ -261,7 +319,8 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
         }
         if (lane == 0) a.shared_g[t] = 1.0f / (1.0f + expf(-__ldcg(l + E)));
     }
-    // permutation: counts, exclusive scan over experts, rank = earlier entries with the same id
+    // permutation: counts, exclusive scan over experts, then warp 0 places the assignments in order,
+    // 32 at a time: rank = earlier lanes with the same id (match) + the id's running count
     const int n = T * k;
     for (int i = tid; i < E; i += kFrontThreads) cnt_s[i] = 0;
     __syncthreads();
@@ -273,16 +332,25 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
         a.offsets[E] = total;
         a.offsets[E + 1] = total + T;
     }
-    for (int f = tid; f < n; f += kFrontThreads) {
-        const int id = ids_s[f];
-        int r = 0;
-        for (int q = 0; q < f; ++q) r += ids_s[q] == id;
-        const int pos = cnt_s[id] + r;
-        a.perm_src[pos] = f;
-        a.src_perm[f] = pos;
-        a.row_token[pos] = f / k;
+    __syncthreads();
+    if (warp == 0) {
+        for (int c0 = 0; c0 < n; c0 += 32) {
+            const int f = c0 + lane;
+            const int id = f < n ? ids_s[f] : -1;
+            const unsigned m = __match_any_sync(0xFFFFFFFFu, id);
+            if (f < n) {
+                const int pos = cnt_s[id] + __popc(m & ((1u << lane) - 1u));
+                a.perm_src[pos] = f;
+                a.src_perm[f] = pos;
+                a.row_token[pos] = f / k;
+            }
+            __syncwarp();
+            if (f < n && (m >> lane) == 1u) cnt_s[id] += __popc(m);  // highest lane of each id
+            __syncwarp();
+        }
     }
     for (int t = tid; t < T; t += kFrontThreads) a.row_token[n + t] = t;
+    for (int i = tid; i < a.n_ready; i += kFrontThreads) a.ready[i] = 0;
     if (tid == 0) *a.ticket = 0u;  // every CTA has taken its ticket: ready for the next call
 }
 
@@ -294,7 +362,7 @@ bool front_fits(int T, int H, int E, int k)
 cudaError_t launch_front(const uint16_t* x, int T, int H, int E, int k, const uint16_t* w_router, const float* bias,
                          float* logits, uint8_t* xq_codes, uint8_t* xq_sf, float* s_x, int32_t* topk_ids, float* topk_w,
                          float* shared_g, int32_t* offsets, int32_t* perm_src, int32_t* src_perm, int32_t* row_token,
-                         unsigned* ticket, cudaStream_t stream)
+                         unsigned* ticket, int32_t* ready, int n_ready, cudaStream_t stream)
 {
     const size_t smem = static_cast<size_t>(kFrontTT) * H * sizeof(uint16_t);
     static bool attr_set = false;
@@ -304,10 +372,9 @@ cudaError_t launch_front(const uint16_t* x, int T, int H, int E, int k, const ui
         attr_set = true;
     }
     FrontArgs a{x, T, H, E, k, w_router, bias, logits, xq_codes, xq_sf, s_x, topk_ids, topk_w, shared_g, offsets,
-                perm_src, src_perm, row_token, ticket};
-    const int grid = (E + 1 + kFrontWarps - 1) / kFrontWarps;
-    k_decode_front<<<grid, kFrontThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+                perm_src, src_perm, row_token, ticket, ready, n_ready};
+    const int grid = (E + 1 + kFrontWarps - 1) / kFrontWarps + 1;  // router rows + one quantising CTA
+    return launch_pdl(k_decode_front, dim3(grid), dim3(kFrontThreads), smem, stream, a);
 }
 
 }  // namespace moe

@@ -36,43 +36,58 @@ namespace moe {
 namespace {
 
 constexpr int BK_BYTES = 128;              // K-stage: one 128-byte swizzle row = 256 E2M1 values
-constexpr int W_ROWS = 128;                // weight rows per tile (one TMA box)
 constexpr int SF_TILE = 512;               // scale factors of 128 rows x 4 K-blocks
 constexpr int SF_STAGE = 4 * SF_TILE;      // 4 MMA K-steps of 64 per stage
 constexpr int kNumActProducers = 64;       // warps 2-3; each arrives on every stage's full barrier
 
-template <bool kSwap>
+// Tile shapes. W_ROWS weight rows (one TMA box) by ACT_ROWS activation rows per tile; ACC_BUFS
+// accumulators of ACC_COLS tensor-memory columns.
+enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2 };
+template <int kMode>
 struct Cfg;
 template <>
-struct Cfg<false> {                        // activations on the MMA's M side
-    static constexpr int ACT_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128;
+struct Cfg<kModeActM> {                    // activations on the MMA's M side, 128 weight rows on N
+    static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
+    static constexpr bool SWAP = false;
 };
 template <>
-struct Cfg<true> {                         // weights on the MMA's M side
-    static constexpr int ACT_ROWS = 32, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32;
+struct Cfg<kModeSwap> {                    // weights on the MMA's M side, 32 activation rows on N
+    static constexpr int ACT_ROWS = 32, W_ROWS = 128, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 32;
+    static constexpr bool SWAP = true;
+};
+template <>
+struct Cfg<kModeWide> {                    // activations on M, 256 weight rows on N: half the MMAs and
+    // scale copies per weight byte of the 128-row shapes; the 256-column accumulator leaves room for
+    // one buffer only, so the epilogue frees it as soon as its rows are in registers
+    static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
+    static constexpr int MMA_M = 128, MMA_N = 256;
+    static constexpr bool SWAP = false;
 };
 
-template <bool kSwap>
+template <int kMode>
 struct Lay {
-    using C = Cfg<kSwap>;
-    static constexpr int W_BYTES = W_ROWS * BK_BYTES;
+    using C = Cfg<kMode>;
+    static constexpr int WB = C::W_ROWS / 128;  // 128-row weight blocks per tile (scale tiles per K-step)
+    static constexpr int W_BYTES = C::W_ROWS * BK_BYTES;
     static constexpr int ACT_BYTES = C::ACT_ROWS * BK_BYTES;
-    static constexpr int OFF_W = 0, OFF_ACT = W_BYTES, OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + SF_STAGE;
+    static constexpr int OFF_W = 0, OFF_ACT = W_BYTES, OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + WB * SF_STAGE;
     static constexpr int STAGE_BYTES = OFF_SFACT + SF_STAGE;
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
-    static constexpr int SF_COL = 2 * C::ACC_COLS;  // first scale-factor column; 32 per stage
+    static constexpr int SF_COL = C::ACC_BUFS * C::ACC_COLS;  // first scale-factor column
+    static constexpr int SFW_STEP_COLS = 4 * WB;               // weight scale columns per K-step
+    static constexpr int STAGE_SF_COLS = 4 * (SFW_STEP_COLS + 4);
     static constexpr int TMEM_COLS = 512;
     static constexpr int READY_PER_TILE = C::EPI_WARPS;  // epilogue warp arrivals per gate/up tile
-    static_assert(SF_COL + 32 * C::STAGES <= TMEM_COLS, "tensor memory budget");
+    static_assert(SF_COL + STAGE_SF_COLS * C::STAGES <= TMEM_COLS, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
 
-template <bool kSwap>
+template <int kMode>
 struct Tail {
-    uint64_t full[Cfg<kSwap>::STAGES];
-    uint64_t empty[Cfg<kSwap>::STAGES];
+    uint64_t full[Cfg<kMode>::STAGES];
+    uint64_t empty[Cfg<kMode>::STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -89,11 +104,11 @@ struct SwapXchg {
     float u[64][33];
 };
 
-template <bool kSwap>
+template <int kMode>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(Cfg<kSwap>::STAGES) * Lay<kSwap>::STAGE_BYTES + sizeof(Tail<kSwap>) +
-           (kSwap ? sizeof(SwapXchg) : 0);
+    return 1024 + static_cast<size_t>(Cfg<kMode>::STAGES) * Lay<kMode>::STAGE_BYTES + sizeof(Tail<kMode>) +
+           (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0);
 }
 
 struct TileInfo {
@@ -141,12 +156,13 @@ __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, in
 }
 
 // Tile L of the launch: phase-0 tiles first (token block major, weight block minor), then phase 1.
-__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmArgs& a, int act_rows, int tiles0, int L)
+__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmArgs& a, int act_rows, int w_rows,
+                                              int tiles0, int L)
 {
     TileInfo ti;
     ti.ph = L >= tiles0 ? 1 : 0;
     const int Lp = L - (ti.ph ? tiles0 : 0);
-    const int n_wb = a.p[ti.ph].N / W_ROWS;
+    const int n_wb = a.p[ti.ph].N / w_rows;
     ti.tbg = Lp / n_wb;
     ti.nb = Lp - ti.tbg * n_wb;
     int lo = 0, hi = a.G;  // tb_off[lo] <= tbg < tb_off[hi]
@@ -161,14 +177,14 @@ __device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmA
     return ti;
 }
 
-template <bool kSwap>
-__device__ __forceinline__ void set_abort(Tail<kSwap>& t, int* status)
+template <int kMode>
+__device__ __forceinline__ void set_abort(Tail<kMode>& t, int* status)
 {
     if (atomicExch(&t.abort, 1) == 0) record_status(status, kDevTimeoutGemm);
 }
 
-template <bool kSwap>
-__device__ __forceinline__ bool aborted(const Tail<kSwap>& t)
+template <int kMode>
+__device__ __forceinline__ bool aborted(const Tail<kMode>& t)
 {
     return *reinterpret_cast<const volatile int*>(&t.abort) != 0;
 }
@@ -220,16 +236,18 @@ __device__ __forceinline__ uint32_t encode16_rcp(const float (&v)[16], float S, 
 
 }  // namespace
 
-template <bool kSwap>
-__global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
+template <int kMode>
+__global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     k_grouped_gemm_nvf4(const __grid_constant__ CUtensorMap tmap_w0, const __grid_constant__ CUtensorMap tmap_w1,
                         const GemmArgs a)
 {
-    using C = Cfg<kSwap>;
-    using LY = Lay<kSwap>;
+    using C = Cfg<kMode>;
+    using LY = Lay<kMode>;
+    constexpr bool kSwap = C::SWAP;
+    constexpr int W_ROWS = C::W_ROWS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Tail<kSwap>& st = *reinterpret_cast<Tail<kSwap>*>(smem + C::STAGES * LY::STAGE_BYTES);
+    Tail<kMode>& st = *reinterpret_cast<Tail<kMode>*>(smem + C::STAGES * LY::STAGE_BYTES);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
     // ---- setup
@@ -238,7 +256,7 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
             ptx::mbar_init(&st.full[s], 1 + kNumActProducers);
             ptx::mbar_init(&st.empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::ACC_BUFS; ++s) {
             ptx::mbar_init(&st.acc_full[s], 1);
             ptx::mbar_init(&st.acc_empty[s], 32 * C::EPI_WARPS);
         }
@@ -254,6 +272,9 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         ptx::tmem_alloc(&st.tmem_base, LY::TMEM_COLS);
         ptx::tmem_relinquish();
     }
+    // everything above overlaps the previous launch; the group offsets and activations come from it
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
     block_tile_prefix(a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.wsum);
     ptx::tc_fence_before();
     __syncthreads();
@@ -271,19 +292,23 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
             uint32_t ph = 0;
             bool ok = true;
             for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
-                const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, tiles0, L);
+                const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
                 const GemmProblem& P = a.p[ti.ph];
                 const CUtensorMap* tm = ti.ph ? &tmap_w1 : &tmap_w0;
-                const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256, n_wb = P.N / W_ROWS;
-                const uint8_t* sf_src = P.b_sf + ((static_cast<int64_t>(ti.g) * n_wb + ti.nb) * kb64) * SF_TILE;
+                const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256, n_blk = P.N / 128;
+                // scale tiles of the tile's 128-row weight blocks: [G][N/128][K/64][512 bytes]
+                const uint8_t* sf_src = P.b_sf + ((static_cast<int64_t>(ti.g) * n_blk + ti.nb * LY::WB) * kb64) * SF_TILE;
                 const int row = ti.nb * W_ROWS;
                 for (int kt = 0; kt < k_stages; ++kt) {
                     if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
                     uint8_t* sbase = smem + s * LY::STAGE_BYTES;
                     const int nat = min(4, kb64 - kt * 4);
-                    ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + nat * SF_TILE);
+                    ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + LY::WB * nat * SF_TILE);
                     ptx::tma_load_3d(sbase + LY::OFF_W, tm, &st.full[s], kt * BK_BYTES, row, ti.g);
-                    ptx::bulk_load(sbase + LY::OFF_SFW, sf_src, nat * SF_TILE, &st.full[s]);
+#pragma unroll
+                    for (int j = 0; j < LY::WB; ++j)
+                        ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sf_src + static_cast<int64_t>(j) * kb64 * SF_TILE,
+                                       nat * SF_TILE, &st.full[s]);
                     sf_src += 4 * SF_TILE;
                     if (++s == C::STAGES) { s = 0; ph ^= 1; }
                 }
@@ -305,25 +330,39 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
             for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x, ++lt) {
                 const int kK = a.p[L >= tiles0 ? 1 : 0].K;
                 const int kb64 = kK / 64, k_stages = (kK + 255) / 256;
-                const uint32_t as = lt & 1, aph = (lt >> 1) & 1;
+                const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
                 if (!ptx::mbar_wait(&st.acc_empty[as], aph ^ 1)) { set_abort(st, a.status); break; }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem + as * C::ACC_COLS;
                 uint32_t acc = 0;
+                // one K-step: both scale tiles into tensor memory, then the MMA (the tensor pipe runs
+                // them in issue order); the issuing thread's own instruction count bounds the rate,
+                // so full stages take a straight-line path
+                // (a 256-row weight tile has two scale tiles per K-step: rows 128..255 go to the next
+                // four columns)
+                auto kstep = [&](uint64_t so, uint32_t tsfw, uint32_t tsfact, int kk) {
+                    const uint32_t tw = tsfw + kk * LY::SFW_STEP_COLS;
+#pragma unroll
+                    for (int j = 0; j < LY::WB; ++j)
+                        ptx::tmem_cp_32x128b_x4(tw + j * 4, dsfw0 + so + kk * kSfAdv + j * (SF_STAGE >> 4));
+                    ptx::tmem_cp_32x128b_x4(tsfact + kk * 4, dsfact0 + so + kk * kSfAdv);
+                    const uint64_t dw = dw0 + so + kk * kOpAdv, dact = dact0 + so + kk * kOpAdv;
+                    if (kSwap)
+                        ptx::mma_nvf4(d_tmem, dw, dact, idesc, tw, tsfact + kk * 4, acc);
+                    else
+                        ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsfact + kk * 4, tw, acc);
+                    acc = 1;
+                };
                 for (int kt = 0; kt < k_stages; ++kt) {
                     if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
                     const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
-                    const uint32_t tsfw = tmem + LY::SF_COL + s * 32, tsfact = tsfw + 16;
+                    const uint32_t tsfw = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS, tsfact = tsfw + 4 * LY::SFW_STEP_COLS;
                     const int nk = min(4, kb64 - kt * 4);
-                    for (int kk = 0; kk < nk; ++kk) {
-                        ptx::tmem_cp_32x128b_x4(tsfw + kk * 4, dsfw0 + so + kk * kSfAdv);
-                        ptx::tmem_cp_32x128b_x4(tsfact + kk * 4, dsfact0 + so + kk * kSfAdv);
-                        const uint64_t dw = dw0 + so + kk * kOpAdv, dact = dact0 + so + kk * kOpAdv;
-                        if (kSwap)
-                            ptx::mma_nvf4(d_tmem, dw, dact, idesc, tsfw + kk * 4, tsfact + kk * 4, acc);
-                        else
-                            ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsfact + kk * 4, tsfw + kk * 4, acc);
-                        acc = 1;
+                    if (nk == 4) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) kstep(so, tsfw, tsfact, kk);
+                    } else {
+                        for (int kk = 0; kk < nk; ++kk) kstep(so, tsfw, tsfact, kk);
                     }
                     ptx::tc_commit(&st.empty[s]);
                     if (++s == C::STAGES) { s = 0; ph ^= 1; }
@@ -354,7 +393,7 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         uint32_t ph = 0, issued = 0;
         bool ok = true;
         for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
-            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, tiles0, L);
+            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
             const GemmProblem& P = a.p[ti.ph];
             const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
             const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
@@ -442,84 +481,118 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
         const int q = warp & 3;  // TMEM lane quarter of this warp
         uint32_t lt = 0, xt = 0;
         for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x, ++lt) {
-            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, tiles0, L);
+            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
             const GemmProblem& P = a.p[ti.ph];
-            const uint32_t as = lt & 1, aph = (lt >> 1) & 1;
+            const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
+            // the tile's scales are loaded before waiting for its accumulator, hiding their latency:
+            // sb0 / sb1 the gate / up (or only) weight scale, S_h the tensor scale of h (SwiGLU)
+            const float sa = __ldg(P.a_scale + (P.a_scale_per_group ? ti.g : 0));
+            const float sb0 = __ldg(P.b_scale + (P.gate_up ? 2 * ti.g : ti.g));
+            const float sb1 = P.gate_up ? __ldg(P.b_scale + 2 * ti.g + 1) : sb0;
+            const float S_h = P.epilogue == kEpiSwiGLU ? __ldg(P.epi_scale + ti.g) : 1.0f;
             const bool got = ptx::mbar_wait(&st.acc_full[as], aph);
             __syncwarp();
             if (!__all_sync(0xFFFFFFFFu, got)) { set_abort(st, a.status); break; }
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + as * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
-            const float sa = __ldg(P.a_scale + (P.a_scale_per_group ? ti.g : 0));
             const int I = P.N / 2;  // h columns (SwiGLU)
             // scale tile of h for this token block and weight block: [token block][I/64][512 bytes]
             uint8_t* hsf_tile = P.out_sf_tiled ? P.out_sf + (static_cast<int64_t>(ti.tbg) * (I / 64) + ti.nb) * SF_TILE : nullptr;
             if constexpr (!kSwap) {
-                // ---- TMEM lane = token row r; columns = weight rows of block nb
+                // ---- TMEM lane = token row r; columns = the tile's weight rows. The warps of lane
+                // quarter q split the columns in two halves; each loads all of its columns, frees the
+                // accumulator, then converts and stores.
+                constexpr int CPW = W_ROWS / 2;  // accumulator columns per warp
+                constexpr int NLD = CPW / 16;
+                constexpr int NB = W_ROWS / 64;  // SwiGLU: 16-column blocks of h per warp
                 const int half = ew >> 2;
                 const int r = q * 32 + lane;
                 const bool valid = r < ti.rows;
+                const bool any = q * 32 < ti.rows;  // warp-uniform: the quarter holds rows of the tile
                 const int64_t p = ti.row0 + r;
-                if (P.epilogue == kEpiSwiGLU) {
-                    const float sg = sa * __ldg(P.b_scale + 2 * ti.g), su = sa * __ldg(P.b_scale + 2 * ti.g + 1);
-                    const float S = __ldg(P.epi_scale + ti.g);
-                    const float inv_six_s = 1.0f / (6.0f * S);
-                    uint32_t cw[4], sfw = 0;
+                const bool swiglu = P.epilogue == kEpiSwiGLU;
+                uint32_t v[NLD][16];
+                if (any) {
+                    // SwiGLU: h block beta = half * NB + b takes gate column c*128 + jj*16 and up column
+                    // + 64 (c = beta / 4, jj = beta % 4: 128-row blocks hold 64 gate then 64 up rows);
+                    // otherwise the warp's columns are [half * CPW, half * CPW + CPW)
 #pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        const int blk = half * 2 + b;  // 16 h columns: gate cols blk*16, up cols 64 + blk*16
-                        uint32_t gr[16], ur[16];
-                        ptx::tmem_ld16(tbase + blk * 16, gr);
-                        ptx::tmem_ld16(tbase + 64 + blk * 16, ur);
-                        ptx::tmem_ld_wait();
+                    for (int i = 0; i < NLD; ++i) {
+                        uint32_t col;
+                        if (swiglu) {
+                            const int beta = half * NB + (i >> 1);
+                            col = (beta >> 2) * 128 + (beta & 3) * 16 + (i & 1) * 64;
+                        } else {
+                            col = half * CPW + i * 16;
+                        }
+                        ptx::tmem_ld16(tbase + col, v[i]);
+                    }
+                    ptx::tmem_ld_wait();
+                }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&st.acc_empty[as]);
+                if (any && swiglu) {
+                    const float sg = sa * sb0, su = sa * sb1;
+                    const float S = S_h;
+                    const float inv_six_s = 1.0f / (6.0f * S);
+                    uint32_t cw[2 * NB], sfw = 0;
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
                         float h[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) h[i] = silu(__uint_as_float(gr[i]) * sg) * (__uint_as_float(ur[i]) * su);
+                        for (int i = 0; i < 16; ++i)
+                            h[i] = silu(__uint_as_float(v[2 * b][i]) * sg) * (__uint_as_float(v[2 * b + 1][i]) * su);
                         uint32_t lo, hi;
                         sfw |= encode16_rcp(h, S, inv_six_s, lo, hi) << (8 * b);
                         cw[2 * b] = lo;
                         cw[2 * b + 1] = hi;
                     }
                     if (valid) {
-                        uint8_t* hrow = static_cast<uint8_t*>(P.out) + p * (I / 2) + ti.nb * 32 + half * 16;
-                        *reinterpret_cast<uint4*>(hrow) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                        if (P.out_sf_tiled)
-                            *reinterpret_cast<uint16_t*>(hsf_tile + (r % 32) * 16 + (r / 32) * 4 + half * 2) =
-                                static_cast<uint16_t>(sfw);
-                        else
-                            *reinterpret_cast<uint16_t*>(P.out_sf + p * (I / 16) + ti.nb * 4 + half * 2) =
-                                static_cast<uint16_t>(sfw);
+                        const int beta0 = half * NB;  // first h block of this warp
+                        uint8_t* hrow = static_cast<uint8_t*>(P.out) + p * (I / 2) + ti.nb * (W_ROWS / 4) + beta0 * 8;
+#pragma unroll
+                        for (int b = 0; b < NB; b += 2)
+                            *reinterpret_cast<uint4*>(hrow + b * 8) = make_uint4(cw[2 * b], cw[2 * b + 1], cw[2 * b + 2], cw[2 * b + 3]);
+                        if (P.out_sf_tiled) {
+                            // tile of h's 64-column block nb * WB + beta0 / 4; the warp's bytes jj = beta0 % 4 ..
+                            uint8_t* t = P.out_sf + (static_cast<int64_t>(ti.tbg) * (I / 64) + ti.nb * LY::WB + (beta0 >> 2)) * SF_TILE +
+                                         (r % 32) * 16 + (r / 32) * 4 + (beta0 & 3);
+                            if constexpr (NB == 4) *reinterpret_cast<uint32_t*>(t) = sfw;
+                            else *reinterpret_cast<uint16_t*>(t) = static_cast<uint16_t>(sfw);
+                        } else {
+                            uint8_t* t = P.out_sf + p * (I / 16) + ti.nb * (W_ROWS / 32) + beta0;
+                            if constexpr (NB == 4) *reinterpret_cast<uint32_t*>(t) = sfw;
+                            else *reinterpret_cast<uint16_t*>(t) = static_cast<uint16_t>(sfw);
+                        }
                     }
-                } else {
-#pragma unroll 1
-                    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 16) {
-                        uint32_t v[16];
-                        ptx::tmem_ld16(tbase + c0, v);
-                        ptx::tmem_ld_wait();
+                } else if (any) {
+#pragma unroll
+                    for (int i = 0; i < NLD; ++i) {
+                        const int c0 = half * CPW + i * 16;  // tile column
                         int col;
                         float sb;
                         if (P.gate_up) {
-                            const int upper = c0 >= 64;
-                            col = (upper ? P.N / 2 : 0) + ti.nb * 64 + (c0 & 63);
-                            sb = __ldg(P.b_scale + 2 * ti.g + upper);
+                            const int cc = c0 & 127, upper = cc >= 64;
+                            col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
+                            sb = upper ? sb1 : sb0;
                         } else {
                             col = ti.nb * W_ROWS + c0;
-                            sb = __ldg(P.b_scale + ti.g);
+                            sb = sb0;
                         }
-                        const float s = sa * sb;
+                        const float sc = sa * sb;
                         if (valid) {
                             if (P.epilogue == kEpiF32) {
                                 float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + p * P.N + col);
 #pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    o[i] = make_float4(__uint_as_float(v[4 * i]) * s, __uint_as_float(v[4 * i + 1]) * s,
-                                                       __uint_as_float(v[4 * i + 2]) * s, __uint_as_float(v[4 * i + 3]) * s);
+                                for (int j = 0; j < 4; ++j)
+                                    o[j] = make_float4(__uint_as_float(v[i][4 * j]) * sc, __uint_as_float(v[i][4 * j + 1]) * sc,
+                                                       __uint_as_float(v[i][4 * j + 2]) * sc, __uint_as_float(v[i][4 * j + 3]) * sc);
                             } else {
                                 uint32_t w[8];
 #pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    w[i] = f32_to_bf16(__uint_as_float(v[2 * i]) * s) |
-                                           (f32_to_bf16(__uint_as_float(v[2 * i + 1]) * s) << 16);
+                                for (int j = 0; j < 8; ++j)
+                                    w[j] = f32_to_bf16(__uint_as_float(v[i][2 * j]) * sc) |
+                                           (f32_to_bf16(__uint_as_float(v[i][2 * j + 1]) * sc) << 16);
                                 uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + p * P.N + col);
                                 o[0] = make_uint4(w[0], w[1], w[2], w[3]);
                                 o[1] = make_uint4(w[4], w[5], w[6], w[7]);
@@ -537,8 +610,8 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                 const int nv = ti.rows;
                 if (P.epilogue == kEpiSwiGLU) {
                     // interleaved gate/up block: lanes 0..63 gate rows, 64..127 the matching up rows
-                    SwapXchg& xg = *reinterpret_cast<SwapXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kSwap>));
-                    const float sg = sa * __ldg(P.b_scale + 2 * ti.g), su = sa * __ldg(P.b_scale + 2 * ti.g + 1);
+                    SwapXchg& xg = *reinterpret_cast<SwapXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kMode>));
+                    const float sg = sa * sb0, su = sa * sb1;
                     const uint32_t xph = xt & 1;
                     ++xt;
                     bool xok = true;
@@ -555,7 +628,7 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                     }
                     if (!xok) set_abort(st, a.status);
                     if (q < 2 && xok) {
-                        const float S = __ldg(P.epi_scale + ti.g);
+                        const float S = S_h;
                         const float inv_six_s = 1.0f / (6.0f * S);
 #pragma unroll
                         for (int t = 0; t < 32; ++t) {
@@ -589,10 +662,10 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                     if (P.gate_up) {
                         const int upper = m >= 64;
                         col = (upper ? P.N / 2 : 0) + ti.nb * 64 + (m & 63);
-                        sb = __ldg(P.b_scale + 2 * ti.g + upper);
+                        sb = upper ? sb1 : sb0;
                     } else {
                         col = ti.nb * W_ROWS + m;
-                        sb = __ldg(P.b_scale + ti.g);
+                        sb = sb0;
                     }
                     const float s = sa * sb;
 #pragma unroll
@@ -607,9 +680,9 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
                         }
                     }
                 }
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(&st.acc_empty[as]);
             }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&st.acc_empty[as]);
             if (a.nphase > 1 && ti.ph == 0) {
                 // publish this warp's part of h for the down GEMM of the same token block: the warp
                 // barrier orders the lanes' stores before lane 0's (cumulative) fence and count
@@ -632,17 +705,16 @@ __global__ void __launch_bounds__(Lay<kSwap>::THREADS, 1)
     }
 }
 
-size_t grouped_gemm_smem_bytes() { return smem_bytes<false>() > smem_bytes<true>() ? smem_bytes<false>() : smem_bytes<true>(); }
+int gemm_act_rows(bool weights_on_m) { return weights_on_m ? Cfg<kModeSwap>::ACT_ROWS : Cfg<kModeActM>::ACT_ROWS; }
 
-int gemm_act_rows(bool weights_on_m) { return weights_on_m ? Cfg<true>::ACT_ROWS : Cfg<false>::ACT_ROWS; }
-
-template <bool kSwap>
+template <int kMode>
 static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream)
 {
+    using C = Cfg<kMode>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_nvf4<kSwap>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem_bytes<kSwap>()));
+        cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm_nvf4<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_bytes<kMode>()));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -650,36 +722,46 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
     for (int i = 0; i < a.nphase; ++i) {
         const GemmProblem& P = a.p[i];
         CUresult cr = encode_tmap_3d_u8(&tmap[i], P.b_codes, static_cast<uint64_t>(P.K / 2), static_cast<uint64_t>(P.N),
-                                        static_cast<uint64_t>(a.G), BK_BYTES, W_ROWS);
+                                        static_cast<uint64_t>(a.G), BK_BYTES, C::W_ROWS);
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     if (a.nphase == 1) tmap[1] = tmap[0];
-    const int act_rows = Cfg<kSwap>::ACT_ROWS;
-    const int64_t blocks_ub = (p_max + act_rows - 1) / act_rows + a.G;
-    const int64_t tiles_ub = blocks_ub * (a.p[0].N / W_ROWS);
+    const int64_t blocks_ub = (p_max + C::ACT_ROWS - 1) / C::ACT_ROWS + a.G;
+    const int64_t tiles_ub = blocks_ub * (a.p[0].N / C::W_ROWS);
     const int grid = static_cast<int>(tiles_ub < sms ? (tiles_ub < 1 ? 1 : tiles_ub) : sms);
-    if (a.nphase == 1) {
-        k_grouped_gemm_nvf4<kSwap><<<grid, Lay<kSwap>::THREADS, smem_bytes<kSwap>(), stream>>>(tmap[0], tmap[1], a);
-        return cudaGetLastError();
-    }
+    if (a.nphase == 1)
+        return launch_pdl(k_grouped_gemm_nvf4<kMode>, dim3(grid), dim3(Lay<kMode>::THREADS), smem_bytes<kMode>(), stream,
+                          tmap[0], tmap[1], a);
     // two phases: CTAs wait on one another's results, so all of them must be resident
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(Lay<kSwap>::THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<kSwap>();
+    cfg.blockDim = dim3(Lay<kMode>::THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<kMode>();
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_grouped_gemm_nvf4<kSwap>, tmap[0], tmap[1], a);
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, k_grouped_gemm_nvf4<kMode>, tmap[0], tmap[1], a);
+}
+
+bool gemm_wide_fits(const GemmArgs& a)
+{
+    return a.p[0].N % Cfg<kModeWide>::W_ROWS == 0 && (a.nphase < 2 || a.p[1].N % Cfg<kModeWide>::W_ROWS == 0);
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream)
 {
-    const bool swap = schedule == kSchedWeightsOnM || (schedule == kSchedAuto && p_max <= 64);
-    return swap ? launch_t<true>(a, p_max, sms, stream) : launch_t<false>(a, p_max, sms, stream);
+    if (schedule == kSchedWide && !gemm_wide_fits(a)) schedule = kSchedActOnM;
+    if (schedule == kSchedAuto) schedule = p_max <= 64 ? kSchedWeightsOnM : kSchedActOnM;
+    switch (schedule) {
+        case kSchedWeightsOnM: return launch_t<kModeSwap>(a, p_max, sms, stream);
+        case kSchedWide: return launch_t<kModeWide>(a, p_max, sms, stream);
+        default: return launch_t<kModeActM>(a, p_max, sms, stream);
+    }
 }
 
 }  // namespace moe

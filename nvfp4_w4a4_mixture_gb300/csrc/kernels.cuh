@@ -37,7 +37,7 @@ bool front_fits(int T, int H, int E, int k);
 cudaError_t launch_front(const uint16_t* x, int T, int H, int E, int k, const uint16_t* w_router, const float* bias,
                          float* logits, uint8_t* xq_codes, uint8_t* xq_sf, float* s_x, int32_t* topk_ids, float* topk_w,
                          float* shared_g, int32_t* offsets, int32_t* perm_src, int32_t* src_perm, int32_t* row_token,
-                         unsigned* ticket, cudaStream_t stream);
+                         unsigned* ticket, int32_t* ready, int n_ready, cudaStream_t stream);
 
 // ---- prepack.cu
 cudaError_t launch_prepack(const uint8_t* codes, const uint8_t* sf, int G, int N, int K, int interleave,
@@ -77,11 +77,13 @@ struct GemmArgs {
     int* status;
 };
 constexpr int kGemmMaxG = 1025;
-// Tile schedules: activations on the MMA's M side (128-row token blocks) or weights on M
-// (32-row token blocks, for small groups); auto picks weights-on-M when p_max <= 64.
-enum GemmSchedule : int { kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2 };
+// Tile schedules: activations on the MMA's M side (128-row token blocks x 128 weight rows),
+// weights on M (128 weight rows x 32-row token blocks, for small groups), or activations on M with
+// 256 weight rows per tile (wide: fewer MMAs and scale copies per weight byte; needs N % 256 == 0,
+// else it falls back to activations on M). Auto picks weights-on-M when p_max <= 64.
+enum GemmSchedule : int { kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2, kSchedWide = 3 };
+bool gemm_wide_fits(const GemmArgs& a);
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream);
-size_t grouped_gemm_smem_bytes();
 int gemm_act_rows(bool weights_on_m);  // token rows per tile of a schedule
 
 // ---- combine.cu
@@ -90,6 +92,26 @@ cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* 
 
 // ---- api.cu
 int device_sm_count();
+
+// Launches with programmatic stream serialisation (the kernel calls ptx::griddep_wait() before it
+// touches anything the previous launch writes or reads), unless MOE_NVFP4_NO_PDL is set to 1.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 void set_last_error_detail(const char* msg);  // text returned by moe_last_error_detail()
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                            uint32_t box1);

@@ -74,6 +74,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
 }
 
 // ------------------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
+// before the previous kernel on the stream has finished. griddep_wait() blocks until that kernel has
+// completed and its memory operations are visible (a no-op without a programmatic dependency);
+// griddep_launch_dependents() lets the next such kernel start its own prologue early.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// ------------------------------------------------------------------------------------------------
 // TMA (tensor) and bulk copies, global -> shared, completion counted on an mbarrier
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m)

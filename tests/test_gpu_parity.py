@@ -222,11 +222,11 @@ def _gemm_case(seed, counts, H, I, N_kind):
     return dict(offsets=offsets, P=P, ac=ac, asf=asf, sa=sa, a_row=a_row, bc=bc, bs=bs, bsc=bsc, N=N, K=K)
 
 
-SCHEDS = ["act_on_m", "weights_on_m"]
+SCHEDS = ["act_on_m", "weights_on_m", "wide"]
 
 
 def _sched(moe, name):
-    return moe.SCHED_ACT_ON_M if name == "act_on_m" else moe.SCHED_WEIGHTS_ON_M
+    return {"act_on_m": moe.SCHED_ACT_ON_M, "weights_on_m": moe.SCHED_WEIGHTS_ON_M, "wide": moe.SCHED_WIDE}[name]
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
