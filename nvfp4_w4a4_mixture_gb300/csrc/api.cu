@@ -87,7 +87,7 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     const int64_t nblk = (P + 31) / 32 + E + 1;
     L.h_codes = take(P * I / 2);
     L.h_sf = take(nblk * (I / 64) * 512);  // h block scales in token-block tiles
-    L.ready = take(nblk * 4);
+    L.ready = take((nblk + 1) * 4);  // + the expert GEMMs' tile counter
     L.y = take(P * H * 2);
     L.total = off;
     return L;
@@ -348,6 +348,8 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     ga.offsets = group_offsets;
     ga.G = G;
     ga.status = &hdr->status;
+    ga.tile_counter = &hdr->gemm_tiles;
+    MOE_CUDA(cudaMemsetAsync(&hdr->gemm_tiles, 0, sizeof(int32_t), s), "clear tile counter");
     MOE_CUDA(launch_grouped_gemm(ga, p_max, schedule, device_sm_count(), s), "grouped GEMM launch");
     return MOE_OK;
 }
@@ -401,7 +403,8 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         return n_events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
 
-    const int n_ready = static_cast<int>((P + 31) / 32 + E + 1);  // token blocks of the expert GEMMs
+    // token-block counters of the expert GEMMs, then their tile counter (all zeroed before the launch)
+    const int n_ready = static_cast<int>((P + 31) / 32 + E + 1);
     const bool one_launch_front = front_fits(T, H, E, k);
     MOE_CUDA(mark(0), "event record");
     if (one_launch_front) {
@@ -409,7 +412,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         MOE_CUDA(launch_front(x, T, H, E, k, L->w_router, L->logit_bias, PF(W.logits), P8(W.x_codes), P8(W.x_sf),
                               &hdr->s_x, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), P32(W.offsets),
                               P32(W.perm_src), P32(W.src_perm), P32(W.row_token), &hdr->ticket, P32(W.ready),
-                              n_ready, s),
+                              n_ready + 1, s),
                  "front");
         MOE_CUDA(mark(1), "event record");
         MOE_CUDA(mark(2), "event record");
@@ -464,13 +467,14 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     ga.offsets = P32(W.offsets);
     ga.G = E + 1;
     ga.ready = P32(W.ready);
+    ga.tile_counter = P32(W.ready) + n_ready;
     ga.status = &hdr->status;
     // few rows per expert (decode): 256-row weight tiles when H allows, else weights on the MMA's M
     // side; otherwise 128 x 128 tiles with activations on M
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
     const int sched = small ? (gemm_wide_fits(ga) ? kSchedWide : kSchedWeightsOnM) : kSchedActOnM;
     if (!one_launch_front)  // (the one-launch front half clears them itself)
-        MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready) * 4, s), "clear ready counters");
+        MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");
     MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");
     MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)

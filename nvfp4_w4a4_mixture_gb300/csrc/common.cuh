@@ -21,7 +21,8 @@ struct WsHeader {
     unsigned amax_bits;    // bit pattern of amax(|x|) (non-negative floats order like integers)
     float s_x;             // tensor scale of the layer input
     unsigned ticket;       // CTAs of the one-launch front half that finished (zero between calls)
-    int pad[60];
+    int gemm_tiles;        // tile counter of a standalone grouped GEMM (cleared before its launch)
+    int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

@@ -39,6 +39,7 @@ constexpr int BK_BYTES = 128;              // K-stage: one 128-byte swizzle row 
 constexpr int SF_TILE = 512;               // scale factors of 128 rows x 4 K-blocks
 constexpr int SF_STAGE = 4 * SF_TILE;      // 4 MMA K-steps of 64 per stage
 constexpr int kNumActProducers = 64;       // warps 2-3; each arrives on every stage's full barrier
+constexpr int kTileRing = 8;               // tiles handed from the weight producer to the other roles
 
 // Tile shapes. W_ROWS weight rows (one TMA box) by ACT_ROWS activation rows per tile; ACC_BUFS
 // accumulators of ACC_COLS tensor-memory columns.
@@ -93,6 +94,9 @@ struct Tail {
     uint64_t drain;
     uint64_t xchg_full;   // weights-on-M SwiGLU: up values written (64 arrivals)
     uint64_t xchg_empty;  // weights-on-M SwiGLU: up values consumed (64 arrivals)
+    uint64_t tile_full[kTileRing];   // tile index written (1 arrival)
+    uint64_t tile_empty[kTileRing];  // tile index read by the act producers, MMA and epilogue warps
+    int32_t tile_L[kTileRing];
     uint32_t tmem_base;
     int abort;
     int32_t wsum[32];
@@ -189,6 +193,38 @@ __device__ __forceinline__ bool aborted(const Tail<kMode>& t)
     return *reinterpret_cast<const volatile int*>(&t.abort) != 0;
 }
 
+// Tile hand-over: the weight producer takes tiles from a global counter (the first one is
+// blockIdx.x) and passes each index, then a final index >= total, through the ring; the act
+// producer warps, the MMA thread and the epilogue warps read them in the same order.
+struct TileCursor {
+    int i = 0;
+    uint32_t ph = 0;
+};
+
+template <int kMode>
+__device__ __forceinline__ bool tile_publish(Tail<kMode>& t, TileCursor& c, int L)
+{
+    if (!ptx::mbar_wait(&t.tile_empty[c.i], c.ph ^ 1)) return false;
+    t.tile_L[c.i] = L;
+    ptx::mbar_arrive(&t.tile_full[c.i]);
+    if (++c.i == kTileRing) { c.i = 0; c.ph ^= 1; }
+    return true;
+}
+
+// Warp-wide (all lanes of the calling warp, or a single thread with one_thread); returns total
+// when the wait runs out.
+template <int kMode>
+__device__ __forceinline__ int tile_take(Tail<kMode>& t, TileCursor& c, int total, bool one_thread)
+{
+    int L = total;
+    const bool got = ptx::mbar_wait(&t.tile_full[c.i], c.ph);
+    if (got) L = *reinterpret_cast<const volatile int32_t*>(&t.tile_L[c.i]);
+    if (!one_thread) __syncwarp();
+    if (one_thread || (threadIdx.x & 31) == 0) ptx::mbar_arrive(&t.tile_empty[c.i]);
+    if (++c.i == kTileRing) { c.i = 0; c.ph ^= 1; }
+    return got ? L : total;
+}
+
 __device__ __forceinline__ int ld_acquire(const int32_t* p)
 {
     int v;
@@ -263,6 +299,10 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         ptx::mbar_init(&st.drain, 1);
         ptx::mbar_init(&st.xchg_full, 64);
         ptx::mbar_init(&st.xchg_empty, 64);
+        for (int i = 0; i < kTileRing; ++i) {
+            ptx::mbar_init(&st.tile_full[i], 1);
+            ptx::mbar_init(&st.tile_empty[i], 2 + 1 + C::EPI_WARPS);
+        }
         st.abort = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmap_w0);
@@ -291,7 +331,14 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
+            // tiles in the order the CTAs come for them (phase-0 tiles first): a CTA whose tiles
+            // run short takes more, and the down tiles go out in the order their inputs complete
+            TileCursor tc;
+            int L = blockIdx.x;
+            while (ok && !aborted(st)) {
+                if (L > total) L = total;
+                if (!tile_publish(st, tc, L)) { set_abort(st, a.status); break; }
+                if (L >= total) break;
                 const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
                 const GemmProblem& P = a.p[ti.ph];
                 const CUtensorMap* tm = ti.ph ? &tmap_w1 : &tmap_w0;
@@ -312,6 +359,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     sf_src += 4 * SF_TILE;
                     if (++s == C::STAGES) { s = 0; ph ^= 1; }
                 }
+                L = static_cast<int>(gridDim.x) + atomicAdd(a.tile_counter, 1);
             }
         }
     } else if (warp == 1) {
@@ -327,7 +375,10 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             int s = 0;
             uint32_t ph = 0, lt = 0;
             bool ok = true;
-            for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x, ++lt) {
+            TileCursor tc;
+            for (;; ++lt) {
+                const int L = tile_take(st, tc, total, true);
+                if (L >= total || aborted(st)) break;
                 const int kK = a.p[L >= tiles0 ? 1 : 0].K;
                 const int kb64 = kK / 64, k_stages = (kK + 255) / 256;
                 const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
@@ -390,15 +441,29 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         const uint8_t* sptr[NSR];
         uint32_t cvalid = 0, svalid = 0;
         int s = 0, pub = 0;
-        uint32_t ph = 0, issued = 0;
+        uint32_t ph = 0, issued = 0, published = 0;
         bool ok = true;
-        for (int L = blockIdx.x; L < total && ok && !aborted(st); L += gridDim.x) {
+        // publish (arrive on the full barrier of) every stage whose copies are issued: needed before
+        // any wait on other CTAs, which may be waiting for the tile those stages complete
+        auto publish_all = [&]() {
+            ptx::cp_async_wait<0>();
+            ptx::fence_proxy_async_smem();
+            for (; published < issued; ++published) {
+                ptx::mbar_arrive(&st.full[pub]);
+                if (++pub == C::STAGES) pub = 0;
+            }
+        };
+        TileCursor tc;
+        for (;;) {
+            const int L = tile_take(st, tc, total, false);
+            if (L >= total || !ok || aborted(st)) break;
             const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
             const GemmProblem& P = a.p[ti.ph];
             const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
             const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
             if (ti.ph == 1) {
                 // the down GEMM reads h: wait until every gate/up tile of this token block stored it
+                publish_all();
                 const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS);
                 if (!spin_until(a.ready + ti.tbg, target)) { set_abort(st, a.status); break; }
             }
@@ -460,27 +525,27 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 ptx::cp_async_commit();
                 ++issued;
                 ptx::cp_async_wait<LAG>();
-                if (issued > static_cast<uint32_t>(LAG)) {
+                if (issued > published + LAG) {
                     ptx::fence_proxy_async_smem();
-                    ptx::mbar_arrive(&st.full[pub]);
-                    if (++pub == C::STAGES) pub = 0;
+                    for (; published + LAG < issued; ++published) {
+                        ptx::mbar_arrive(&st.full[pub]);
+                        if (++pub == C::STAGES) pub = 0;
+                    }
                 }
                 if (++s == C::STAGES) { s = 0; ph ^= 1; }
             }
         }
         // publish the stages still in flight
-        ptx::cp_async_wait<0>();
-        ptx::fence_proxy_async_smem();
-        for (uint32_t j = issued > static_cast<uint32_t>(LAG) ? issued - LAG : 0; j < issued; ++j) {
-            ptx::mbar_arrive(&st.full[pub]);
-            if (++pub == C::STAGES) pub = 0;
-        }
+        publish_all();
     } else {
         // ================================ epilogue
         const int ew = warp - 4;
         const int q = warp & 3;  // TMEM lane quarter of this warp
         uint32_t lt = 0, xt = 0;
-        for (int L = blockIdx.x; L < total && !aborted(st); L += gridDim.x, ++lt) {
+        TileCursor tc;
+        for (;; ++lt) {
+            const int L = tile_take(st, tc, total, false);
+            if (L >= total || aborted(st)) break;
             const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
             const GemmProblem& P = a.p[ti.ph];
             const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;

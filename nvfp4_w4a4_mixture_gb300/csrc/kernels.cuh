@@ -74,6 +74,7 @@ struct GemmArgs {
     const int32_t* offsets;   // [G+1]
     int G;
     int32_t* ready;           // [token blocks], zeroed before a two-phase launch
+    int32_t* tile_counter;    // tiles handed out beyond the first gridDim.x, zeroed before each launch
     int* status;
 };
 constexpr int kGemmMaxG = 1025;
