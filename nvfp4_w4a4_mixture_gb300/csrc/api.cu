@@ -75,7 +75,7 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     L.topk_ids = take(n * 4);
     L.topk_w = take(n * 4);
     L.shared_g = take(T * 4);
-    L.logits = take(T * (E + 1) * 4);
+    L.logits = take(T * router_tc_ld(static_cast<int>(E)) * 4);  // rows router_tc_ld(E) >= E + 1 floats apart
     L.x_codes = take(T * H / 2);
     L.x_sf = take(T * H / 16);
     L.offsets = take((E + 2) * 4);
@@ -134,6 +134,34 @@ int device_sm_count()
     return sms > 0 ? sms : 1;
 }
 
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                             uint32_t box_outer)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
+    if (!fn) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t es[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 bool pdl_enabled()
 {
     static const bool on = [] {
@@ -146,15 +174,7 @@ bool pdl_enabled()
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                            uint32_t box1)
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        cudaDriverEntryPointQueryResult q;
-        void* p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {d0, d0 * d1};
@@ -203,6 +223,7 @@ moe_status_t moe_read_device_status(void* ws, moe_stream_t stream)
     MOE_CUDA(cudaMemcpy(&status, ws, sizeof(int), cudaMemcpyDeviceToHost), "read status");
     MOE_CUDA(cudaMemset(ws, 0, sizeof(int)), "clear status");
     if (status & kDevTimeoutGemm) return fail(MOE_ERR_DEVICE_TIMEOUT, "device status 0x%x: grouped GEMM wait timed out", status);
+    if (status & kDevTimeoutRouter) return fail(MOE_ERR_DEVICE_TIMEOUT, "device status 0x%x: router wait timed out", status);
     if (status & kDevBadExpertId) return fail(MOE_ERR_INVALID_ARG, "device status 0x%x: expert id outside [0, E)", status);
     return MOE_OK;
 }
@@ -237,6 +258,16 @@ moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, con
     return quantize_common(x, true, rows, K, s_in, codes, sf, s_out, ws, ws_bytes, stream);
 }
 
+// Router logits into the workspace: tensor cores above kRouterTcMinT tokens (rows router_tc_ld(E)
+// apart), else the CUDA-core kernel with its fixed summation order (rows E + 1 apart).
+constexpr int kRouterTcMinT = 64;
+cudaError_t route_logits(const uint16_t* x, int T, const moe_layer_t* L, float* logits, WsHeader* hdr, cudaStream_t s)
+{
+    if (T > kRouterTcMinT)
+        return launch_router_logits_tc(x, T, L->H, L->E, L->w_router, L->logit_bias, logits, router_tc_ld(L->E), &hdr->status, s);
+    return launch_router_logits(x, T, L->H, L->E, L->w_router, L->logit_bias, logits, s);
+}
+
 moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids, float* topk_w,
                             float* shared_g, float* logits_out, void* ws, size_t ws_bytes, moe_stream_t stream)
 {
@@ -246,13 +277,15 @@ moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int3
     if (!x || !L->w_router || !topk_ids || !topk_w) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     if (!aligned(x, 16) || !aligned(L->w_router, 16)) return fail(MOE_ERR_MISALIGNED, "x and w_router must be 16-byte aligned");
     const WsLayout W = ws_layout(L->H, L->E, L->k, L->I, T);
-    MOE_TRY(check_ws(ws, ws_bytes, W.logits + static_cast<size_t>(T) * (L->E + 1) * 4));
+    const int ld = router_tc_ld(L->E);
+    MOE_TRY(check_ws(ws, ws_bytes, W.logits + static_cast<size_t>(T) * ld * 4));
     MOE_TRY(check_device());
     if (T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* logits = reinterpret_cast<float*>(static_cast<char*>(ws) + W.logits);
-    MOE_CUDA(launch_router_logits(x, T, L->H, L->E, L->w_router, L->logit_bias, logits, s), "router launch");
-    MOE_CUDA(launch_topk(logits, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s), "top-k launch");
+    MOE_CUDA(route_logits(x, T, L, logits, reinterpret_cast<WsHeader*>(ws), s), "router launch");
+    MOE_CUDA(launch_topk(logits, T > kRouterTcMinT ? ld : L->E + 1, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s),
+             "top-k launch");
     return MOE_OK;
 }
 
@@ -422,8 +455,10 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
                  "quantize");
         MOE_CUDA(mark(1), "event record");
         // router, softmax, top-k, shared gate
-        MOE_CUDA(launch_router_logits(x, T, H, E, L->w_router, L->logit_bias, PF(W.logits), s), "router");
-        MOE_CUDA(launch_topk(PF(W.logits), T, E, k, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), nullptr, s), "top-k");
+        MOE_CUDA(route_logits(x, T, L, PF(W.logits), hdr, s), "router");
+        MOE_CUDA(launch_topk(PF(W.logits), T > kRouterTcMinT ? router_tc_ld(E) : E + 1, T, E, k, P32(W.topk_ids),
+                             PF(W.topk_w), PF(W.shared_g), nullptr, s),
+                 "top-k");
         MOE_CUDA(mark(2), "event record");
         // permutation by expert id, the shared expert appended as group E
         MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), nullptr, P32(W.perm_src),
@@ -469,10 +504,10 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     ga.ready = P32(W.ready);
     ga.tile_counter = P32(W.ready) + n_ready;
     ga.status = &hdr->status;
-    // few rows per expert (decode): 256-row weight tiles when H allows, else weights on the MMA's M
-    // side; otherwise 128 x 128 tiles with activations on M
+    // 256-row weight tiles when H allows (half the MMAs and scale copies per weight byte); else
+    // weights on the MMA's M side for few rows per expert (decode), 128 x 128 tiles otherwise
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
-    const int sched = small ? (gemm_wide_fits(ga) ? kSchedWide : kSchedWeightsOnM) : kSchedActOnM;
+    const int sched = gemm_wide_fits(ga) ? kSchedWide : small ? kSchedWeightsOnM : kSchedActOnM;
     if (!one_launch_front)  // (the one-launch front half clears them itself)
         MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");
     MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");

@@ -18,8 +18,16 @@ cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const f
 // logits: FP32 [T][E+1] (column E = shared-gate logit, no bias).
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
                                  float* logits, cudaStream_t stream);
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w, float* shared_g,
-                        float* logits_out, cudaStream_t stream);
+// logits rows ld floats apart (ld >= E + 1)
+cudaError_t launch_topk(const float* logits, int ld, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                        float* shared_g, float* logits_out, cudaStream_t stream);
+
+// ---- router_tc.cu (large batches: router logits on the tensor cores)
+// logits: FP32 [T][ld] with ld = router_tc_ld(E) (a multiple of 16; columns E+1.. hold 0);
+// H % 64 == 0. A bounded wait that runs out sets kDevTimeoutRouter in *status.
+int router_tc_ld(int E);
+cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
+                                    float* logits, int ld, int* status, cudaStream_t stream);
 
 // ---- permute.cu
 constexpr int kPermChunk = 512;  // assignments per warp-chunk
@@ -114,6 +122,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
 }
 void set_last_error_detail(const char* msg);  // text returned by moe_last_error_detail()
+CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                             uint32_t box_outer);
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                            uint32_t box1);
 

@@ -81,7 +81,7 @@ extern "C" moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const m
     if (T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_router_logits(x, T, L->H, L->E, L->w_router, L->logit_bias, scratch, s) != cudaSuccess ||
-        launch_topk(scratch, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s) != cudaSuccess)
+        launch_topk(scratch, L->E + 1, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s) != cudaSuccess)
         return noalloc_fail(MOE_ERR_CUDA, "router launch failed");
     return MOE_OK;
 }

@@ -87,7 +87,7 @@ __device__ __forceinline__ bool before(float a, int ia, float b, int ib) { retur
 
 // One CTA (4 warps) per token: each thread holds 8 logits; k rounds of a block arg-max.
 __global__ void __launch_bounds__(kTopkThreads)
-    k_topk(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
+    k_topk(const float* __restrict__ logits, int ld, int T, int E, int k, int32_t* __restrict__ topk_ids,
            float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
 {
     __shared__ float wb[kTopkThreads / 32];
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     __shared__ float sel_l[32];
     __shared__ int sel_i[32];
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float* l = logits + static_cast<int64_t>(t) * (E + 1);
+    const float* l = logits + static_cast<int64_t>(t) * ld;
     float v[kTopkPer];
     unsigned live = 0;
 #pragma unroll
@@ -179,11 +179,11 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const u
     return cudaGetLastError();
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w, float* shared_g,
-                        float* logits_out, cudaStream_t stream)
+cudaError_t launch_topk(const float* logits, int ld, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                        float* shared_g, float* logits_out, cudaStream_t stream)
 {
     if (T <= 0) return cudaSuccess;
-    k_topk<<<T, kTopkThreads, 0, stream>>>(logits, T, E, k, topk_ids, topk_w, shared_g, logits_out);
+    k_topk<<<T, kTopkThreads, 0, stream>>>(logits, ld, T, E, k, topk_ids, topk_w, shared_g, logits_out);
     return cudaGetLastError();
 }
 

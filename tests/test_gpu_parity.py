@@ -115,6 +115,19 @@ def test_quantize_static_scale_edge_values(moe):
 # router
 # ------------------------------------------------------------------------------------------------
 
+def _check_route_values(w, g, lg, w_ref, g_ref, lg_ref):
+    # The logits are FP32 sums (their order differs between the CUDA-core and tensor-core routers);
+    # the renormalised softmax moves each weight by at most half the largest logit change (its
+    # Jacobian rows sum to 2 p (1 - p) <= 1/2 in absolute value) and the sigmoid gate by a quarter
+    # of it, so the weights are held to the logits' own error plus FP32 rounding.
+    dl = float(np.max(np.abs(lg.cpu().numpy() - lg_ref)))
+    assert dl <= 1e-4, dl
+    w = w.cpu().numpy()
+    assert np.max(np.abs(w - w_ref)) <= dl + W_TOL
+    assert np.max(np.abs(w.sum(1) - 1.0)) <= W_TOL
+    assert np.max(np.abs(g.cpu().numpy() - g_ref)) <= 0.5 * dl + W_TOL
+
+
 @pytest.mark.parametrize("config", ["tiny", "decode", "prefill4k"])
 def test_route_topk(moe, config):
     c = wl.CONFIGS[config]
@@ -129,10 +142,24 @@ def test_route_topk(moe, config):
                          logit_bias=None if bias is None else dev(bias), prepacked=True)
     ids, w, g, lg = moe.moe_route_topk(bf16_dev(x), layer, want_logits=True)
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
-    assert np.max(np.abs(w.cpu().numpy() - w_ref)) <= W_TOL
-    assert np.max(np.abs(w.cpu().numpy().sum(1) - 1.0)) <= W_TOL
-    assert np.max(np.abs(g.cpu().numpy() - g_ref)) <= W_TOL
-    assert np.max(np.abs(lg.cpu().numpy() - lg_ref)) <= 1e-4
+    _check_route_values(w, g, lg, w_ref, g_ref, lg_ref)
+
+
+@pytest.mark.parametrize("config,T", [("tiny", 65), ("tiny", 130), ("decode", 300)])
+def test_route_topk_tensor_core_ragged(moe, config, T):
+    # more than 64 tokens take the tensor-core router: token blocks of 128 and router-row tiles of
+    # 176 with ragged edges (E + 1 = 17 and 513)
+    c = wl.CONFIGS[config]
+    H, E, k = c["H"], c["E"], c["k"]
+    w_r = wl.gen_router(T, E, H)
+    x, _ = I_.draw_x(T, T, H, w_r, k)
+    ids_ref, w_ref, g_ref, lg_ref = oracle.router(x, w_r, k, want_logits=True)
+    dummy = (torch.zeros(1, 1, 8, dtype=torch.uint8, device="cuda"),) * 2 + (torch.ones(1, 2, device="cuda"),)
+    layer = moe.MoeLayer(H, E, k, 128, bf16_dev(w_r), dummy, dummy, torch.ones(E + 1, device="cuda"), prepacked=True)
+    ids, w, g, lg = moe.moe_route_topk(bf16_dev(x), layer, want_logits=True)
+    moe.moe_read_device_status()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    _check_route_values(w, g, lg, w_ref, g_ref, lg_ref)
 
 
 def test_route_exact_ties_lowest_index(moe):
