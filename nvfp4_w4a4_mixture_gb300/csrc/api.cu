@@ -164,9 +164,11 @@ CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
 
 bool pdl_enabled()
 {
+    // Off unless MOE_NVFP4_PDL=1: in a CUDA graph replay of the decode layer the programmatic
+    // launches measured about 5 us slower per step than plain stream order.
     static const bool on = [] {
-        const char* v = std::getenv("MOE_NVFP4_NO_PDL");
-        return !(v && v[0] == '1');
+        const char* v = std::getenv("MOE_NVFP4_PDL");
+        return v && v[0] == '1';
     }();
     return on;
 }

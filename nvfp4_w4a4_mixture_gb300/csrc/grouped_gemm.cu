@@ -4,23 +4,28 @@
 // computed by tcgen05.mma kind::mxf4nvf4 (E2M1 x E2M1 products, one UE4M3 scale per 16 along K,
 // FP32 accumulation in tensor memory).
 //
-// One persistent CTA per SM walks a list of output tiles (token block of a group, 128 weight
-// rows), weight blocks fastest, so consecutive CTAs share the token block's activation rows and
-// one expert's weights stay in L2 across its token blocks. Two schedules:
-//   activations on M (large groups): 128 token rows x 128 weight rows per tile, MMA 128 x 128;
-//   weights on M (small groups): 128 weight rows x 32 token rows per tile, MMA 128 x 32, so a decode
-//     step with one or two tokens per expert does not pay for 128-row tiles.
+// One persistent CTA per SM; the weight producer of each CTA takes output tiles (token block of a
+// group x W_ROWS weight rows) from a global counter, weight blocks fastest, so CTAs working at the
+// same time share a token block's activation rows and one expert's weights stay in L2 across its
+// token blocks. Three tile shapes:
+//   activations on M (large groups): 128 token rows x 128 weight rows, MMA 128 x 128;
+//   weights on M (small groups): 128 weight rows x 32 token rows, MMA 128 x 32;
+//   wide: 128 token rows x 256 weight rows, MMA 128 x 256 (half the MMAs and scale copies per
+//     weight byte; single-buffered accumulator).
 // A launch can hold two problems (phases) over the same groups: the gate/up GEMM with its SwiGLU
-// epilogue, then the down GEMM reading the intermediate h. A down tile of token block b waits
-// (bounded) until every gate/up tile of block b has stored its part of h: the gate/up epilogue
-// threads publish with a fence and an atomic count per token block. The two-phase launch is
-// cooperative, so all CTAs are resident and such a wait ends. h's block scales are written in
-// 512-byte token-block tiles, the layout the down GEMM copies straight into shared memory.
+// epilogue, then the down GEMM reading the intermediate h. All phase-0 tiles are handed out before
+// any phase-1 tile. A down tile of token block b waits (bounded) until every gate/up tile of block
+// b has stored its part of h: the gate/up epilogue warps publish with a fence and an atomic count
+// per token block. The grid is at most one CTA per SM, each needing most of an SM's shared memory,
+// so all CTAs become resident and such a wait ends. h's block scales are written in 512-byte
+// token-block tiles, the layout the down GEMM copies straight into shared memory.
 // Warp roles:
-//   warp 0       weight producer: TMA of the 128 x 128-byte weight box (128-byte swizzle) and one
-//                bulk copy of its scale-factor tiles, per K-stage of 256 elements;
-//   warp 1       TMEM owner and MMA issuer: per K-step of 64, tcgen05.cp of both scale-factor
-//                tiles into tensor memory and one tcgen05.mma into a double-buffered accumulator;
+//   warp 0       weight producer: takes the tiles and hands their indices to the other roles through
+//                a shared-memory ring; per K-stage of 256 elements, TMA of the W_ROWS x 128-byte
+//                weight box (128-byte swizzle) and bulk copies of its scale-factor tiles;
+//   warp 1       TMEM owner and MMA issuer: per K-step of 64, tcgen05.cp of the scale-factor tiles
+//                into tensor memory and one tcgen05.mma into the (double- or single-buffered)
+//                accumulator;
 //   warps 2-3    activation producers: gather the tile's activation rows (row index list) with
 //                cp.async into the swizzled layout, and their scale factors into tile layout;
 //   warps 4..    epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31), apply
@@ -794,23 +799,12 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
     const int64_t blocks_ub = (p_max + C::ACT_ROWS - 1) / C::ACT_ROWS + a.G;
     const int64_t tiles_ub = blocks_ub * (a.p[0].N / C::W_ROWS);
     const int grid = static_cast<int>(tiles_ub < sms ? (tiles_ub < 1 ? 1 : tiles_ub) : sms);
-    if (a.nphase == 1)
-        return launch_pdl(k_grouped_gemm_nvf4<kMode>, dim3(grid), dim3(Lay<kMode>::THREADS), smem_bytes<kMode>(), stream,
-                          tmap[0], tmap[1], a);
-    // two phases: CTAs wait on one another's results, so all of them must be resident
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(Lay<kMode>::THREADS);
-    cfg.dynamicSmemBytes = smem_bytes<kMode>();
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k_grouped_gemm_nvf4<kMode>, tmap[0], tmap[1], a);
+    // Two phases: CTAs wait on one another's results, so all of them must become resident. The
+    // grid is at most one CTA per SM and a CTA needs most of an SM's shared memory, so the whole
+    // grid is resident once earlier kernels on the SMs have drained (they never wait on this one);
+    // the waits are bounded in any case and report a timeout in the status word.
+    return launch_pdl(k_grouped_gemm_nvf4<kMode>, dim3(grid), dim3(Lay<kMode>::THREADS), smem_bytes<kMode>(), stream,
+                      tmap[0], tmap[1], a);
 }
 
 bool gemm_wide_fits(const GemmArgs& a)

@@ -102,8 +102,9 @@ cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* 
 // ---- api.cu
 int device_sm_count();
 
-// Launches with programmatic stream serialisation (the kernel calls ptx::griddep_wait() before it
-// touches anything the previous launch writes or reads), unless MOE_NVFP4_NO_PDL is set to 1.
+// Launches with programmatic stream serialisation when MOE_NVFP4_PDL=1 (the kernel calls
+// ptx::griddep_wait() before it touches anything the previous launch writes or reads; without the
+// attribute that call returns at once).
 bool pdl_enabled();
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
