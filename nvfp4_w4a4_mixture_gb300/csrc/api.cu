@@ -500,6 +500,8 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     g2.K = I;
     g2.epilogue = kEpiBF16;
     g2.out = base + W.y;
+    g2.out_row = P32(W.perm_src);  // routed rows back in assignment order t*k + j; shared rows stay
+    g2.out_row_n = static_cast<int>(static_cast<int64_t>(T) * k);
     ga.nphase = 2;
     ga.offsets = P32(W.offsets);
     ga.G = E + 1;
@@ -515,8 +517,8 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");
     MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)
-    MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), P32(W.src_perm), T,
-                            k, H, residual, out, s),
+    MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), nullptr, T, k,
+                            H, residual, out, s),
              "combine");
     MOE_CUDA(mark(5), "event record");
     return MOE_OK;

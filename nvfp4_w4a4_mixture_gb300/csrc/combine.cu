@@ -1,17 +1,19 @@
 // combine.cu -- weighted un-permute of the expert outputs with FP32 accumulation.
 //
-// One CTA per (token, 2048-column slice): the token's k routing slots (row index and weight) are
-// staged in shared memory first, then every thread owns 8 consecutive hidden columns and issues
-// the 16-byte loads of all k routed rows and the shared row before it accumulates, so the loads of
-// one token are in flight together. The sum runs in a fixed order (slots j = 0..k-1, then the
-// shared expert, then the residual), each product rounded to FP32 before it is added:
-// deterministic.
+// One CTA per (token, column slice): 64 threads (512 columns) for few tokens, 256 (2048 columns)
+// for many; every thread owns 8 consecutive hidden columns. With a src_perm index the token's routed rows are y[src_perm[t*k + j]] (rows in
+// permuted order); without one they are y[t*k + j] (the expert GEMM wrote them back in assignment
+// order), so no index load precedes the row loads. The shared expert's row is y[T*k + t]. Each
+// thread issues the 16-byte loads of up to 16 slots together, then accumulates in a fixed order
+// (slots j = 0..k-1, the shared expert, the residual), each product rounded to FP32 before it is
+// added: deterministic.
 #include "kernels.cuh"
 
 namespace moe {
 
-constexpr int kCombineThreads = 256;  // x 8 columns = 2048 columns per CTA
-constexpr int kMaxK = 32;
+constexpr int kCombineThreadsSmall = 64;  // x 8 columns = 512 columns per CTA (few tokens: more CTAs)
+constexpr int kCombineThreadsLarge = 256;
+constexpr int kCombineChunk = 16;    // slots whose rows are loaded together
 
 __device__ __forceinline__ void axpy8(float (&acc)[8], float w, const uint4& v)
 {
@@ -23,55 +25,59 @@ __device__ __forceinline__ void axpy8(float (&acc)[8], float w, const uint4& v)
     }
 }
 
-__global__ void __launch_bounds__(kCombineThreads)
+__global__ void __launch_bounds__(kCombineThreadsLarge)
     k_combine(const uint16_t* __restrict__ y, const float* __restrict__ topk_w, const float* __restrict__ shared_g,
               const int32_t* __restrict__ src_perm, int T, int k, int H, const uint16_t* __restrict__ residual,
               uint16_t* __restrict__ out)
 {
-    __shared__ int64_t rows_s[kMaxK + 1];
-    __shared__ float w_s[kMaxK + 1];
     ptx::griddep_wait();  // y comes from the launch before this one
     ptx::griddep_launch_dependents();
     const int t = blockIdx.x;
-    const int64_t tk = static_cast<int64_t>(t) * k;
-    if (threadIdx.x < k) {
-        rows_s[threadIdx.x] = __ldg(src_perm + tk + threadIdx.x);
-        w_s[threadIdx.x] = __ldg(topk_w + tk + threadIdx.x);
-    }
-    const int nslot = k + (shared_g ? 1 : 0);
-    if (shared_g && threadIdx.x == 0) {
-        rows_s[k] = static_cast<int64_t>(T) * k + t;
-        w_s[k] = __ldg(shared_g + t);
-    }
-    __syncthreads();
-    const int c = (blockIdx.y * kCombineThreads + threadIdx.x) * 8;
+    const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
     if (c >= H) return;
+    const int64_t tk = static_cast<int64_t>(t) * k;
+    const int nslot = k + (shared_g ? 1 : 0);
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    int j = 0;
-    for (; j + 4 <= nslot; j += 4) {
-        uint4 v[4];
+    uint4 res = make_uint4(0, 0, 0, 0);
+    if (residual) res = __ldg(reinterpret_cast<const uint4*>(residual + static_cast<int64_t>(t) * H + c));
+    for (int j0 = 0; j0 < nslot; j0 += kCombineChunk) {
+        uint4 v[kCombineChunk];
+        float w[kCombineChunk];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const uint4*>(y + rows_s[j + u] * H + c));
+        for (int u = 0; u < kCombineChunk; ++u) {
+            const int j = j0 + u;
+            if (j < nslot) {
+                int64_t row;
+                if (j < k) {
+                    row = src_perm ? static_cast<int64_t>(__ldg(src_perm + tk + j)) : tk + j;
+                    w[u] = __ldg(topk_w + tk + j);
+                } else {
+                    row = static_cast<int64_t>(T) * k + t;
+                    w[u] = __ldg(shared_g + t);
+                }
+                v[u] = __ldg(reinterpret_cast<const uint4*>(y + row * H + c));
+            }
+        }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) axpy8(acc, w_s[j + u], v[u]);
+        for (int u = 0; u < kCombineChunk; ++u)
+            if (j0 + u < nslot) axpy8(acc, w[u], v[u]);
     }
-    for (; j < nslot; ++j) axpy8(acc, w_s[j], __ldg(reinterpret_cast<const uint4*>(y + rows_s[j] * H + c)));
-    if (residual) axpy8(acc, 1.0f, __ldg(reinterpret_cast<const uint4*>(residual + static_cast<int64_t>(t) * H + c)));
-    uint32_t w[4];
+    if (residual) axpy8(acc, 1.0f, res);
+    uint32_t o[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = f32_to_bf16(acc[2 * i]) | (f32_to_bf16(acc[2 * i + 1]) << 16);
-    *reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H + c) = make_uint4(w[0], w[1], w[2], w[3]);
+    for (int i = 0; i < 4; ++i) o[i] = f32_to_bf16(acc[2 * i]) | (f32_to_bf16(acc[2 * i + 1]) << 16);
+    *reinterpret_cast<uint4*>(out + static_cast<int64_t>(t) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* shared_g, const int32_t* src_perm, int T,
                            int k, int H, const uint16_t* residual, uint16_t* out, cudaStream_t stream)
 {
     if (T <= 0) return cudaSuccess;
-    dim3 grid(T, (H + kCombineThreads * 8 - 1) / (kCombineThreads * 8));
-    return launch_pdl(k_combine, grid, dim3(kCombineThreads), 0, stream, y, topk_w, shared_g, src_perm, T, k, H, residual,
-                      out);
+    const int threads = T >= 256 ? kCombineThreadsLarge : kCombineThreadsSmall;
+    dim3 grid(T, (H + threads * 8 - 1) / (threads * 8));
+    return launch_pdl(k_combine, grid, dim3(threads), 0, stream, y, topk_w, shared_g, src_perm, T, k, H, residual, out);
 }
 
 }  // namespace moe

@@ -2,16 +2,17 @@
 // router logits, FP32 softmax top-k with renormalised weights, shared gate, and the stable
 // permutation by expert id.
 //
-// Every CTA computes the logits of 8 router rows for all tokens (the same per-lane strided FP32
-// sums and butterfly as the standalone router, so the logits are bit-identical to it); CTA 0 also
-// quantises x (it reads the whole tensor anyway for its max). Each CTA then takes a ticket; the
-// last CTA to finish reads all logits and does the top-k (one warp per token, k rounds of a warp
-// arg-max, lowest index first on ties) and the permutation (counts, scan, rank by direct count:
-// stable and bit-exact), then returns the ticket counter to zero for the next call. No CTA waits
+// Every CTA but the last computes the logits of 8 router rows for all tokens (the same per-lane
+// strided FP32 sums and butterfly as the standalone router, so the logits are bit-identical to it);
+// the last CTA quantises x. Each CTA then takes a ticket; the last CTA to finish reads all logits
+// and does the top-k (one warp per token: integer keys, a four-entry cache per lane, lowest index
+// first on ties) and the stable permutation (rank by counting, offsets by binary search over the
+// ids in position order), then returns the ticket counter to zero for the next call. No CTA waits
 // for another, so the launch needs no co-residency.
 #include <cfloat>
 
 #include "kernels.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -23,92 +24,6 @@ constexpr int kFrontTT = 8;        // tokens staged per pass
 constexpr int kFrontMaxE = 1024;
 constexpr int kFrontMaxT = 64;
 constexpr int kSmallFrontAssign = 512;  // T * k
-
-// Order-preserving key of a logit: a larger logit has a larger key; every logit, -inf included, has
-// a key >= 1, and NaN ranks with -inf (so the selected ids always lie in [0, E)).
-__device__ __forceinline__ uint32_t order_key(float v)
-{
-    if (v != v) v = -INFINITY;
-    if (v == 0.0f) v = 0.0f;  // -0 ties with +0
-    const uint32_t b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_value(uint32_t k)
-{
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// A lane's four largest keys, largest first (equal keys: lowest slot first); unused entries hold 0.
-struct Top4 {
-    uint32_t k[4];
-    int s[4];
-};
-
-__device__ __forceinline__ void lane_top4(const uint32_t (&key)[32], Top4& c)
-{
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        c.k[q] = 0u;
-        c.s[q] = 31;
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        uint32_t kv = key[i];
-        int sv = i;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {  // insertion: a strictly larger key moves ahead
-            const bool gt = kv > c.k[q];
-            const uint32_t tk = gt ? c.k[q] : kv;
-            const int ts = gt ? c.s[q] : sv;
-            c.k[q] = gt ? kv : c.k[q];
-            c.s[q] = gt ? sv : c.s[q];
-            kv = tk;
-            sv = ts;
-        }
-    }
-}
-
-// Exclusive scan of cnt[0..n) (n <= 1024) in place by 256 threads; returns the total.
-__device__ int32_t block_exclusive_scan(int32_t* cnt, int n, int32_t* wsum)
-{
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    int32_t v[4], s = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int e = t * 4 + i;
-        v[i] = e < n ? cnt[e] : 0;
-        s += v[i];
-    }
-    int32_t x = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int32_t w = lane < kFrontWarps ? wsum[lane] : 0;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-            if (lane >= o) w += y;
-        }
-        if (lane < kFrontWarps) wsum[lane] = w;
-    }
-    __syncthreads();
-    int32_t run = x - s + (warp > 0 ? wsum[warp - 1] : 0);
-    const int32_t total = wsum[kFrontWarps - 1];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int e = t * 4 + i;
-        if (e < n) cnt[e] = run;
-        run += v[i];
-    }
-    __syncthreads();
-    return total;
-}
 
 }  // namespace
 
@@ -138,8 +53,7 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     extern __shared__ __align__(16) uint8_t fsm[];
     uint16_t* xs = reinterpret_cast<uint16_t*>(fsm);  // [kFrontTT][H]
     __shared__ int32_t ids_s[kSmallFrontAssign];
-    __shared__ int32_t cnt_s[kFrontMaxE];
-    __shared__ int32_t wsum_s[32];
+    __shared__ int32_t sorted_s[kSmallFrontAssign];
     __shared__ float red_s[kFrontWarps];
     __shared__ unsigned last_s;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -265,90 +179,48 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     if (!last_s) return;
     __threadfence();
 
-    // top-k per token: warp w takes tokens w, w + 8, ...; lane l holds logits l, l + 32, ... as
-    // order-preserving integer keys (a removed or absent entry has key 0, below every logit) and a
-    // cache of its four largest. A round takes the warp's largest cached key with one reduction and
-    // the lowest expert id holding it with a second; the winning lane pops its cache and rebuilds it
-    // from its remaining keys only when it runs empty.
+    // top-k per token: warp w takes tokens w, w + 8, ...
     for (int t = warp; t < T; t += kFrontWarps) {
         const float* l = a.logits + static_cast<int64_t>(t) * (E + 1);
-        uint32_t key[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int ee = i * 32 + lane;
-            key[i] = ee < E ? order_key(__ldcg(l + ee)) : 0u;
-        }
-        Top4 c;
-        lane_top4(key, c);
-        float sel_l = 0.0f;
-        int sel_i = 0;
-        uint32_t k0 = 0;
-        for (int j = 0; j < k; ++j) {
-            const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, c.k[0]);
-            const int widx = static_cast<int>(__reduce_min_sync(
-                0xFFFFFFFFu, c.k[0] == wmax ? static_cast<unsigned>(c.s[0] * 32 + lane) : 0x7FFFFFFFu));
-            if (j == 0) k0 = wmax;
-            if (lane == j) {
-                sel_l = key_value(wmax);
-                sel_i = widx;
-            }
-            if ((widx & 31) == lane) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i == c.s[0]) key[i] = 0u;
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    c.k[q] = c.k[q + 1];
-                    c.s[q] = c.s[q + 1];
-                }
-                c.k[3] = 0u;
-                c.s[3] = 31;
-                if (c.k[0] == 0u) lane_top4(key, c);
-            }
-        }
-        // renormalised weights: softmax over the selected logits (the first one is the largest)
-        const float l0 = key_value(k0);
-        const float p = lane < k ? expf(sel_l - l0) : 0.0f;
-        float sum = p;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        const float l_gate = lane == 0 ? __ldcg(l + E) : 0.0f;  // shared-gate logit, loaded with the rest
+        float sel_l, l0;
+        int sel_i;
+        warp_topk(l, E, k, sel_l, sel_i, l0);
+        const float w = warp_topk_weight(sel_l, l0, k);
         if (lane < k) {
             a.topk_ids[static_cast<int64_t>(t) * k + lane] = sel_i;
-            a.topk_w[static_cast<int64_t>(t) * k + lane] = p / sum;
+            a.topk_w[static_cast<int64_t>(t) * k + lane] = w;
             ids_s[t * k + lane] = sel_i;
         }
-        if (lane == 0) a.shared_g[t] = 1.0f / (1.0f + expf(-__ldcg(l + E)));
+        if (lane == 0) a.shared_g[t] = 1.0f / (1.0f + expf(-l_gate));
     }
-    // permutation: counts, exclusive scan over experts, then warp 0 places the assignments in order,
-    // 32 at a time: rank = earlier lanes with the same id (match) + the id's running count
+    // permutation: the position of assignment f is the number of assignments with a smaller id plus
+    // the earlier ones with the same id (stable); the ids in position order then give the expert
+    // offsets by binary search (offsets[e] = assignments with an id below e)
     const int n = T * k;
-    for (int i = tid; i < E; i += kFrontThreads) cnt_s[i] = 0;
-    __syncthreads();
-    for (int f = tid; f < n; f += kFrontThreads) atomicAdd(&cnt_s[ids_s[f]], 1);
-    __syncthreads();
-    const int32_t total = block_exclusive_scan(cnt_s, E, wsum_s);
-    for (int i = tid; i < E; i += kFrontThreads) a.offsets[i] = cnt_s[i];
-    if (tid == 0) {
-        a.offsets[E] = total;
-        a.offsets[E + 1] = total + T;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        for (int c0 = 0; c0 < n; c0 += 32) {
-            const int f = c0 + lane;
-            const int id = f < n ? ids_s[f] : -1;
-            const unsigned m = __match_any_sync(0xFFFFFFFFu, id);
-            if (f < n) {
-                const int pos = cnt_s[id] + __popc(m & ((1u << lane) - 1u));
-                a.perm_src[pos] = f;
-                a.src_perm[f] = pos;
-                a.row_token[pos] = f / k;
-            }
-            __syncwarp();
-            if (f < n && (m >> lane) == 1u) cnt_s[id] += __popc(m);  // highest lane of each id
-            __syncwarp();
+    __syncthreads();  // ids_s complete
+    for (int f = tid; f < n; f += kFrontThreads) {
+        const int id = ids_s[f];
+        int pos = 0;
+        for (int q = 0; q < n; ++q) {
+            const int o = ids_s[q];
+            pos += (o < id) | ((o == id) & (q < f));
         }
+        a.perm_src[pos] = f;
+        a.src_perm[f] = pos;
+        a.row_token[pos] = f / k;
+        sorted_s[pos] = id;
     }
+    __syncthreads();
+    for (int e = tid; e <= E; e += kFrontThreads) {
+        int lo = 0, hi = n;  // first position whose id is >= e
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sorted_s[mid] < e) lo = mid + 1; else hi = mid;
+        }
+        a.offsets[e] = lo;
+    }
+    if (tid == 0) a.offsets[E + 1] = n + T;
     for (int t = tid; t < T; t += kFrontThreads) a.row_token[n + t] = t;
     for (int i = tid; i < a.n_ready; i += kFrontThreads) a.ready[i] = 0;
     if (tid == 0) *a.ticket = 0u;  // every CTA has taken its ticket: ready for the next call

@@ -560,6 +560,13 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             const float sb0 = __ldg(P.b_scale + (P.gate_up ? 2 * ti.g : ti.g));
             const float sb1 = P.gate_up ? __ldg(P.b_scale + 2 * ti.g + 1) : sb0;
             const float S_h = P.epilogue == kEpiSwiGLU ? __ldg(P.epi_scale + ti.g) : 1.0f;
+            // output row of this lane's tile row (row r = q*32 + lane on M, or token slot = lane on N)
+            int64_t po;
+            {
+                const int rr = kSwap ? lane : q * 32 + lane;
+                const int64_t p = ti.row0 + rr;
+                po = (P.out_row && rr < ti.rows && p < P.out_row_n) ? static_cast<int64_t>(__ldg(P.out_row + p)) : p;
+            }
             const bool got = ptx::mbar_wait(&st.acc_full[as], aph);
             __syncwarp();
             if (!__all_sync(0xFFFFFFFFu, got)) { set_abort(st, a.status); break; }
@@ -652,7 +659,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         const float sc = sa * sb;
                         if (valid) {
                             if (P.epilogue == kEpiF32) {
-                                float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + p * P.N + col);
+                                float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + po * P.N + col);
 #pragma unroll
                                 for (int j = 0; j < 4; ++j)
                                     o[j] = make_float4(__uint_as_float(v[i][4 * j]) * sc, __uint_as_float(v[i][4 * j + 1]) * sc,
@@ -663,7 +670,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                                 for (int j = 0; j < 8; ++j)
                                     w[j] = f32_to_bf16(__uint_as_float(v[i][2 * j]) * sc) |
                                            (f32_to_bf16(__uint_as_float(v[i][2 * j + 1]) * sc) << 16);
-                                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + p * P.N + col);
+                                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + po * P.N + col);
                                 o[0] = make_uint4(w[0], w[1], w[2], w[3]);
                                 o[1] = make_uint4(w[4], w[5], w[6], w[7]);
                             }
@@ -741,7 +748,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         if (t < nv) {
-                            const int64_t p = ti.row0 + t;
+                            const int64_t p = __shfl_sync(0xFFFFFFFFu, po, t);  // warp-uniform t
                             const float val = __uint_as_float(v[t]) * s;
                             if (P.epilogue == kEpiF32)
                                 static_cast<float*>(P.out)[p * P.N + col] = val;

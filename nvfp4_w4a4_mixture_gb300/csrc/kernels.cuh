@@ -72,6 +72,8 @@ struct GemmProblem {
     void* out;
     uint8_t* out_sf;          // SwiGLU: h scales, row-major [P][N/32] or tiles when out_sf_tiled
     int out_sf_tiled;
+    const int32_t* out_row;   // nullable (FP32 / bf16 epilogues): row p < out_row_n goes to out row
+    int out_row_n;            //   out_row[p] (e.g. back to assignment order), rows p >= out_row_n stay
 };
 
 // A launch: one problem, or the gate/up problem (phase 0) followed by the down problem (phase 1)

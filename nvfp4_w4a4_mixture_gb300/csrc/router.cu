@@ -4,12 +4,13 @@
 // loads of the router row (each row of W_r is read once per token tile). Every product of two
 // bf16 values is exact in FP32; the sum runs in a fixed order (per-lane strided partial sums,
 // then a butterfly), so the result is deterministic.
-// Top-k: one CTA of 4 warps per token; k rounds of a block arg-max on (logit desc, expert id
+// Top-k: one warp per token (see topk.cuh): k rounds of a warp arg-max on (logit desc, expert id
 // asc), which is the lowest-index tie rule; the renormalised weights are the softmax over the
 // selected logits (the full softmax denominator cancels), the shared gate is sigmoid(logit E).
 #include <cfloat>
 
 #include "kernels.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -79,89 +80,30 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     }
 }
 
-constexpr int kTopkThreads = 128;
-constexpr int kTopkPer = 8;  // E <= 1024 = kTopkThreads * kTopkPer
 
-// (value desc, index asc) order: true when (a, ia) comes before (b, ib)
-__device__ __forceinline__ bool before(float a, int ia, float b, int ib) { return a > b || (a == b && ia < ib); }
+// One warp per token (8 per CTA): the warp top-k, renormalised weights, shared gate.
+constexpr int kTopkWarps = 8;
 
-// One CTA (4 warps) per token: each thread holds 8 logits; k rounds of a block arg-max.
-__global__ void __launch_bounds__(kTopkThreads)
+__global__ void __launch_bounds__(kTopkWarps * 32)
     k_topk(const float* __restrict__ logits, int ld, int T, int E, int k, int32_t* __restrict__ topk_ids,
            float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
 {
-    __shared__ float wb[kTopkThreads / 32];
-    __shared__ int wi[kTopkThreads / 32];
-    __shared__ float sel_l[32];
-    __shared__ int sel_i[32];
-    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
     const float* l = logits + static_cast<int64_t>(t) * ld;
-    float v[kTopkPer];
-    unsigned live = 0;
-#pragma unroll
-    for (int i = 0; i < kTopkPer; ++i) {
-        const int e = i * kTopkThreads + tid;
-        v[i] = e < E ? l[e] : 0.0f;
-        if (e < E) {
-            live |= 1u << i;
-            if (logits_out) logits_out[static_cast<int64_t>(t) * E + e] = v[i];
-            if (v[i] != v[i]) v[i] = -INFINITY;  // a NaN logit ranks below every number
-        }
+    const float l_gate = lane == 0 ? __ldcg(l + E) : 0.0f;
+    float sel_l, l0;
+    int sel_i;
+    warp_topk(l, E, k, sel_l, sel_i, l0);
+    const float w = warp_topk_weight(sel_l, l0, k);
+    if (lane < k) {
+        topk_ids[static_cast<int64_t>(t) * k + lane] = sel_i;
+        topk_w[static_cast<int64_t>(t) * k + lane] = w;
     }
-    for (int j = 0; j < k; ++j) {
-        float b = -INFINITY;  // (-inf, INT_MAX) loses to every live logit
-        int bi = 0x7FFFFFFF;
-#pragma unroll
-        for (int i = 0; i < kTopkPer; ++i) {
-            const int e = i * kTopkThreads + tid;
-            if (((live >> i) & 1u) && before(v[i], e, b, bi)) {
-                b = v[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xFFFFFFFFu, b, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (before(ob, oi, b, bi)) {
-                b = ob;
-                bi = oi;
-            }
-        }
-        if (lane == 0) {
-            wb[warp] = b;
-            wi[warp] = bi;
-        }
-        __syncthreads();
-        b = wb[0];
-        bi = wi[0];
-#pragma unroll
-        for (int w = 1; w < kTopkThreads / 32; ++w)
-            if (before(wb[w], wi[w], b, bi)) {
-                b = wb[w];
-                bi = wi[w];
-            }
-        if (tid == 0) {
-            sel_l[j] = b;
-            sel_i[j] = bi;
-        }
-#pragma unroll
-        for (int i = 0; i < kTopkPer; ++i)
-            if (i * kTopkThreads + tid == bi) live &= ~(1u << i);
-        __syncthreads();
-    }
-    // renormalised weights: softmax over the selected logits (the first one is the largest)
-    if (warp == 0) {
-        const float p = lane < k ? expf(sel_l[lane] - sel_l[0]) : 0.0f;
-        float sum = p;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-        if (lane < k) {
-            topk_ids[static_cast<int64_t>(t) * k + lane] = sel_i[lane];
-            topk_w[static_cast<int64_t>(t) * k + lane] = p / sum;
-        }
-        if (shared_g && lane == 0) shared_g[t] = 1.0f / (1.0f + expf(-l[E]));
-    }
+    if (shared_g && lane == 0) shared_g[t] = 1.0f / (1.0f + expf(-l_gate));
+    if (logits_out)
+        for (int e = lane; e < E; e += 32) logits_out[static_cast<int64_t>(t) * E + e] = __ldcg(l + e);
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
@@ -183,7 +125,8 @@ cudaError_t launch_topk(const float* logits, int ld, int T, int E, int k, int32_
                         float* shared_g, float* logits_out, cudaStream_t stream)
 {
     if (T <= 0) return cudaSuccess;
-    k_topk<<<T, kTopkThreads, 0, stream>>>(logits, ld, T, E, k, topk_ids, topk_w, shared_g, logits_out);
+    k_topk<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(logits, ld, T, E, k, topk_ids, topk_w,
+                                                                             shared_g, logits_out);
     return cudaGetLastError();
 }
 
