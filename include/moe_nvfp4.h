@@ -66,7 +66,7 @@ typedef void* moe_stream_t; /* cudaStream_t */
 /* NVFP4 weights of G experts, each an [N][K] matrix, in the PREPACKED layout that
  * moe_prepack_nvfp4() writes (see there). gscale: [G][nscale] FP32 per-expert tensor scales. */
 typedef struct {
-    const uint8_t* codes; /* [G][N][K/2], rows in prepacked order */
+    const uint8_t* codes; /* [G][ceil(K/256)][N][128] K-slabs, rows in prepacked order */
     const uint8_t* sf;    /* [G][N/128][K/64][512] scale-factor tiles */
     const float* gscale;  /* [G][nscale] */
 } moe_nvfp4_bank_t;
@@ -141,9 +141,11 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int k, int E, int with_
 
 /* ---------------------------------------------------------------------------------------------
  * moe_prepack_nvfp4 -- rewrite G row-major NVFP4 matrices [N][K] into the layout the grouped GEMM
- *   streams with TMA: codes keep [G][N][K/2] (with gate_up_interleave = 1 the rows are reordered
- *   in blocks of 128 = 64 gate rows n..n+63 followed by the 64 up rows N/2+n..N/2+n+63); block
- *   scales become 512-byte tiles [G][N/128][K/64]: tile byte (r % 32) * 16 + (r / 32) * 4 + j
+ *   streams with TMA: codes become K-slab-major [G][ceil(K/256)][N][128 bytes] (slab s = bytes
+ *   128 s .. 128 s + 127 of every row, zero past K/2; codes_out holds G * N * ceil(K/256) * 128
+ *   bytes), so one TMA box of rows is one contiguous run; with gate_up_interleave = 1 the rows are
+ *   reordered in blocks of 128 = 64 gate rows n..n+63 followed by the 64 up rows N/2+n..N/2+n+63.
+ *   Block scales become 512-byte tiles [G][N/128][K/64]: tile byte (r % 32) * 16 + (r / 32) * 4 + j
  *   holds the scale of row r (of the 128) for K-block 4 * (tile index) + j.
  *   N % 128 == 0, K % 64 == 0; outputs must not alias inputs.
  * ------------------------------------------------------------------------------------------- */

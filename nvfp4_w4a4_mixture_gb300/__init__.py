@@ -160,10 +160,11 @@ def moe_quantize_nvfp4(x, s_in=None, ws=None, out=None):
 
 
 def moe_prepack_nvfp4(codes, sf, gate_up_interleave):
-    """codes u8 [G, N, K/2], sf u8 [G, N, K/16] (row-major) -> prepacked (codes, sf tiles)."""
+    """codes u8 [G, N, K/2], sf u8 [G, N, K/16] (row-major) -> prepacked (codes [G, ceil(K/256), N, 128]
+    K-slabs, sf tiles)."""
     G, N, Kh = codes.shape
     K = Kh * 2
-    codes_out = torch.empty_like(codes)
+    codes_out = torch.empty(G, (K + 255) // 256, N, 128, dtype=torch.uint8, device=codes.device)
     sf_out = torch.empty(G * (N // 128) * (K // 64) * 512, dtype=torch.uint8, device=codes.device)
     _check(lib().moe_prepack_nvfp4(_p(codes), _p(sf), G, N, K, int(gate_up_interleave), _p(codes_out), _p(sf_out),
                                    _stream()))

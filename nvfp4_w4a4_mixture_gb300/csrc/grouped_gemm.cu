@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     uint8_t* sbase = smem + s * LY::STAGE_BYTES;
                     const int nat = min(4, kb64 - kt * 4);
                     ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + LY::WB * nat * SF_TILE);
-                    ptx::tma_load_3d(sbase + LY::OFF_W, tm, &st.full[s], kt * BK_BYTES, row, ti.g);
+                    ptx::tma_load_3d(sbase + LY::OFF_W, tm, &st.full[s], 0, row, ti.g * k_stages + kt);
 #pragma unroll
                     for (int j = 0; j < LY::WB; ++j)
                         ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sf_src + static_cast<int64_t>(j) * kb64 * SF_TILE,
@@ -798,8 +798,10 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
     CUtensorMap tmap[2];
     for (int i = 0; i < a.nphase; ++i) {
         const GemmProblem& P = a.p[i];
-        CUresult cr = encode_tmap_3d_u8(&tmap[i], P.b_codes, static_cast<uint64_t>(P.K / 2), static_cast<uint64_t>(P.N),
-                                        static_cast<uint64_t>(a.G), BK_BYTES, C::W_ROWS);
+        // codes prepacked K-slab-major: [G][ceil(K/256)][N][128 bytes]; a tile's K-stage is one
+        // contiguous run of W_ROWS x 128 bytes
+        const uint64_t slabs = static_cast<uint64_t>(a.G) * ((P.K + 255) / 256);
+        CUresult cr = encode_tmap_3d_u8(&tmap[i], P.b_codes, BK_BYTES, static_cast<uint64_t>(P.N), slabs, BK_BYTES, C::W_ROWS);
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     if (a.nphase == 1) tmap[1] = tmap[0];

@@ -162,6 +162,34 @@ def test_route_topk_tensor_core_ragged(moe, config, T):
     _check_route_values(w, g, lg, w_ref, g_ref, lg_ref)
 
 
+@pytest.mark.parametrize("interleave", [0, 1])
+def test_prepack_layout(moe, interleave):
+    # the documented prepacked layout, restated with numpy: K-slab-major codes (zero past K/2) with
+    # the optional 64 gate + 64 up row interleave, and 512-byte scale tiles
+    rng = np.random.default_rng(11 + interleave)
+    G, N, K = 3, 256, 384
+    codes = rng.integers(0, 256, (G, N, K // 2), dtype=np.uint8)
+    sf = rng.integers(0, 256, (G, N, K // 16), dtype=np.uint8)
+    cp, sp = moe.moe_prepack_nvfp4(dev(codes), dev(sf), bool(interleave))
+    src = np.arange(N)
+    if interleave:
+        blk, w = src // 128, src % 128
+        src = np.where(w < 64, blk * 64 + w, N // 2 + blk * 64 + (w - 64))
+    slabs = (K + 255) // 256
+    padded = np.zeros((G, N, slabs * 128), np.uint8)
+    padded[:, :, :K // 2] = codes[:, src, :]
+    want_codes = padded.reshape(G, N, slabs, 128).transpose(0, 2, 1, 3)
+    np.testing.assert_array_equal(cp.cpu().numpy().reshape(G, slabs, N, 128), want_codes)
+    want_sf = np.zeros((G, N // 128, K // 64, 512), np.uint8)
+    rs = sf[:, src, :]
+    for r in range(N):
+        for kb in range(K // 64):
+            t = want_sf[:, r // 128, kb]
+            rr = r % 128
+            t[:, (rr % 32) * 16 + (rr // 32) * 4:(rr % 32) * 16 + (rr // 32) * 4 + 4] = rs[:, r, kb * 4:kb * 4 + 4]
+    np.testing.assert_array_equal(sp.cpu().numpy().reshape(G, N // 128, K // 64, 512), want_sf)
+
+
 def test_route_exact_ties_lowest_index(moe):
     H, E, k, T = 256, 16, 4, 8
     rng = np.random.default_rng(3)
