@@ -82,7 +82,7 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     L.perm_src = take(n * 4);
     L.src_perm = take(n * 4);
     L.row_token = take(P * 4);
-    L.hist = take(perm_chunks(n) * E * 4);
+    L.hist = take((perm_chunks(n) + 1) * E * 4);  // per-chunk counts + per-expert totals
     // token blocks of the expert GEMMs: at most ceil(P / 32) + E + 1 (32-row blocks in the smallest schedule)
     const int64_t nblk = (P + 31) / 32 + E + 1;
     L.h_codes = take(P * I / 2);
@@ -298,14 +298,14 @@ moe_status_t moe_permute(const int32_t* topk_ids, int T, int k, int E, int with_
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32 || k > E)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d k=%d E=%d outside the supported range", T, k, E);
     if (!topk_ids || !expert_offsets || !perm_src || !src_perm) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
-    const size_t need = 256 + static_cast<size_t>(perm_chunks(static_cast<int64_t>(T) * k)) * E * 4;
+    const size_t need = 256 + static_cast<size_t>(perm_chunks(static_cast<int64_t>(T) * k) + 1) * E * 4;
     MOE_TRY(check_ws(ws, ws_bytes, need));
     MOE_TRY(check_device());
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     WsHeader* hdr = static_cast<WsHeader*>(ws);
     int32_t* hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
-    MOE_CUDA(launch_permute(topk_ids, T, k, E, with_shared ? 1 : 0, expert_offsets, nullptr, perm_src, src_perm, row_token,
-                            hist, &hdr->status, s),
+    MOE_CUDA(launch_permute(topk_ids, T, k, E, with_shared ? 1 : 0, expert_offsets, perm_src, src_perm, row_token, hist,
+                            &hdr->perm_ticket, &hdr->status, s),
              "permute launch");
     return MOE_OK;
 }
@@ -463,8 +463,8 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
                  "top-k");
         MOE_CUDA(mark(2), "event record");
         // permutation by expert id, the shared expert appended as group E
-        MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), nullptr, P32(W.perm_src),
-                                P32(W.src_perm), P32(W.row_token), P32(W.hist), &hdr->status, s),
+        MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), P32(W.perm_src), P32(W.src_perm),
+                                P32(W.row_token), P32(W.hist), &hdr->perm_ticket, &hdr->status, s),
                  "permute");
     }
     MOE_CUDA(mark(3), "event record");

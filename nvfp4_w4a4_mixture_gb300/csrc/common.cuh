@@ -23,7 +23,8 @@ struct WsHeader {
     float s_x;             // tensor scale of the layer input
     unsigned ticket;       // CTAs of the one-launch front half that finished (zero between calls)
     int gemm_tiles;        // tile counter of a standalone grouped GEMM (cleared before its launch)
-    int pad[59];
+    unsigned perm_ticket;  // row-scan CTAs of the permutation that finished (zero between calls)
+    int pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

@@ -31,14 +31,11 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, int E, cons
 
 // ---- permute.cu
 constexpr int kPermChunk = 512;  // assignments per warp-chunk
-constexpr int kGemmBM = 128;     // rows per GEMM M-tile (the permutation also writes tile offsets)
 inline int64_t perm_chunks(int64_t n) { return n <= 0 ? 1 : (n + kPermChunk - 1) / kPermChunk; }
-// offsets: [E+2]; tile_off: [E+2] prefix of ceil(rows_g / kGemmBM) over the E+1 groups (nullable).
+// offsets: [E+2]; hist: (perm_chunks(n) + 1) * E ints of scratch; ticket: zero between calls.
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* offsets,
-                           int32_t* tile_off, int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist,
+                           int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist, unsigned* ticket,
                            int* status, cudaStream_t stream);
-// tile_off[g] = sum_{g' < g} ceil((offsets[g'+1] - offsets[g']) / kGemmBM), g = 0..G.
-cudaError_t launch_tile_offsets(const int32_t* offsets, int G, int32_t* tile_off, cudaStream_t stream);
 
 // ---- front.cu (small batches: quantize + router + top-k + permute in one launch)
 bool front_fits(int T, int H, int E, int k);

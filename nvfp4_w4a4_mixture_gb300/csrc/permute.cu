@@ -2,13 +2,13 @@
 //
 // The flat assignment list f = t*k + j is cut into warp-chunks of kPermChunk entries.
 //   1. histogram: each warp counts its chunk per expert (warp match: one shared-memory add per
-//      run of equal ids, no atomics) -> hist[chunk][E];
-//   2. scan (one CTA): per expert, an exclusive scan over the chunks, then an exclusive scan over
-//      experts -> expert offsets, the global base of every (chunk, expert) and the GEMM tile
-//      offsets (ceil(rows / 128) per group, the shared expert appended as group E);
-//   3. scatter: each warp walks its chunk in order; an entry's position is its chunk base plus
-//      the number of earlier entries of the same expert in the chunk. Ascending f within every
-//      expert (stable), independent of scheduling: bit-exact.
+//      run of equal ids, no atomics) -> hist[expert][chunk];
+//   2. row scan (one CTA per expert): exclusive scan of the expert's counts over the chunks, the
+//      expert's total to totals[expert]; the last CTA to finish (atomic ticket, no waiting) scans
+//      the totals over the experts -> expert offsets (the shared expert appended as group E);
+//   3. scatter: each warp walks its chunk in order; an entry's position is its expert's offset
+//      plus its chunk's base plus the number of earlier entries of the same expert in the chunk.
+//      Ascending f within every expert (stable), independent of scheduling: bit-exact.
 #include <cub/block/block_scan.cuh>
 
 #include "kernels.cuh"
@@ -43,61 +43,67 @@ __global__ void __launch_bounds__(kPermWarps * 32)
         if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
         __syncwarp();
     }
-    for (int e = lane; e < E; e += 32) hist[c * E + e] = my[e];
+    for (int e = lane; e < E; e += 32) hist[static_cast<int64_t>(e) * nchunks + c] = my[e];
 }
 
 constexpr int kScanThreads = 1024;
+constexpr int kRowScanThreads = 256;
 
-__global__ void __launch_bounds__(kScanThreads)
-    k_perm_scan(int32_t* __restrict__ hist, int64_t nchunks, int E, int T, int k, int with_shared,
-                int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off)
+// One CTA per expert row of hist [E][nchunks]: exclusive scan in place, row total to totals[e];
+// the last CTA scans the totals into the expert offsets and returns the ticket to zero.
+__global__ void __launch_bounds__(kRowScanThreads)
+    k_perm_rowscan(int32_t* __restrict__ hist, int32_t* __restrict__ totals, int64_t nchunks, int E, int T,
+                   int with_shared, int32_t* __restrict__ offsets, unsigned* ticket)
 {
-    using Scan = cub::BlockScan<int32_t, kScanThreads>;
+    using Scan = cub::BlockScan<int32_t, kRowScanThreads>;
     __shared__ typename Scan::TempStorage tmp;
-    __shared__ int32_t total_s;
-    // items per thread: E <= 1024 experts (+ the shared group)
-    const int e = threadIdx.x;
-    int32_t cnt = 0;
-    if (e < E) {
-        for (int64_t c = 0; c < nchunks; ++c) {
-            const int32_t v = hist[c * E + e];
-            hist[c * E + e] = cnt;
-            cnt += v;
-        }
+    __shared__ unsigned last_s;
+    const int e = blockIdx.x, tid = threadIdx.x;
+    int32_t* row = hist + static_cast<int64_t>(e) * nchunks;
+    const int64_t per = (nchunks + kRowScanThreads - 1) / kRowScanThreads;
+    const int64_t c0 = tid * per, c1 = min(nchunks, c0 + per);
+    int32_t sum = 0;
+    for (int64_t c = c0; c < c1; ++c) sum += row[c];
+    int32_t run, agg;
+    Scan(tmp).ExclusiveSum(sum, run, agg);
+    for (int64_t c = c0; c < c1; ++c) {
+        const int32_t v = row[c];
+        row[c] = run;
+        run += v;
     }
-    int32_t off;
-    Scan(tmp).ExclusiveSum(cnt, off);
-    if (e < E) offsets[e] = off;
-    if (e == E - 1) total_s = off + cnt;
+    if (tid == 0) totals[e] = agg;
+    __threadfence();
     __syncthreads();
-    const int32_t total = total_s;  // == T*k
-    if (e == 0) {
+    if (tid == 0) last_s = atomicAdd(ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
+    __syncthreads();
+    if (!last_s) return;
+    __threadfence();
+    // expert offsets: exclusive scan of the E <= 1024 totals, 4 per thread
+    int32_t v[4], o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int g = tid * 4 + i;
+        v[i] = g < E ? __ldcg(totals + g) : 0;
+    }
+    int32_t total;
+    __syncthreads();  // tmp reused
+    Scan(tmp).ExclusiveSum(v, o, total);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int g = tid * 4 + i;
+        if (g < E) offsets[g] = o[i];
+    }
+    if (tid == 0) {
         offsets[E] = total;
         offsets[E + 1] = total + (with_shared ? T : 0);
-    }
-    if (e < E)
-        for (int64_t c = 0; c < nchunks; ++c) hist[c * E + e] += off;
-    if (tile_off) {
-        __syncthreads();
-        // groups 0..E-1 (routed) and E (shared): ceil(rows / BM)
-        int32_t mt = e < E ? (cnt + kGemmBM - 1) / kGemmBM : 0;
-        Scan(tmp).ExclusiveSum(mt, off);
-        if (e < E) tile_off[e] = off;
-        __syncthreads();
-        if (e == E - 1) total_s = off + mt;
-        __syncthreads();
-        if (e == 0) {
-            const int32_t shared_rows = with_shared ? T : 0;
-            tile_off[E] = total_s;
-            tile_off[E + 1] = total_s + (shared_rows + kGemmBM - 1) / kGemmBM;
-        }
+        *ticket = 0u;
     }
 }
 
 __global__ void __launch_bounds__(kPermWarps * 32)
     k_perm_scatter(const int32_t* __restrict__ ids, int64_t n, int E, int k, int T, int with_shared, int64_t nchunks,
-                   const int32_t* __restrict__ hist, int32_t* __restrict__ perm_src, int32_t* __restrict__ src_perm,
-                   int32_t* __restrict__ row_token)
+                   const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+                   int32_t* __restrict__ src_perm, int32_t* __restrict__ row_token)
 {
     extern __shared__ int32_t base_s[];  // [kPermWarps][E]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kPermWarps * 32)
     const int64_t c = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp;
     if (c >= nchunks) return;
     int32_t* my = base_s + warp * E;
-    for (int e = lane; e < E; e += 32) my[e] = hist[c * E + e];
+    for (int e = lane; e < E; e += 32) my[e] = __ldg(offsets + e) + hist[static_cast<int64_t>(e) * nchunks + c];
     __syncwarp();
     const int64_t beg = c * kPermChunk, end = min(n, beg + kPermChunk);
     const unsigned lt = (1u << lane) - 1u;
@@ -190,11 +196,11 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* offsets,
-                           int32_t* tile_off, int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist,
+                           int32_t* perm_src, int32_t* src_perm, int32_t* row_token, int32_t* hist, unsigned* ticket,
                            int* status, cudaStream_t stream)
 {
     const int64_t n = static_cast<int64_t>(T) * k;
-    if (n <= kSmallPerm && !tile_off) {
+    if (n <= kSmallPerm) {
         k_perm_small<<<1, kScanThreads, 0, stream>>>(topk_ids, static_cast<int>(n), E, k, T, with_shared, offsets,
                                                      perm_src, src_perm, row_token, status);
         return cudaGetLastError();
@@ -202,43 +208,11 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int wit
     const int64_t nchunks = perm_chunks(n);
     const int blocks = static_cast<int>((nchunks + kPermWarps - 1) / kPermWarps);
     const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
+    int32_t* totals = hist + nchunks * E;
     k_perm_hist<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, nchunks, hist, status);
-    k_perm_scan<<<1, kScanThreads, 0, stream>>>(hist, nchunks, E, T, k, with_shared, offsets, tile_off);
-    k_perm_scatter<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, k, T, with_shared, nchunks, hist,
+    k_perm_rowscan<<<E, kRowScanThreads, 0, stream>>>(hist, totals, nchunks, E, T, with_shared, offsets, ticket);
+    k_perm_scatter<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, k, T, with_shared, nchunks, hist, offsets,
                                                               perm_src, src_perm, row_token);
-    return cudaGetLastError();
-}
-
-// tile_off[g] for caller-given group offsets (the public grouped GEMM).
-__global__ void __launch_bounds__(kScanThreads) k_tile_offsets(const int32_t* __restrict__ offsets, int G,
-                                                               int32_t* __restrict__ tile_off)
-{
-    using Scan = cub::BlockScan<int32_t, kScanThreads>;
-    __shared__ typename Scan::TempStorage tmp;
-    __shared__ int32_t carry;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
-    for (int g0 = 0; g0 < G; g0 += kScanThreads) {
-        const int g = g0 + threadIdx.x;
-        int32_t mt = 0;
-        if (g < G) {
-            const int32_t rows = offsets[g + 1] - offsets[g];
-            mt = rows > 0 ? (rows + kGemmBM - 1) / kGemmBM : 0;
-        }
-        int32_t off, agg;
-        Scan(tmp).ExclusiveSum(mt, off, agg);
-        const int32_t c = carry;
-        if (g < G) tile_off[g] = c + off;
-        __syncthreads();
-        if (threadIdx.x == 0) carry = c + agg;
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) tile_off[G] = carry;
-}
-
-cudaError_t launch_tile_offsets(const int32_t* offsets, int G, int32_t* tile_off, cudaStream_t stream)
-{
-    k_tile_offsets<<<1, kScanThreads, 0, stream>>>(offsets, G, tile_off);
     return cudaGetLastError();
 }
 
