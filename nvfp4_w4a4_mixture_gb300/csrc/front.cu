@@ -2,16 +2,18 @@
 // router logits, FP32 softmax top-k with renormalised weights, shared gate, and the stable
 // permutation by expert id.
 //
-// Every CTA but the last computes the logits of 8 router rows for all tokens (the same per-lane
-// strided FP32 sums and butterfly as the standalone router, so the logits are bit-identical to it);
-// the last CTA quantises x. Each CTA then takes a ticket; the last CTA to finish reads all logits
-// and does the top-k (one warp per token: integer keys, a four-entry cache per lane, lowest index
-// first on ties) and the stable permutation (rank by counting, offsets by binary search over the
-// ids in position order), then returns the ticket counter to zero for the next call. No CTA waits
-// for another, so the launch needs no co-residency.
+// Every CTA computes the logits of 8 router rows for all tokens (the same per-lane strided FP32
+// sums and butterfly as the standalone router, so the logits are bit-identical to it), takes the
+// tensor max of x while staging it and quantises its share of x's 16-element blocks. Each CTA then
+// takes a ticket; the last CTA to finish reads all logits and does the top-k (one warp per token:
+// integer keys, a four-entry cache per lane, lowest index first on ties) and the stable
+// permutation (rank by counting, offsets by binary search over the ids in position order), then
+// returns the ticket counter to zero for the next call. No CTA waits for another, so the launch
+// needs no co-residency.
 #include <cfloat>
 
 #include "kernels.cuh"
+#include "route.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -59,66 +61,33 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = a.H, E = a.E, T = a.T, k = a.k;
     const int e = blockIdx.x * kFrontWarps + warp;  // this warp's router row (E = shared gate)
-    const int n_logit_ctas = (E + 1 + kFrontWarps - 1) / kFrontWarps;
 
     // The router row does not depend on the previous launch on the stream: its first 2048 columns
     // are loaded before waiting for that launch (x and the routing outputs may still be in use there).
-    const bool has_row = blockIdx.x < n_logit_ctas && e <= E;
+    const bool has_row = e <= E;
     const uint16_t* wr = a.w_router + static_cast<int64_t>(has_row ? e : 0) * H;
     uint4 wv0[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-        const int h0 = u * 256 + lane * 8;
-        wv0[u] = has_row && h0 < H ? __ldg(reinterpret_cast<const uint4*>(wr + h0)) : make_uint4(0, 0, 0, 0);
-    }
+    router_row_prefetch(wr, H, has_row, wv0);
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
 
-    // ---- logits of this CTA's router rows, kFrontTT tokens per pass (CTAs 0 .. n_logit_ctas-1)
-    for (int t0 = 0; t0 < T && blockIdx.x < n_logit_ctas; t0 += kFrontTT) {
+    // ---- logits of this CTA's router rows, kFrontTT tokens per pass; every CTA sees all of x, so
+    // it also takes the tensor max on the way
+    uint32_t amax_bits = 0;
+    for (int t0 = 0; t0 < T; t0 += kFrontTT) {
         const int nt = min(kFrontTT, T - t0);
         const int vec_per_row = H / 8;
 #pragma unroll 4
         for (int i = tid; i < nt * vec_per_row; i += kFrontThreads) {
             const int t = i / vec_per_row, c = i % vec_per_row;
-            reinterpret_cast<uint4*>(xs + t * H)[c] =
-                __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t0 + t) * H) + c);
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<int64_t>(t0 + t) * H) + c);
+            reinterpret_cast<uint4*>(xs + t * H)[c] = v;
+            amax_bits = max(amax_bits, absmax8_bits(v));
         }
         __syncthreads();
         if (has_row) {
             float acc[kFrontTT];
-#pragma unroll
-            for (int t = 0; t < kFrontTT; ++t) acc[t] = 0.0f;
-            for (int base = 0; base < H; base += 8 * 256) {
-                uint4 wv[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int h0 = base + u * 256 + lane * 8;
-                    wv[u] = base == 0 ? wv0[u]
-                                      : (h0 < H ? __ldg(reinterpret_cast<const uint4*>(wr + h0)) : make_uint4(0, 0, 0, 0));
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int h0 = base + u * 256 + lane * 8;
-                    if (h0 >= H) break;
-                    const uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
-#pragma unroll
-                    for (int t = 0; t < kFrontTT; ++t) {
-                        const uint4 xv = *reinterpret_cast<const uint4*>(xs + t * H + h0);
-                        const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu)));
-                            acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16)));
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < kFrontTT; ++t) {
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[t] = __fadd_rn(acc[t], __shfl_xor_sync(0xFFFFFFFFu, acc[t], o));
-            }
+            router_row_logits<kFrontTT>(xs, H, wr, wv0, acc);
             if (lane < nt) {
                 float v = 0.0f;
 #pragma unroll
@@ -131,44 +100,20 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
         __syncthreads();
     }
 
-    // ---- last CTA: W4A4 quantisation of x (tensor max, then one thread per 16-element block)
-    if (blockIdx.x == n_logit_ctas) {
+    // ---- W4A4 quantisation of x: the tensor scale from the max, then this CTA's share of the blocks
+    amax_bits = __reduce_max_sync(0xFFFFFFFFu, amax_bits);
+    if (lane == 0) red_s[warp] = __uint_as_float(amax_bits);
+    __syncthreads();
+    float amax = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kFrontWarps; ++w) amax = fmaxf(amax, red_s[w]);
+    const float S = nvfp4_tensor_scale(amax);
+    if (blockIdx.x == 0 && tid == 0) *a.s_x = S;
+    {
         const int64_t nblocks = static_cast<int64_t>(T) * H / 16;
-        uint32_t m = 0;
-        for (int64_t b = tid; b < nblocks; b += kFrontThreads) {
-            const uint4 p0 = __ldg(reinterpret_cast<const uint4*>(a.x + b * 16));
-            const uint4 p1 = __ldg(reinterpret_cast<const uint4*>(a.x + b * 16) + 1);
-            const uint32_t w8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                m = max(m, __float_as_uint(fabsf(bf16_to_f32(w8[i] & 0xFFFFu))));
-                m = max(m, __float_as_uint(fabsf(bf16_to_f32(w8[i] >> 16))));
-            }
-        }
-        m = __reduce_max_sync(0xFFFFFFFFu, m);
-        if (lane == 0) red_s[warp] = __uint_as_float(m);
-        __syncthreads();
-        float amax = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kFrontWarps; ++w) amax = fmaxf(amax, red_s[w]);
-        const float S = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
-        if (tid == 0) *a.s_x = S;
-        const float six_s = __fmul_rn(6.0f, S);
-        for (int64_t b = tid; b < nblocks; b += kFrontThreads) {
-            float v[16];
-            const uint4 p0 = __ldg(reinterpret_cast<const uint4*>(a.x + b * 16));
-            const uint4 p1 = __ldg(reinterpret_cast<const uint4*>(a.x + b * 16) + 1);
-            const uint32_t w8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                v[2 * i] = bf16_to_f32(w8[i] & 0xFFFFu);
-                v[2 * i + 1] = bf16_to_f32(w8[i] >> 16);
-            }
-            uint32_t lo, hi;
-            const uint32_t sf = nvfp4_encode16(v, S, six_s, lo, hi);
-            *reinterpret_cast<uint2*>(a.xq_codes + b * 8) = make_uint2(lo, hi);
-            a.xq_sf[b] = static_cast<uint8_t>(sf);
-        }
+        const int64_t per = (nblocks + gridDim.x - 1) / gridDim.x;
+        const int64_t b0 = min(nblocks, static_cast<int64_t>(blockIdx.x) * per), b1 = min(nblocks, b0 + per);
+        quantize_blocks(a.x, b0, b1, S, kFrontThreads, a.xq_codes, a.xq_sf);
     }
 
     // ---- ticket: the last CTA to finish routes and permutes
@@ -194,34 +139,9 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
         }
         if (lane == 0) a.shared_g[t] = 1.0f / (1.0f + expf(-l_gate));
     }
-    // permutation: the position of assignment f is the number of assignments with a smaller id plus
-    // the earlier ones with the same id (stable); the ids in position order then give the expert
-    // offsets by binary search (offsets[e] = assignments with an id below e)
-    const int n = T * k;
+    // permutation (stable; offsets by binary search over the ids in position order)
     __syncthreads();  // ids_s complete
-    for (int f = tid; f < n; f += kFrontThreads) {
-        const int id = ids_s[f];
-        int pos = 0;
-        for (int q = 0; q < n; ++q) {
-            const int o = ids_s[q];
-            pos += (o < id) | ((o == id) & (q < f));
-        }
-        a.perm_src[pos] = f;
-        a.src_perm[f] = pos;
-        a.row_token[pos] = f / k;
-        sorted_s[pos] = id;
-    }
-    __syncthreads();
-    for (int e = tid; e <= E; e += kFrontThreads) {
-        int lo = 0, hi = n;  // first position whose id is >= e
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sorted_s[mid] < e) lo = mid + 1; else hi = mid;
-        }
-        a.offsets[e] = lo;
-    }
-    if (tid == 0) a.offsets[E + 1] = n + T;
-    for (int t = tid; t < T; t += kFrontThreads) a.row_token[n + t] = t;
+    block_small_permute(ids_s, T * k, k, T, E, kFrontThreads, sorted_s, a.offsets, a.perm_src, a.src_perm, a.row_token);
     for (int i = tid; i < a.n_ready; i += kFrontThreads) a.ready[i] = 0;
     if (tid == 0) *a.ticket = 0u;  // every CTA has taken its ticket: ready for the next call
 }
@@ -245,7 +165,7 @@ cudaError_t launch_front(const uint16_t* x, int T, int H, int E, int k, const ui
     }
     FrontArgs a{x, T, H, E, k, w_router, bias, logits, xq_codes, xq_sf, s_x, topk_ids, topk_w, shared_g, offsets,
                 perm_src, src_perm, row_token, ticket, ready, n_ready};
-    const int grid = (E + 1 + kFrontWarps - 1) / kFrontWarps + 1;  // router rows + one quantising CTA
+    const int grid = (E + 1 + kFrontWarps - 1) / kFrontWarps;  // 8 router rows per CTA
     return launch_pdl(k_decode_front, dim3(grid), dim3(kFrontThreads), smem, stream, a);
 }
 

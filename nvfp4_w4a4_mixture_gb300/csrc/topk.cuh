@@ -19,13 +19,15 @@ __device__ __forceinline__ float key_value(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// A lane's four largest keys, largest first (equal keys: lowest slot first); unused entries hold 0.
+// A lane's four largest keys not yet taken (bit i of `taken` set: slot i is gone), largest first
+// (equal keys: lowest slot first); unused entries hold 0. The keys stay read-only so the array lives
+// in registers.
 struct Top4 {
     uint32_t k[4];
     int s[4];
 };
 
-__device__ __forceinline__ void lane_top4(const uint32_t (&key)[32], Top4& c)
+__device__ __forceinline__ void lane_top4(const uint32_t (&key)[32], uint32_t taken, Top4& c)
 {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -34,7 +36,7 @@ __device__ __forceinline__ void lane_top4(const uint32_t (&key)[32], Top4& c)
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        uint32_t kv = key[i];
+        uint32_t kv = ((taken >> i) & 1u) ? 0u : key[i];
         int sv = i;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // insertion: a strictly larger key moves ahead
@@ -64,7 +66,8 @@ __device__ __forceinline__ void warp_topk(const float* l, int E, int k, float& s
         key[i] = ee < E ? order_key(__ldcg(l + ee)) : 0u;
     }
     Top4 c;
-    lane_top4(key, c);
+    uint32_t taken = 0;
+    lane_top4(key, taken, c);
     sel_l = 0.0f;
     sel_i = 0;
     uint32_t k0 = 0;
@@ -78,9 +81,7 @@ __device__ __forceinline__ void warp_topk(const float* l, int E, int k, float& s
             sel_i = widx;
         }
         if ((widx & 31) == lane) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i == c.s[0]) key[i] = 0u;
+            taken |= 1u << c.s[0];
 #pragma unroll
             for (int q = 0; q < 3; ++q) {
                 c.k[q] = c.k[q + 1];
@@ -88,7 +89,7 @@ __device__ __forceinline__ void warp_topk(const float* l, int E, int k, float& s
             }
             c.k[3] = 0u;
             c.s[3] = 31;
-            if (c.k[0] == 0u) lane_top4(key, c);
+            if (c.k[0] == 0u) lane_top4(key, taken, c);
         }
     }
     l0 = key_value(k0);
