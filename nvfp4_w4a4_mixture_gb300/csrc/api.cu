@@ -511,7 +511,8 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     // 256-row weight tiles when H allows (half the MMAs and scale copies per weight byte); else
     // weights on the MMA's M side for few rows per expert (decode), 128 x 128 tiles otherwise
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
-    const int sched = gemm_wide_fits(ga) ? kSchedWide : small ? kSchedWeightsOnM : kSchedActOnM;
+    const int sched = gemm_wide_fits(ga) ? (T <= 32 ? kSchedWideNarrow : kSchedWide)
+                                         : small ? kSchedWeightsOnM : kSchedActOnM;
     if (!one_launch_front)  // (the one-launch front half clears them itself)
         MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");
     MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");

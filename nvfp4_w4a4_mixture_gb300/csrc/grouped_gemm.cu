@@ -48,7 +48,7 @@ constexpr int kTileRing = 8;               // tiles handed from the weight produ
 
 // Tile shapes. W_ROWS weight rows (one TMA box) by ACT_ROWS activation rows per tile; ACC_BUFS
 // accumulators of ACC_COLS tensor-memory columns.
-enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2 };
+enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3 };
 template <int kMode>
 struct Cfg;
 template <>
@@ -72,13 +72,26 @@ struct Cfg<kModeWide> {                    // activations on M, 256 weight rows 
     static constexpr bool SWAP = false;
 };
 
+template <>
+struct Cfg<kModeWideNarrow> {              // wide, for token blocks of at most 32 rows (decode): the
+    // activation region holds 32 rows, the MMA's other 96 A rows read the weight region behind it
+    // (their accumulator rows are never stored); the freed shared memory buys a fifth stage
+    static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 5, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
+    static constexpr int MMA_M = 128, MMA_N = 256;
+    static constexpr bool SWAP = false;
+};
+
 template <int kMode>
 struct Lay {
     using C = Cfg<kMode>;
     static constexpr int WB = C::W_ROWS / 128;  // 128-row weight blocks per tile (scale tiles per K-step)
     static constexpr int W_BYTES = C::W_ROWS * BK_BYTES;
     static constexpr int ACT_BYTES = C::ACT_ROWS * BK_BYTES;
-    static constexpr int OFF_W = 0, OFF_ACT = W_BYTES, OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + WB * SF_STAGE;
+    // activation rows first, so an MMA reading MMA_M > ACT_ROWS rows from them stays inside the stage
+    static constexpr bool ACT_FIRST = C::ACT_ROWS < C::MMA_M && !C::SWAP;
+    static_assert(!ACT_FIRST || (C::MMA_M - C::ACT_ROWS) * BK_BYTES <= W_BYTES, "A rows read past the activations");
+    static constexpr int OFF_ACT = ACT_FIRST ? 0 : W_BYTES, OFF_W = ACT_FIRST ? ACT_BYTES : 0;
+    static constexpr int OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + WB * SF_STAGE;
     static constexpr int STAGE_BYTES = OFF_SFACT + SF_STAGE;
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
     static constexpr int SF_COL = C::ACC_BUFS * C::ACC_COLS;  // first scale-factor column
@@ -823,11 +836,12 @@ bool gemm_wide_fits(const GemmArgs& a)
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream)
 {
-    if (schedule == kSchedWide && !gemm_wide_fits(a)) schedule = kSchedActOnM;
+    if ((schedule == kSchedWide || schedule == kSchedWideNarrow) && !gemm_wide_fits(a)) schedule = kSchedActOnM;
     if (schedule == kSchedAuto) schedule = p_max <= 64 ? kSchedWeightsOnM : kSchedActOnM;
     switch (schedule) {
         case kSchedWeightsOnM: return launch_t<kModeSwap>(a, p_max, sms, stream);
         case kSchedWide: return launch_t<kModeWide>(a, p_max, sms, stream);
+        case kSchedWideNarrow: return launch_t<kModeWideNarrow>(a, p_max, sms, stream);
         default: return launch_t<kModeActM>(a, p_max, sms, stream);
     }
 }
