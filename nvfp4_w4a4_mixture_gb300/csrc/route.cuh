@@ -1,5 +1,5 @@
-// route.cuh -- block-level pieces of the small-batch routing front half, shared by the one-launch
-// front kernel and the routing prologue of the fused decode launch.
+// route.cuh -- block-level pieces of the small-batch routing front half (the one-launch front
+// kernel): router-row logits, x quantisation, the small stable permutation.
 #pragma once
 #include <cstdint>
 
