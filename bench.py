@@ -402,17 +402,20 @@ def run_ours(args, c, d):
     ms = d.max(ms_local)
     value = d.world * T / (ms / 1000.0)
 
-    # ---- per-stage durations of the same launch sequence (CUDA events at the stage boundaries)
+    # ---- per-stage durations of the same launch sequence (CUDA events at the stage boundaries). A
+    # spin kernel (~0.5 ms) ahead of each step lets the host queue the whole step first, so an
+    # interval holds its kernel's device time (with the launch gap in front of it), not the host's
+    # launch latency.
     Kp = min(K, 500)
     st_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(m.LAYER_STAGES) + 1)] for _ in range(Kp)]
     with torch.cuda.stream(stream):
         for i in range(Kp):
             flush.zero_()
+            torch.cuda._sleep(1_000_000)
             m.moe_layer_forward_profiled(layers[0], x, st_ev[i], residual=x if L > 1 else None, out=bufs[0], ws=ws)
     torch.cuda.synchronize()
-    stage_us = {}
-    for j, name in enumerate(m.LAYER_STAGES):
-        stage_us[name] = 1000.0 * statistics.mean(e[j].elapsed_time(e[j + 1]) for e in st_ev)
+    durs = [[e[j].elapsed_time(e[j + 1]) for e in st_ev] for j in range(len(m.LAYER_STAGES))]
+    stage_us = {name: 1000.0 * statistics.mean(durs[j]) for j, name in enumerate(m.LAYER_STAGES)}
     if one_launch_front(c):
         # one launch covers the first three stages: events 1..3 follow it back to back
         stage_us = {"front": sum(stage_us.pop(n) for n in ("quantize", "route", "permute")), **stage_us}
@@ -475,6 +478,7 @@ def run_ours(args, c, d):
                            "fp4_tc_frac": fp4_frac, "fp4_peak_tflops": fp4_peak,
                            "fp4_peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (peak_src, FP4_OVER_BF16)},
         "stages_us": stage_us,
+        "stages_timed_by": "stream events at the stage boundaries, each step queued behind a spin kernel",
         "step_ms_median": statistics.median(step_ms),
         "e2e": {"value": d.world * T / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms, "cuda_graph": False},

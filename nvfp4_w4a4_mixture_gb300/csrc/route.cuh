@@ -10,7 +10,8 @@ namespace moe {
 // Router logits of one router row for kTT staged tokens, by one warp: xs = kTT rows of H bf16 in
 // shared memory, wr = the router row, w0 = its first 2048 columns already loaded (lane l holds
 // columns u*256 + 8l .. +7 of each 2048-column chunk). Per-lane strided FP32 sums in a fixed order,
-// then a butterfly: every caller gets bit-identical logits.
+// then a butterfly: every caller gets bit-identical logits. A product of two bf16 values is exact in
+// FP32 (8 + 8 significand bits), so each fused multiply-add rounds once, like an add of the product.
 template <int kTT>
 __device__ __forceinline__ void router_row_logits(const uint16_t* xs, int H, const uint16_t* wr, const uint4 (&w0)[8],
                                                   float (&acc)[kTT])
@@ -36,8 +37,8 @@ __device__ __forceinline__ void router_row_logits(const uint16_t* xs, int H, con
                 const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu)));
-                    acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16)));
+                    acc[t] = __fmaf_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu), acc[t]);
+                    acc[t] = __fmaf_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16), acc[t]);
                 }
             }
         }
@@ -79,15 +80,16 @@ __device__ __forceinline__ uint32_t absmax8_bits(const uint4& v)
 __device__ __forceinline__ float nvfp4_tensor_scale(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f); }
 
 // NVFP4 encoding of the 16-element blocks b0 .. b1-1 of bf16 x with tensor scale S, one block per
-// thread (nthreads threads).
-__device__ __forceinline__ void quantize_blocks(const uint16_t* x, int64_t b0, int64_t b1, float S, int nthreads,
-                                                uint8_t* codes, uint8_t* sf)
+// thread: thread tid of a group of nthreads. x is global or shared memory (row-major [T][H], H a
+// multiple of 16, so block b is the 16 values from x + 16 b).
+__device__ __forceinline__ void quantize_blocks(const uint16_t* x, int64_t b0, int64_t b1, float S, int tid,
+                                                int nthreads, uint8_t* codes, uint8_t* sf)
 {
     const float six_s = __fmul_rn(6.0f, S);
-    for (int64_t b = b0 + threadIdx.x; b < b1; b += nthreads) {
+    for (int64_t b = b0 + tid; b < b1; b += nthreads) {
         float v[16];
-        const uint4 p0 = __ldg(reinterpret_cast<const uint4*>(x + b * 16));
-        const uint4 p1 = __ldg(reinterpret_cast<const uint4*>(x + b * 16) + 1);
+        const uint4 p0 = reinterpret_cast<const uint4*>(x + b * 16)[0];
+        const uint4 p1 = reinterpret_cast<const uint4*>(x + b * 16)[1];
         const uint32_t w8[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -101,22 +103,40 @@ __device__ __forceinline__ void quantize_blocks(const uint16_t* x, int64_t b0, i
     }
 }
 
-// Stable permutation of the n = T*k assignments ids[0..n) (shared memory) by expert id, by one CTA:
-// the position of assignment f is the number of assignments with a smaller id plus the earlier ones
-// with the same id; offsets[e] (e = 0..E) = assignments with an id below e, found by binary search
-// over the ids in position order (sorted: n ints of shared memory); offsets[E+1] = n + T and the
-// shared expert's rows n + t hold token t. Contains one block barrier (all threads must call).
-__device__ __forceinline__ void block_small_permute(const int32_t* ids, int n, int k, int T, int E, int nthreads,
-                                                    int32_t* sorted, int32_t* offsets, int32_t* perm_src,
-                                                    int32_t* src_perm, int32_t* row_token)
+// GPU-scope fetch-and-add with acquire-release semantics: the caller's earlier writes (and those
+// of its CTA, ordered before it by a block barrier) are visible to whoever reads the result, and
+// writes that preceded the earlier additions are visible to the caller.
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Stable permutation of the n = T*k assignments ids[0..n) (shared memory, n <= 2 * kThreads, the
+// entries from n up to the next multiple of 4 set to INT_MAX) by expert id, by one CTA of kThreads
+// threads: the position of assignment f is the number of assignments with a smaller id plus the
+// earlier ones with the same id (ids read 4 at a time); offsets[e] (e = 0..E, E + 1 <= 5 *
+// kThreads) = the assignments with an id below e, a lower bound in the ids in position order
+// (sorted: n ints of shared memory), every thread running its bounds side by side; offsets[E+1] =
+// n + T and the shared expert's rows n + t hold token t. Contains one block barrier (all threads
+// must call).
+template <int kThreads>
+__device__ __forceinline__ void block_small_permute(const int32_t* ids, int n, int k, int T, int E, int32_t* sorted,
+                                                    int32_t* offsets, int32_t* perm_src, int32_t* src_perm,
+                                                    int32_t* row_token)
 {
     const int tid = threadIdx.x;
-    for (int f = tid; f < n; f += nthreads) {
+    for (int f = tid; f < n; f += kThreads) {
         const int id = ids[f];
         int pos = 0;
-        for (int q = 0; q < n; ++q) {
-            const int o = ids[q];
-            pos += (o < id) | ((o == id) & (q < f));
+#pragma unroll 2
+        for (int q0 = 0; q0 < n; q0 += 4) {
+            const int4 v = *reinterpret_cast<const int4*>(ids + q0);
+            pos += (v.x < id) | ((v.x == id) & (q0 < f));
+            pos += (v.y < id) | ((v.y == id) & (q0 + 1 < f));
+            pos += (v.z < id) | ((v.z == id) & (q0 + 2 < f));
+            pos += (v.w < id) | ((v.w == id) & (q0 + 3 < f));
         }
         perm_src[pos] = f;
         if (src_perm) src_perm[f] = pos;
@@ -124,16 +144,23 @@ __device__ __forceinline__ void block_small_permute(const int32_t* ids, int n, i
         sorted[pos] = id;
     }
     __syncthreads();
-    for (int e = tid; e <= E; e += nthreads) {
-        int lo = 0, hi = n;  // first position whose id is >= e
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sorted[mid] < e) lo = mid + 1; else hi = mid;
-        }
-        offsets[e] = lo;
+    constexpr int kE = 5;
+    int base[kE];
+#pragma unroll
+    for (int j = 0; j < kE; ++j) base[j] = 0;
+    for (int len = n; len > 1;) {  // branch-free lower bounds: the answer stays in [base, base + len]
+        const int half = len >> 1;
+#pragma unroll
+        for (int j = 0; j < kE; ++j) base[j] = sorted[base[j] + half] < tid + j * kThreads ? base[j] + half : base[j];
+        len -= half;
+    }
+#pragma unroll
+    for (int j = 0; j < kE; ++j) {
+        const int e = tid + j * kThreads;
+        if (e <= E) offsets[e] = base[j] + (sorted[base[j]] < e);
     }
     if (tid == 0) offsets[E + 1] = n + T;
-    for (int t = tid; t < T; t += nthreads) row_token[n + t] = t;
+    for (int t = tid; t < T; t += kThreads) row_token[n + t] = t;
 }
 
 }  // namespace moe

@@ -2,11 +2,13 @@
 //
 // Logits: one warp per router row, a tile of kRouterTT tokens staged in shared memory, 16-byte
 // loads of the router row (each row of W_r is read once per token tile). Every product of two
-// bf16 values is exact in FP32; the sum runs in a fixed order (per-lane strided partial sums,
-// then a butterfly), so the result is deterministic.
-// Top-k: one warp per token (see topk.cuh): k rounds of a warp arg-max on (logit desc, expert id
-// asc), which is the lowest-index tie rule; the renormalised weights are the softmax over the
-// selected logits (the full softmax denominator cancels), the shared gate is sigmoid(logit E).
+// bf16 values is exact in FP32, so a fused multiply-add rounds only the sum; the sum runs in a
+// fixed order (per-lane strided partial sums, then a butterfly), so the result is deterministic.
+// Top-k: one warp per token (see topk.cuh): the candidates at or above the k-th largest lane
+// maximum ranked on (logit desc, expert id asc), which is the lowest-index tie rule, with k rounds
+// of a warp arg-max when too many logits tie for the candidate list; the renormalised weights are
+// the softmax over the selected logits (the full softmax denominator cancels), the shared gate is
+// sigmoid(logit E).
 #include <cfloat>
 
 #include "kernels.cuh"
@@ -59,8 +61,8 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
                 const uint32_t xx[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu)));
-                    acc[t] = __fadd_rn(acc[t], __fmul_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16)));
+                    acc[t] = __fmaf_rn(bf16_to_f32(xx[i] & 0xFFFFu), bf16_to_f32(ww[i] & 0xFFFFu), acc[t]);
+                    acc[t] = __fmaf_rn(bf16_to_f32(xx[i] >> 16), bf16_to_f32(ww[i] >> 16), acc[t]);
                 }
             }
         }
@@ -88,14 +90,18 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     k_topk(const float* __restrict__ logits, int ld, int T, int E, int k, int32_t* __restrict__ topk_ids,
            float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
 {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
+    __shared__ uint2 cand_s[kTopkWarps][kTopkCand];
+    __shared__ uint2 sel_s[kTopkWarps][32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * kTopkWarps + warp;
     if (t >= T) return;
     const float* l = logits + static_cast<int64_t>(t) * ld;
     const float l_gate = lane == 0 ? __ldcg(l + E) : 0.0f;
     float sel_l, l0;
     int sel_i;
-    warp_topk(l, E, k, sel_l, sel_i, l0);
+    const bool done = E <= 512 ? warp_topk_threshold<16>(l, E, k, cand_s[warp], sel_s[warp], sel_l, sel_i, l0)
+                               : warp_topk_threshold<32>(l, E, k, cand_s[warp], sel_s[warp], sel_l, sel_i, l0);
+    if (!done) warp_topk(l, E, k, sel_l, sel_i, l0);
     const float w = warp_topk_weight(sel_l, l0, k);
     if (lane < k) {
         topk_ids[static_cast<int64_t>(t) * k + lane] = sel_i;

@@ -95,6 +95,72 @@ __device__ __forceinline__ void warp_topk(const float* l, int E, int k, float& s
     l0 = key_value(k0);
 }
 
+// Capacity of the candidate list of warp_topk_threshold, per warp.
+constexpr int kTopkCand = 64;
+
+// One warp, the same selection as warp_topk in a few straight-line steps, for E <= 32 * kNper and
+// k <= 32. Lane l holds logits l, l + 32, ... as keys; tau = the k-th largest of the 32 lane maxima
+// (lowest lane first on ties). At least k logits reach tau (those k maxima), so every logit of the
+// top k does: the candidates are the keys >= tau, compacted into cand[] (kTopkCand entries of
+// shared memory per warp) in lane order by a warp prefix sum. Each candidate's place is the number
+// of candidates ahead of it in (key desc, id asc) order; the first k places are the result, written
+// to out[] (k entries of shared memory). Returns false, with nothing selected, when more than
+// kTopkCand logits reach tau (many equal logits): the caller then runs warp_topk.
+template <int kNper>
+__device__ __forceinline__ bool warp_topk_threshold(const float* l, int E, int k, uint2* cand, uint2* out,
+                                                    float& sel_l, int& sel_i, float& l0)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t key[kNper];
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < kNper; ++i) {
+        const int ee = i * 32 + lane;
+        key[i] = ee < E ? order_key(__ldcg(l + ee)) : 0u;
+        m = max(m, key[i]);
+    }
+    int rank = 0;  // of this lane's maximum among the 32
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t mj = __shfl_sync(0xFFFFFFFFu, m, j);
+        rank += (mj > m) | ((mj == m) & (j < lane));
+    }
+    const unsigned at_k = __ballot_sync(0xFFFFFFFFu, rank == k - 1);
+    const uint32_t tau = __shfl_sync(0xFFFFFFFFu, m, __ffs(at_k) - 1);
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < kNper; ++i) c += key[i] >= tau;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    const int C = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (C > kTopkCand) return false;
+    int pos = incl - c;
+#pragma unroll
+    for (int i = 0; i < kNper; ++i)
+        if (key[i] >= tau) cand[pos++] = make_uint2(key[i], static_cast<uint32_t>(i * 32 + lane));
+    __syncwarp();
+    for (int j = lane; j < C; j += 32) {
+        const uint2 me = cand[j];
+        int r = 0;
+        for (int q = 0; q < C; ++q) {
+            const uint2 o = cand[q];
+            r += (o.x > me.x) | ((o.x == me.x) & (o.y < me.y));
+        }
+        if (r < k) out[r] = me;
+    }
+    __syncwarp();
+    const uint2 s = out[lane < k ? lane : 0];
+    sel_l = lane < k ? key_value(s.x) : 0.0f;
+    sel_i = lane < k ? static_cast<int>(s.y) : 0;
+    l0 = key_value(out[0].x);
+    __syncwarp();
+    return true;
+}
+
 // Renormalised routing weight of lane j < k: the softmax over the selected logits (the full
 // softmax denominator cancels); l0 is the largest selected logit.
 __device__ __forceinline__ float warp_topk_weight(float sel_l, float l0, int k)

@@ -211,6 +211,52 @@ def test_route_exact_ties_lowest_index(moe):
     assert np.all(w[:, 0] == w[:, 1]) and np.all(w[:, 1] == w[:, 2])
 
 
+def _tied_router(seed, E, H, n_tied):
+    """Router whose n_tied rows (scattered ids) are one row with a large bias: those experts tie for
+    every token, so the lowest ids among them must be selected, in id order."""
+    rng = np.random.default_rng(seed)
+    w_r = wl.gen_router(seed, E, H)
+    tied = np.sort(rng.choice(E, size=n_tied, replace=False))
+    w_r[tied] = w_r[tied[0]]
+    bias = np.zeros(E, np.float32)
+    bias[tied] = 100.0
+    return w_r, bias, tied
+
+
+@pytest.mark.parametrize("E,n_tied,T", [(512, 40, 4), (512, 70, 4), (512, 512, 9), (600, 40, 3), (600, 90, 70)])
+def test_route_topk_tied_groups(moe, E, n_tied, T):
+    # up to 64 candidates are ranked in shared memory; 70, 90 or 512 equal logits overflow the list
+    # and take the round-by-round arg-max; E = 600 uses 19 keys per lane
+    H, k = 256, 10
+    w_r, bias, tied = _tied_router(E + n_tied, E, H, n_tied)
+    if n_tied == E:
+        w_r[:E] = 0.0
+        bias[:] = 0.0
+    x = wl.gen_x(7, T, H)
+    ids_ref, w_ref, _, _ = oracle.router(x, w_r, k, bias=bias.astype(np.float64))
+    np.testing.assert_array_equal(ids_ref, np.broadcast_to(tied[:k], (T, k)))
+    dummy = (torch.zeros(1, 1, 8, dtype=torch.uint8, device="cuda"),) * 2 + (torch.ones(1, 2, device="cuda"),)
+    layer = moe.MoeLayer(H, E, k, 128, bf16_dev(w_r), dummy, dummy, torch.ones(E + 1, device="cuda"),
+                         logit_bias=dev(bias), prepacked=True)
+    ids, w, _, _ = moe.moe_route_topk(bf16_dev(x), layer)
+    moe.moe_read_device_status()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.all(w.cpu().numpy() == np.float32(1.0 / k))
+
+
+@pytest.mark.parametrize("n_tied", [40, 70])
+def test_layer_decode_tied_router(moe, n_tied):
+    # the one-launch front half (T = 4) on tied logits: its own top-k must pick the same experts
+    c = wl.CONFIGS["decode"]
+    H, E, k, I, T = c["H"], c["E"], c["k"], c["I"], c["T"]
+    w_r, bias, tied = _tied_router(n_tied, E, H, n_tied)
+    x = wl.gen_x(11, T, H)
+    gu, dn = I_.quantized_experts(n_tied, E, H, I, sorted(tied[:k].tolist()) + [E])
+    case = dict(H=H, E=E, k=k, I=I, T=T, x=x, w_r=w_r, bias=bias, gu=gu, dn=dn,
+                s_mid=np.full(E + 1, wl.s_mid_for("decode"), np.float32), rows=np.arange(T))
+    _check_layer(moe, case)
+
+
 # ------------------------------------------------------------------------------------------------
 # permute
 # ------------------------------------------------------------------------------------------------
@@ -405,10 +451,11 @@ def test_layer_prefill4k_sampled(moe):
     _check_layer(moe, I_.layer_case("prefill4k", sample=12))
 
 
-@pytest.mark.parametrize("T", [1, 7, 8, 9, 63, 64, 65, 130])
+@pytest.mark.parametrize("T", [1, 4, 5, 7, 8, 9, 63, 64, 65, 130])
 def test_layer_tiny_token_counts(moe, T):
-    # T <= 64 with T*k <= 512 takes the one-launch front half, larger T the separate kernels;
-    # 8 tokens are staged per router pass, so 7/8/9 and 63/64/65 straddle its edges
+    # T <= 64 with T*k <= 512 takes the one-launch front half, larger T the separate kernels; the
+    # front half stages 4 tokens per router pass up to T = 4 and 8 beyond, so 4/5, 7/8/9 and
+    # 63/64/65 straddle its edges
     _check_layer(moe, I_.layer_case("tiny", seed=T, T=T))
 
 
