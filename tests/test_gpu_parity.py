@@ -439,8 +439,10 @@ def test_layer_tiny(moe):
     assert err < 5e-3  # requantized codes agree, so the error is the bf16 rounding of y and out
 
 
-def test_layer_tiny_residual(moe):
-    _check_layer(moe, I_.layer_case("tiny"), residual=True)
+@pytest.mark.parametrize("T", [None, 3])
+def test_layer_tiny_residual(moe, T):
+    # 64 tokens: separate front kernels, 3 tokens: the one-launch front half
+    _check_layer(moe, I_.layer_case("tiny", seed=0 if T is None else 21, T=T), residual=True)
 
 
 def test_layer_decode_full_size(moe):
