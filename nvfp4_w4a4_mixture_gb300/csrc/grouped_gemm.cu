@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             uint8_t* hsf_tile = P.out_sf_tiled ? P.out_sf + (static_cast<int64_t>(ti.tbg) * (I / 64) + ti.nb) * SF_TILE : nullptr;
             if constexpr (!kSwap) {
                 // ---- TMEM lane = token row r; columns = the tile's weight rows. The warps of lane
-                // quarter q split the columns in two halves; each loads all of its columns, frees the
+                // quarter q split the columns in two halves; each loads its columns, frees the
                 // accumulator, then converts and stores.
                 constexpr int CPW = W_ROWS / 2;  // accumulator columns per warp
                 constexpr int NLD = CPW / 16;
@@ -601,13 +601,18 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 const bool any = q * 32 < ti.rows;  // warp-uniform: the quarter holds rows of the tile
                 const int64_t p = ti.row0 + r;
                 const bool swiglu = P.epilogue == kEpiSwiGLU;
-                uint32_t v[NLD][16];
-                if (any) {
-                    // SwiGLU: h block beta = half * NB + b takes gate column c*128 + jj*16 and up column
-                    // + 64 (c = beta / 4, jj = beta % 4: 128-row blocks hold 64 gate then 64 up rows);
-                    // otherwise the warp's columns are [half * CPW, half * CPW + CPW)
+                // The warp's columns come out of tensor memory in NR rounds of GPR 16-column groups
+                // (128 columns at once would not fit in registers); the accumulator is freed right
+                // after the last round's load.
+                constexpr int NR = NLD > 4 ? 2 : 1;
+                constexpr int GPR = NLD / NR;
+                auto load_round = [&](int rd, uint32_t (&v)[GPR][16]) {
+                    // SwiGLU: h block beta = half * NB + b takes gate column c*128 + jj*16 and up
+                    // column + 64 (c = beta / 4, jj = beta % 4: 128-row blocks hold 64 gate then 64 up
+                    // rows); otherwise the warp's columns are [half * CPW, half * CPW + CPW)
 #pragma unroll
-                    for (int i = 0; i < NLD; ++i) {
+                    for (int g = 0; g < GPR; ++g) {
+                        const int i = rd * GPR + g;
                         uint32_t col;
                         if (swiglu) {
                             const int beta = half * NB + (i >> 1);
@@ -615,25 +620,37 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         } else {
                             col = half * CPW + i * 16;
                         }
-                        ptx::tmem_ld16(tbase + col, v[i]);
+                        ptx::tmem_ld16(tbase + col, v[g]);
                     }
                     ptx::tmem_ld_wait();
-                }
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&st.acc_empty[as]);
+                };
+                auto release = [&]() {
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&st.acc_empty[as]);
+                };
                 if (any && swiglu) {
                     const float sg = sa * sb0, su = sa * sb1;
                     const float S = S_h;
                     const float inv_six_s = 1.0f / (6.0f * S);
+                    constexpr int BPR = NB / NR;  // h blocks per round
+                    float h[NB][16];
+#pragma unroll
+                    for (int rd = 0; rd < NR; ++rd) {
+                        uint32_t v[GPR][16];
+                        load_round(rd, v);
+                        if (rd == NR - 1) release();
+#pragma unroll
+                        for (int bb = 0; bb < BPR; ++bb)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                h[rd * BPR + bb][i] =
+                                    silu(__uint_as_float(v[2 * bb][i]) * sg) * (__uint_as_float(v[2 * bb + 1][i]) * su);
+                    }
                     uint32_t cw[2 * NB], sfw = 0;
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        float h[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[i] = silu(__uint_as_float(v[2 * b][i]) * sg) * (__uint_as_float(v[2 * b + 1][i]) * su);
                         uint32_t lo, hi;
-                        sfw |= encode16_rcp(h, S, inv_six_s, lo, hi) << (8 * b);
+                        sfw |= encode16_rcp(h[b], S, inv_six_s, lo, hi) << (8 * b);
                         cw[2 * b] = lo;
                         cw[2 * b + 1] = hi;
                     }
@@ -657,38 +674,46 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     }
                 } else if (any) {
 #pragma unroll
-                    for (int i = 0; i < NLD; ++i) {
-                        const int c0 = half * CPW + i * 16;  // tile column
-                        int col;
-                        float sb;
-                        if (P.gate_up) {
-                            const int cc = c0 & 127, upper = cc >= 64;
-                            col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
-                            sb = upper ? sb1 : sb0;
-                        } else {
-                            col = ti.nb * W_ROWS + c0;
-                            sb = sb0;
-                        }
-                        const float sc = sa * sb;
-                        if (valid) {
-                            if (P.epilogue == kEpiF32) {
-                                float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + po * P.N + col);
+                    for (int rd = 0; rd < NR; ++rd) {
+                        uint32_t v[GPR][16];
+                        load_round(rd, v);
+                        if (rd == NR - 1) release();
 #pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    o[j] = make_float4(__uint_as_float(v[i][4 * j]) * sc, __uint_as_float(v[i][4 * j + 1]) * sc,
-                                                       __uint_as_float(v[i][4 * j + 2]) * sc, __uint_as_float(v[i][4 * j + 3]) * sc);
+                        for (int g = 0; g < GPR; ++g) {
+                            const int c0 = half * CPW + (rd * GPR + g) * 16;  // tile column
+                            int col;
+                            float sb;
+                            if (P.gate_up) {
+                                const int cc = c0 & 127, upper = cc >= 64;
+                                col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
+                                sb = upper ? sb1 : sb0;
                             } else {
-                                uint32_t w[8];
+                                col = ti.nb * W_ROWS + c0;
+                                sb = sb0;
+                            }
+                            const float sc = sa * sb;
+                            if (valid) {
+                                if (P.epilogue == kEpiF32) {
+                                    float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + po * P.N + col);
 #pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    w[j] = f32_to_bf16(__uint_as_float(v[i][2 * j]) * sc) |
-                                           (f32_to_bf16(__uint_as_float(v[i][2 * j + 1]) * sc) << 16);
-                                uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + po * P.N + col);
-                                o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                                o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                                    for (int j = 0; j < 4; ++j)
+                                        o[j] = make_float4(__uint_as_float(v[g][4 * j]) * sc, __uint_as_float(v[g][4 * j + 1]) * sc,
+                                                           __uint_as_float(v[g][4 * j + 2]) * sc, __uint_as_float(v[g][4 * j + 3]) * sc);
+                                } else {
+                                    uint32_t w[8];
+#pragma unroll
+                                    for (int j = 0; j < 8; ++j)
+                                        w[j] = f32_to_bf16(__uint_as_float(v[g][2 * j]) * sc) |
+                                               (f32_to_bf16(__uint_as_float(v[g][2 * j + 1]) * sc) << 16);
+                                    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + po * P.N + col);
+                                    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                                    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                                }
                             }
                         }
                     }
+                } else {
+                    release();
                 }
             } else {
                 // ---- TMEM lane = weight row m of block nb; columns = token slots of the tile
