@@ -452,7 +452,11 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         constexpr int RW = C::ACT_ROWS / 2;      // rows per producer warp
         constexpr int NCR = RW / 4;              // code rows per lane (4 rows per warp instruction)
         constexpr int NSR = RW / 8;              // scale rows per lane (8 rows per warp instruction)
-        constexpr int LAG = C::STAGES - 2;       // stages in flight before one is published
+        // stages whose copies may still be in flight when a newer one is issued: stage i is published
+        // once stage i + LAG is issued and stage i's copies have landed. A deeper lag lets the
+        // copies of more stages overlap but holds each stage back until LAG more slots are free,
+        // i.e. until the MMA has consumed stage i + LAG - STAGES (decode: 2 us slower at 3 than at 1).
+        constexpr int LAG = 1;
         const int w2 = warp - 2, pt = tid - 64;
         const int chunk = lane & 7, word = lane & 3;
         const uint8_t* cptr[NCR];
