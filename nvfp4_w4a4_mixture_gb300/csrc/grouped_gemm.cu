@@ -119,6 +119,7 @@ struct Tail {
     int abort;
     int32_t wsum[32];
     int32_t tb_off[kGemmMaxG + 1];
+    int32_t g_off[kGemmMaxG + 1];  // the group offsets, so a tile's rows need no global load
 };
 
 // up-projection values handed from TMEM lanes 64..127 to lanes 0..63 (weights-on-M SwiGLU)
@@ -132,14 +133,18 @@ constexpr size_t smem_bytes()
     return 1024 + static_cast<size_t>(Cfg<kMode>::STAGES) * Lay<kMode>::STAGE_BYTES + sizeof(Tail<kMode>) +
            (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0);
 }
+static_assert(smem_bytes<kModeActM>() <= 232448 && smem_bytes<kModeSwap>() <= 232448 &&
+                  smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448,
+              "shared memory per CTA (227 KB)");
 
 struct TileInfo {
     int ph, g, nb, tbg, row0, rows;
 };
 
-// tb_off[g] = sum_{g' < g} ceil(rows_g' / act_rows), g = 0..G (block-wide scan; contains barriers)
+// tb_off[g] = sum_{g' < g} ceil(rows_g' / act_rows), g = 0..G (block-wide scan; contains barriers),
+// and g_off = offsets[0..G]
 __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, int act_rows, int32_t* tb_off,
-                                  int32_t* wsum)
+                                  int32_t* g_off, int32_t* wsum)
 {
     const int nt = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = nt >> 5;
     const int per = (G + nt - 1) / nt;
@@ -170,16 +175,20 @@ __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, in
     int32_t run = x - s + (warp > 0 ? wsum[warp - 1] : 0);
     for (int g = g0; g < g1; ++g) {
         tb_off[g] = run;
-        const int32_t r = __ldg(offsets + g + 1) - __ldg(offsets + g);
+        const int32_t o0 = __ldg(offsets + g), r = __ldg(offsets + g + 1) - o0;
+        g_off[g] = o0;
         run += r > 0 ? (r + act_rows - 1) / act_rows : 0;
     }
-    if (t == nt - 1) tb_off[G] = wsum[nwarps - 1];
+    if (t == nt - 1) {
+        tb_off[G] = wsum[nwarps - 1];
+        g_off[G] = __ldg(offsets + G);
+    }
     __syncthreads();
 }
 
 // Tile L of the launch: phase-0 tiles first (token block major, weight block minor), then phase 1.
-__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmArgs& a, int act_rows, int w_rows,
-                                              int tiles0, int L)
+__device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const int32_t* g_off, const GemmArgs& a,
+                                              int act_rows, int w_rows, int tiles0, int L)
 {
     TileInfo ti;
     ti.ph = L >= tiles0 ? 1 : 0;
@@ -193,7 +202,7 @@ __device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const GemmA
         if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
     }
     ti.g = lo;
-    const int g0 = __ldg(a.offsets + lo), g1 = __ldg(a.offsets + lo + 1);
+    const int g0 = g_off[lo], g1 = g_off[lo + 1];
     ti.row0 = g0 + (ti.tbg - tb_off[lo]) * act_rows;
     ti.rows = min(act_rows, g1 - ti.row0);
     return ti;
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     // everything above overlaps the previous launch; the group offsets and activations come from it
     ptx::griddep_wait();
     ptx::griddep_launch_dependents();
-    block_tile_prefix(a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.wsum);
+    block_tile_prefix(a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.g_off, st.wsum);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -357,7 +366,11 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 if (L > total) L = total;
                 if (!tile_publish(st, tc, L)) { set_abort(st, a.status); break; }
                 if (L >= total) break;
-                const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+                // claim the next tile now: the atomic's round trip overlaps this tile's stages
+                // instead of stalling the ring between tiles (a phase-1 tile is never followed by a
+                // phase-0 claim, so no CTA holds back a tile another CTA waits for)
+                const int L_next = static_cast<int>(gridDim.x) + atomicAdd(a.tile_counter, 1);
+                const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
                 const GemmProblem& P = a.p[ti.ph];
                 const CUtensorMap* tm = ti.ph ? &tmap_w1 : &tmap_w0;
                 const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256, n_blk = P.N / 128;
@@ -377,7 +390,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     sf_src += 4 * SF_TILE;
                     if (++s == C::STAGES) { s = 0; ph ^= 1; }
                 }
-                L = static_cast<int>(gridDim.x) + atomicAdd(a.tile_counter, 1);
+                L = L_next;
             }
         }
     } else if (warp == 1) {
@@ -479,7 +492,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         for (;;) {
             const int L = tile_take(st, tc, total, false);
             if (L >= total || !ok || aborted(st)) break;
-            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+            const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
             const GemmProblem& P = a.p[ti.ph];
             const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
             const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
@@ -568,7 +581,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         for (;; ++lt) {
             const int L = tile_take(st, tc, total, false);
             if (L >= total || aborted(st)) break;
-            const TileInfo ti = tile_info(st.tb_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+            const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
             const GemmProblem& P = a.p[ti.ph];
             const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
             // the tile's scales are loaded before waiting for its accumulator, hiding their latency:
