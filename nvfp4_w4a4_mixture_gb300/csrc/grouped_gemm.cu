@@ -98,7 +98,10 @@ struct Lay {
     static constexpr int SFW_STEP_COLS = 4 * WB;               // weight scale columns per K-step
     static constexpr int STAGE_SF_COLS = 4 * (SFW_STEP_COLS + 4);
     static constexpr int TMEM_COLS = 512;
-    static constexpr int READY_PER_TILE = C::EPI_WARPS;  // epilogue warp arrivals per gate/up tile
+    // epilogue warps that take tiles: with 32-row token blocks on the MMA's M side only lane quarter
+    // 0 holds rows, so the other quarters' warps stay out (no polling, no arrivals)
+    static constexpr int EPI_ACTIVE = (!C::SWAP && C::ACT_ROWS <= 32) ? C::EPI_WARPS / 4 : C::EPI_WARPS;
+    static constexpr int READY_PER_TILE = EPI_ACTIVE;  // epilogue warp arrivals per gate/up tile
     static_assert(SF_COL + STAGE_SF_COLS * C::STAGES <= TMEM_COLS, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
@@ -321,14 +324,14 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         }
         for (int s = 0; s < C::ACC_BUFS; ++s) {
             ptx::mbar_init(&st.acc_full[s], 1);
-            ptx::mbar_init(&st.acc_empty[s], 32 * C::EPI_WARPS);
+            ptx::mbar_init(&st.acc_empty[s], 32 * LY::EPI_ACTIVE);
         }
         ptx::mbar_init(&st.drain, 1);
         ptx::mbar_init(&st.xchg_full, 64);
         ptx::mbar_init(&st.xchg_empty, 64);
         for (int i = 0; i < kTileRing; ++i) {
             ptx::mbar_init(&st.tile_full[i], 1);
-            ptx::mbar_init(&st.tile_empty[i], 2 + 1 + C::EPI_WARPS);
+            ptx::mbar_init(&st.tile_empty[i], 2 + 1 + LY::EPI_ACTIVE);
         }
         st.abort = 0;
         ptx::fence_mbar_init();
@@ -578,7 +581,8 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         const int q = warp & 3;  // TMEM lane quarter of this warp
         uint32_t lt = 0, xt = 0;
         TileCursor tc;
-        for (;; ++lt) {
+        const bool epi_active = LY::EPI_ACTIVE == C::EPI_WARPS || q == 0;
+        for (; epi_active; ++lt) {
             const int L = tile_take(st, tc, total, false);
             if (L >= total || aborted(st)) break;
             const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
