@@ -38,6 +38,14 @@ __device__ __forceinline__ uint32_t f32_to_bf16(float f)
     return u >> 16;
 }
 
+// Two floats as packed bf16 (round to nearest even; lo in bits 0..15) by one conversion instruction.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Exact value of a UE4M3 byte (code < 0x7F): e == 0 -> m * 2^-9, else 2^(e-7) * (1 + m/8).
 __device__ __forceinline__ float ue4m3_to_f32(uint32_t c)
 {

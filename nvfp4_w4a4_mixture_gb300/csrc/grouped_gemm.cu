@@ -724,8 +724,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                                     uint32_t w[8];
 #pragma unroll
                                     for (int j = 0; j < 8; ++j)
-                                        w[j] = f32_to_bf16(__uint_as_float(v[g][2 * j]) * sc) |
-                                               (f32_to_bf16(__uint_as_float(v[g][2 * j + 1]) * sc) << 16);
+                                        w[j] = pack_bf16x2(__uint_as_float(v[g][2 * j]) * sc, __uint_as_float(v[g][2 * j + 1]) * sc);
                                     uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + po * P.N + col);
                                     o[0] = make_uint4(w[0], w[1], w[2], w[3]);
                                     o[1] = make_uint4(w[4], w[5], w[6], w[7]);

@@ -280,8 +280,7 @@ __host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N)
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
 {
     uint32_t r;
-    asm volatile(
-        "{\n\t.reg .b8 t;\n\t"
+    asm("{\n\t.reg .b8 t;\n\t"
         "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
         "cvt.u32.u8 %0, t;\n\t}\n"
         : "=r"(r)
@@ -293,7 +292,7 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
 {
     uint16_t r;
-    asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(lo), "f"(hi));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(lo), "f"(hi));
     return r;
 }
 
