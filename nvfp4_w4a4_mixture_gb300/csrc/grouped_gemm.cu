@@ -55,13 +55,13 @@ template <>
 struct Cfg<kModeActM> {                    // activations on the MMA's M side, 128 weight rows on N
     static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false;
+    static constexpr bool SWAP = false, XCHG = false;
 };
 template <>
 struct Cfg<kModeSwap> {                    // weights on the MMA's M side, 32 activation rows on N
     static constexpr int ACT_ROWS = 32, W_ROWS = 128, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 32;
-    static constexpr bool SWAP = true;
+    static constexpr bool SWAP = true, XCHG = false;
 };
 template <>
 struct Cfg<kModeWide> {                    // activations on M, 256 weight rows on N: half the MMAs and
@@ -69,16 +69,18 @@ struct Cfg<kModeWide> {                    // activations on M, 256 weight rows 
     // one buffer only, so the epilogue frees it as soon as its rows are in registers
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false;
+    static constexpr bool SWAP = false, XCHG = false;
 };
 
 template <>
 struct Cfg<kModeWideNarrow> {              // wide, for token blocks of at most 32 rows (decode): the
     // activation region holds 32 rows, the MMA's other 96 A rows read the weight region behind it
-    // (their accumulator rows are never stored); the freed shared memory buys a fifth stage
-    static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 5, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
+    // (their accumulator rows are never stored). Only lane quarter 0 of the accumulator holds rows,
+    // so its two warps copy the accumulator to shared memory (XCHG) and all eight epilogue warps
+    // finish it; four stages keep the ring as fast as five did
+    static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false;
+    static constexpr bool SWAP = false, XCHG = true;
 };
 
 template <int kMode>
@@ -99,8 +101,12 @@ struct Lay {
     static constexpr int STAGE_SF_COLS = 4 * (SFW_STEP_COLS + 4);
     static constexpr int TMEM_COLS = 512;
     // epilogue warps that take tiles: with 32-row token blocks on the MMA's M side only lane quarter
-    // 0 holds rows, so the other quarters' warps stay out (no polling, no arrivals)
-    static constexpr int EPI_ACTIVE = (!C::SWAP && C::ACT_ROWS <= 32) ? C::EPI_WARPS / 4 : C::EPI_WARPS;
+    // 0 holds rows, so unless they share the work through shared memory (XCHG) the other quarters'
+    // warps stay out (no polling, no arrivals)
+    static constexpr int EPI_ACTIVE =
+        (!C::SWAP && !C::XCHG && C::ACT_ROWS <= 32) ? C::EPI_WARPS / 4 : C::EPI_WARPS;
+    // arrivals that free the accumulator: the warps that read it
+    static constexpr int ACC_READERS = C::XCHG ? C::EPI_WARPS / 4 : EPI_ACTIVE;
     static constexpr int READY_PER_TILE = EPI_ACTIVE;  // epilogue warp arrivals per gate/up tile
     static_assert(SF_COL + STAGE_SF_COLS * C::STAGES <= TMEM_COLS, "tensor memory budget");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
@@ -130,11 +136,17 @@ struct SwapXchg {
     float u[64][33];
 };
 
+// a 32-row tile's accumulator in shared memory (XCHG epilogue); rows padded to 260 words so a
+// warp's 16-byte accesses to 32 rows at one column hit distinct banks in each 8-lane phase
+struct AccXchg {
+    float v[32][260];
+};
+
 template <int kMode>
 constexpr size_t smem_bytes()
 {
     return 1024 + static_cast<size_t>(Cfg<kMode>::STAGES) * Lay<kMode>::STAGE_BYTES + sizeof(Tail<kMode>) +
-           (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0);
+           (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0) + (Cfg<kMode>::XCHG ? sizeof(AccXchg) : 0);
 }
 static_assert(smem_bytes<kModeActM>() <= 232448 && smem_bytes<kModeSwap>() <= 232448 &&
                   smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448,
@@ -276,6 +288,24 @@ __device__ __forceinline__ bool spin_until(const int32_t* p, int target)
 
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
+// Barriers of the epilogue warps alone (named barriers 1 and 2, 32 * n threads): the first also
+// returns whether any of them passed true.
+__device__ __forceinline__ bool epi_bar_any(bool pred, int n)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(32 * n)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void epi_bar(int n) { asm volatile("bar.sync 2, %0;" ::"r"(32 * n) : "memory"); }
+
 // NVFP4 encoding of the intermediate h (16 values, static tensor scale S): the same rule as the
 // activation quantizer, with the two divisions replaced by multiplications with correctly rounded
 // reciprocals (the requantised intermediate is compared by agreement rate, not bit for bit).
@@ -324,7 +354,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         }
         for (int s = 0; s < C::ACC_BUFS; ++s) {
             ptx::mbar_init(&st.acc_full[s], 1);
-            ptx::mbar_init(&st.acc_empty[s], 32 * LY::EPI_ACTIVE);
+            ptx::mbar_init(&st.acc_empty[s], 32 * LY::ACC_READERS);
         }
         ptx::mbar_init(&st.drain, 1);
         ptx::mbar_init(&st.xchg_full, 64);
@@ -575,6 +605,148 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         }
         // publish the stages still in flight
         publish_all();
+    } else if constexpr (C::XCHG) {
+        // ================================ epilogue through shared memory (32-row token blocks)
+        // The two warps of lane quarter 0 copy the tile's accumulator (rows 0..31) to shared memory
+        // and free it; then every epilogue warp finishes a slice of it: h block ew of the SwiGLU
+        // (16 gate and 16 up columns), or 32 output columns. The per-tile loop of the epilogue
+        // warps is kept in step by two barriers; the first also ends it for all of them at once.
+        static_assert(!kSwap && C::ACT_ROWS == 32 && W_ROWS == 256 && C::EPI_WARPS == 8, "XCHG epilogue shape");
+        AccXchg& xb = *reinterpret_cast<AccXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kMode>));
+        const int ew = warp - 4;
+        const int q = warp & 3;
+        uint32_t lt = 0;
+        TileCursor tc;
+        for (;; ++lt) {
+            const int L = tile_take(st, tc, total, false);
+            const bool have = L < total && !aborted(st);
+            TileInfo ti{};
+            if (have) ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+            const GemmProblem& P = a.p[ti.ph];
+            const int r = lane;  // the tile row of this lane in every slice
+            const int64_t p = ti.row0 + r;
+            const bool valid = have && r < ti.rows;
+            float sa = 1.0f, sb0 = 1.0f, sb1 = 1.0f, S_h = 1.0f;
+            int64_t po = p;
+            if (have) {
+                sa = __ldg(P.a_scale + (P.a_scale_per_group ? ti.g : 0));
+                sb0 = __ldg(P.b_scale + (P.gate_up ? 2 * ti.g : ti.g));
+                sb1 = P.gate_up ? __ldg(P.b_scale + 2 * ti.g + 1) : sb0;
+                S_h = P.epilogue == kEpiSwiGLU ? __ldg(P.epi_scale + ti.g) : 1.0f;
+                if (P.out_row && valid && p < P.out_row_n) po = __ldg(P.out_row + p);
+            }
+            bool ok = true;
+            if (have && q == 0) {
+                const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
+                const bool got = ptx::mbar_wait(&st.acc_full[as], aph);
+                __syncwarp();
+                ok = __all_sync(0xFFFFFFFFu, got);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    const int half = ew >> 2;  // warps 4 and 8: accumulator columns half*128 .. +127
+                    const uint32_t tbase = tmem + as * C::ACC_COLS + half * 128;
+#pragma unroll
+                    for (int rd = 0; rd < 2; ++rd) {
+                        uint32_t v[4][16];
+#pragma unroll
+                        for (int g = 0; g < 4; ++g) ptx::tmem_ld16(tbase + rd * 64 + g * 16, v[g]);
+                        ptx::tmem_ld_wait();
+                        if (rd == 1) {
+                            ptx::tc_fence_before();
+                            ptx::mbar_arrive(&st.acc_empty[as]);
+                        }
+                        float4* row = reinterpret_cast<float4*>(&xb.v[lane][half * 128 + rd * 64]);
+#pragma unroll
+                        for (int g = 0; g < 4; ++g)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                row[g * 4 + j] = make_float4(__uint_as_float(v[g][4 * j]), __uint_as_float(v[g][4 * j + 1]),
+                                                             __uint_as_float(v[g][4 * j + 2]), __uint_as_float(v[g][4 * j + 3]));
+                    }
+                } else {
+                    set_abort(st, a.status);
+                }
+            }
+            if (epi_bar_any(!have || !ok, C::EPI_WARPS)) break;  // the copy is complete (or all stop)
+            const float* xr = xb.v[r];
+            if (P.epilogue == kEpiSwiGLU) {
+                const int I = P.N / 2;
+                const int beta = ew;                                 // h block of the tile
+                const int gc = (beta >> 2) * 128 + (beta & 3) * 16;  // its gate columns; up at + 64
+                const float sg = sa * sb0, su = sa * sb1;
+                const float S = S_h;
+                const float inv_six_s = 1.0f / (6.0f * S);
+                float h[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float4 g4 = reinterpret_cast<const float4*>(xr + gc)[j];
+                    const float4 u4 = reinterpret_cast<const float4*>(xr + gc + 64)[j];
+                    h[4 * j] = silu(g4.x * sg) * (u4.x * su);
+                    h[4 * j + 1] = silu(g4.y * sg) * (u4.y * su);
+                    h[4 * j + 2] = silu(g4.z * sg) * (u4.z * su);
+                    h[4 * j + 3] = silu(g4.w * sg) * (u4.w * su);
+                }
+                uint32_t lo, hi;
+                const uint32_t sf = encode16_rcp(h, S, inv_six_s, lo, hi);
+                if (valid) {
+                    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(P.out) + p * (I / 2) + ti.nb * (W_ROWS / 4) + beta * 8) =
+                        make_uint2(lo, hi);
+                    if (P.out_sf_tiled)
+                        P.out_sf[(static_cast<int64_t>(ti.tbg) * (I / 64) + ti.nb * LY::WB + (beta >> 2)) * SF_TILE + r * 16 +
+                                 (beta & 3)] = static_cast<uint8_t>(sf);
+                    else
+                        P.out_sf[p * (I / 16) + ti.nb * (W_ROWS / 32) + beta] = static_cast<uint8_t>(sf);
+                }
+            } else {
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int c0 = ew * 32 + g * 16;  // tile column
+                    int col;
+                    float sb;
+                    if (P.gate_up) {
+                        const int cc = c0 & 127, upper = cc >= 64;
+                        col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
+                        sb = upper ? sb1 : sb0;
+                    } else {
+                        col = ti.nb * W_ROWS + c0;
+                        sb = sb0;
+                    }
+                    const float sc = sa * sb;
+                    float x[16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float4 v4 = reinterpret_cast<const float4*>(xr + c0)[j];
+                        x[4 * j] = v4.x * sc;
+                        x[4 * j + 1] = v4.y * sc;
+                        x[4 * j + 2] = v4.z * sc;
+                        x[4 * j + 3] = v4.w * sc;
+                    }
+                    if (valid) {
+                        if (P.epilogue == kEpiF32) {
+                            float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + po * P.N + col);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) o[j] = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                        } else {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) w[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+                            uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + po * P.N + col);
+                            o[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                    }
+                }
+            }
+            if (a.nphase > 1 && ti.ph == 0) {
+                // publish this warp's part of h (see the other epilogue)
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    atomicAdd(a.ready + ti.tbg, 1);
+                }
+            }
+            epi_bar(C::EPI_WARPS);  // every slice read: the next tile may overwrite the copy
+        }
     } else {
         // ================================ epilogue
         const int ew = warp - 4;
