@@ -164,11 +164,13 @@ CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
 
 bool pdl_enabled()
 {
-    // Off unless MOE_NVFP4_PDL=1: in a CUDA graph replay of the decode layer the programmatic
-    // launches measured about 5 us slower per step than plain stream order.
+    // On unless MOE_NVFP4_PDL=0. Each CTA of the front half and of the expert GEMMs allows the next
+    // launch only when its own work is done, so the next kernel's launch and prologue overlap the
+    // previous one's tail (triggered at the start instead, the early CTAs of the next launch held
+    // SMs and a decode step was 4-5 us slower than plain stream order).
     static const bool on = [] {
         const char* v = std::getenv("MOE_NVFP4_PDL");
-        return v && v[0] == '1';
+        return !(v && v[0] == '0');
     }();
     return on;
 }

@@ -80,7 +80,6 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     uint4 wv0[8];
     router_row_prefetch(wr, H, has_row, wv0);
     ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
 
     // ---- logits of this CTA's router rows, kTT tokens per pass; every CTA sees all of x, so it
     // also takes the tensor max on the way
@@ -131,7 +130,10 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     const int64_t b0 = min(nblocks, static_cast<int64_t>(arrival) * per), b1 = min(nblocks, b0 + per);
     const uint16_t* xq = T <= kTT ? xs : a.x;  // a single pass left every token staged
     quantize_blocks(xq, b0, b1, S, tid, kFrontThreads, a.xq_codes, a.xq_sf);
-    if (arrival != gridDim.x - 1) return;
+    if (arrival != gridDim.x - 1) {
+        ptx::griddep_launch_dependents();  // this CTA's outputs are written
+        return;
+    }
 
     // ---- last CTA: one warp per token (top-k), then the permutation
     for (int t = warp; t < T; t += kFrontWarps) {
@@ -157,6 +159,7 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     block_small_permute<kFrontThreads>(ids_s, n, k, T, E, sorted_s, a.offsets, a.perm_src, a.src_perm, a.row_token);
     for (int i = tid; i < a.n_ready; i += kFrontThreads) a.ready[i] = 0;
     if (tid == 0) *a.ticket = 0u;  // every CTA has taken its ticket: ready for the next call
+    ptx::griddep_launch_dependents();
 }
 
 bool front_fits(int T, int H, int E, int k)

@@ -374,7 +374,6 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     }
     // everything above overlaps the previous launch; the group offsets and activations come from it
     ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
     block_tile_prefix(a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.g_off, st.wsum);
     ptx::tc_fence_before();
     __syncthreads();
@@ -1010,6 +1009,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         __syncwarp();
         ptx::tmem_dealloc(tmem, LY::TMEM_COLS);
     }
+    ptx::griddep_launch_dependents();  // the next launch may start its prologue on this SM
 }
 
 int gemm_act_rows(bool weights_on_m) { return weights_on_m ? Cfg<kModeSwap>::ACT_ROWS : Cfg<kModeActM>::ACT_ROWS; }
