@@ -211,6 +211,23 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
                                         void* const* events, int n_events);
 
 /* ---------------------------------------------------------------------------------------------
+ * moe_layer_forward_host -- moe_layer_forward for a caller whose tokens live in HOST memory: the
+ *   call enqueues on `stream` the copy of x (and residual) into device staging inside the
+ *   workspace, the whole layer, and the copy of the result back to `out`.
+ *   x: host bf16 [T][H]; residual: nullable host bf16 [T][H]; out: host bf16 [T][H], must not
+ *   overlap x or residual. Page-locked host memory (cudaHostAlloc / cudaHostRegister) keeps the
+ *   call asynchronous; pageable memory also works, with the copies then behaving as
+ *   cudaMemcpyAsync does for pageable memory (staged, partly synchronous). The call returns once
+ *   everything is enqueued: `out` holds the result when `stream` has passed this point (for
+ *   example after cudaStreamSynchronize), and x / residual must stay unchanged until then.
+ *   A device pointer for x, residual or out returns MOE_ERR_INVALID_ARG.
+ *   ws: >= moe_workspace_bytes_host(H, E, k, I, T) (the layer's workspace followed by three
+ *   256-byte-aligned staging buffers of T*H bf16).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
+                                    uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
  * moe_route_topk_noalloc -- moe_route_topk for callers that cannot give the library scratch
  *   memory: an application whose device memory is owned by another allocator and may not grow
  *   by extra cudaMalloc calls, or a decode loop that cannot afford cudaMalloc's implicit device
@@ -229,6 +246,9 @@ moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const moe_layer_t*
 
 /* Workspace bytes for any call above with these sizes (T tokens). */
 size_t moe_workspace_bytes(int H, int E, int k, int I, int T);
+
+/* Workspace bytes for moe_layer_forward_host with these sizes (T tokens). */
+size_t moe_workspace_bytes_host(int H, int E, int k, int I, int T);
 
 /* Synchronise `stream`, read and clear the device status word of `ws`: MOE_OK or
  * MOE_ERR_DEVICE_TIMEOUT. */

@@ -19,6 +19,7 @@ ENTRY_POINTS = (
     "moe_quantize_nvfp4", "moe_quantize_nvfp4_f32", "moe_route_topk", "moe_permute", "moe_prepack_nvfp4",
     "moe_grouped_gemm_nvfp4", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled", "moe_workspace_bytes",
     "moe_read_device_status", "moe_status_string", "moe_last_error_detail", "moe_route_topk_noalloc",
+    "moe_layer_forward_host", "moe_workspace_bytes_host",
 )
 
 
@@ -55,6 +56,8 @@ def lib():
         L.moe_last_error_detail.argtypes = []
         L.moe_workspace_bytes.restype = sz
         L.moe_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+        L.moe_workspace_bytes_host.restype = sz
+        L.moe_workspace_bytes_host.argtypes = [i32, i32, i32, i32, i32]
         L.moe_read_device_status.restype = i32
         L.moe_read_device_status.argtypes = [vp, vp]
         for name in ("moe_quantize_nvfp4", "moe_quantize_nvfp4_f32"):
@@ -76,6 +79,8 @@ def lib():
         L.moe_combine.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.moe_layer_forward.restype = i32
         L.moe_layer_forward.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp]
+        L.moe_layer_forward_host.restype = i32
+        L.moe_layer_forward_host.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp]
         L.moe_layer_forward_profiled.restype = i32
         L.moe_layer_forward_profiled.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp,
                                                  ctypes.POINTER(vp), i32]
@@ -99,6 +104,10 @@ def _stream():
 
 def moe_workspace_bytes(H, E, k, I, T):
     return int(lib().moe_workspace_bytes(H, E, k, I, T))
+
+
+def moe_workspace_bytes_host(H, E, k, I, T):
+    return int(lib().moe_workspace_bytes_host(H, E, k, I, T))
 
 
 class Workspace:
@@ -267,6 +276,21 @@ def moe_layer_forward(layer, x, residual=None, out=None, ws=None):
     ws = ws or _ws(layer.workspace_bytes(T))
     _check(lib().moe_layer_forward(ctypes.byref(layer.desc), _p(_bf16_bits(x)), T, _p(residual), _p(out), ws.ptr,
                                    ws.nbytes, _stream()))
+    return out
+
+
+def moe_layer_forward_host(layer, x, residual=None, out=None, ws=None):
+    """The layer on host tensors (bf16 [T][H] on the CPU; page-locked keeps the call asynchronous):
+    the copies in and out and the layer are enqueued on the current stream. `out` holds the result
+    once that stream has passed this call."""
+    T = x.shape[0]
+    for t in (x, residual, out):
+        assert t is None or (t.dtype == torch.bfloat16 and not t.is_cuda and t.is_contiguous())
+    if out is None:
+        out = torch.empty(T, layer.H, dtype=torch.bfloat16).pin_memory()
+    ws = ws or _ws(moe_workspace_bytes_host(layer.H, layer.E, layer.k, layer.I, T))
+    _check(lib().moe_layer_forward_host(ctypes.byref(layer.desc), _p(x), T, _p(residual), _p(out), ws.ptr, ws.nbytes,
+                                        _stream()))
     return out
 
 

@@ -93,6 +93,9 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     return L;
 }
 
+// one device staging buffer of moe_layer_forward_host: T x H bf16, 256-byte aligned
+size_t host_stage_bytes(int64_t H, int64_t T) { return (static_cast<size_t>(T * H * 2) + 255) & ~size_t(255); }
+
 moe_status_t check_layer_shape(int H, int E, int k, int I)
 {
     if (H < 128 || H > 8192 || H % 128) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "H=%d not a multiple of 128 in [128, 8192]", H);
@@ -216,6 +219,12 @@ size_t moe_workspace_bytes(int H, int E, int k, int I, int T)
 {
     if (H < 0 || E < 0 || k < 0 || I < 0 || T < 0) return 0;
     return ws_layout(H, E, k, I, T).total;
+}
+
+size_t moe_workspace_bytes_host(int H, int E, int k, int I, int T)
+{
+    if (H < 0 || E < 0 || k < 0 || I < 0 || T < 0) return 0;
+    return ws_layout(H, E, k, I, T).total + 3 * host_stage_bytes(H, T);
 }
 
 moe_status_t moe_read_device_status(void* ws, moe_stream_t stream)
@@ -531,6 +540,47 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
                                void* ws, size_t ws_bytes, moe_stream_t stream)
 {
     return moe_layer_forward_profiled(L, x, T, residual, out, ws, ws_bytes, stream, nullptr, 0);
+}
+
+moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
+                                    uint16_t* out, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
+    MOE_TRY(check_layer_shape(L->H, L->E, L->k, L->I));
+    if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
+    const size_t bytes = static_cast<size_t>(T) * L->H * 2;
+    const char *xb = reinterpret_cast<const char*>(x), *ob = reinterpret_cast<const char*>(out);
+    const char* rb = reinterpret_cast<const char*>(residual);
+    if (bytes && ((ob < xb + bytes && xb < ob + bytes) || (rb && ob < rb + bytes && rb < ob + bytes)))
+        return fail(MOE_ERR_INVALID_ARG, "out overlaps x or residual");
+    const WsLayout W = ws_layout(L->H, L->E, L->k, L->I, T);
+    const size_t stage = host_stage_bytes(L->H, T);
+    MOE_TRY(check_ws(ws, ws_bytes, W.total + 3 * stage));
+    MOE_TRY(check_device());
+    const void* host_ptrs[3] = {x, residual, out};
+    const char* names[3] = {"x", "residual", "out"};
+    for (int i = 0; i < 3; ++i) {
+        if (!host_ptrs[i]) continue;
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, host_ptrs[i]) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(MOE_ERR_INVALID_ARG, "%s: not a valid pointer", names[i]);
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+            return fail(MOE_ERR_INVALID_ARG, "%s is device memory; moe_layer_forward_host takes host buffers", names[i]);
+    }
+    if (T == 0) return MOE_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* base = static_cast<char*>(ws);
+    uint16_t* xd = reinterpret_cast<uint16_t*>(base + W.total);
+    uint16_t* od = reinterpret_cast<uint16_t*>(base + W.total + stage);
+    uint16_t* rd = residual ? reinterpret_cast<uint16_t*>(base + W.total + 2 * stage) : nullptr;
+    MOE_CUDA(cudaMemcpyAsync(xd, x, bytes, cudaMemcpyHostToDevice, s), "copy x to the device");
+    if (rd) MOE_CUDA(cudaMemcpyAsync(rd, residual, bytes, cudaMemcpyHostToDevice, s), "copy residual to the device");
+    MOE_TRY(moe_layer_forward_profiled(L, xd, T, rd, od, ws, W.total, stream, nullptr, 0));
+    MOE_CUDA(cudaMemcpyAsync(out, od, bytes, cudaMemcpyDeviceToHost, s), "copy the result to the host");
+    return MOE_OK;
 }
 
 }  // extern "C"

@@ -5,6 +5,8 @@ permutation indices; the gate/up GEMM (FP32 out) within 1e-5 relative Frobenius 
 per expert); the layer output within 2e-2 relative Frobenius error; >= 99.9 % of the requantized
 intermediate codes identical; routing weights within 1e-6.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -477,6 +479,39 @@ def test_layer_repeat_bit_identical(moe):
     moe.moe_read_device_status(ws=ws)
     for o in outs[1:]:
         assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+
+
+@pytest.mark.parametrize("name,residual", [("decode", False), ("tiny", True)])
+def test_layer_host_buffers_match_device_call(moe, name, residual):
+    # moe_layer_forward_host (host tensors in and out, copies enqueued by the library) gives the
+    # same bits as moe_layer_forward on device copies of the same tensors
+    case = I_.layer_case(name, seed=9, sample=4) if name == "decode" else I_.layer_case(name, seed=9)
+    layer = gpu_layer(moe, case)
+    x = bf16_dev(case["x"])
+    res = bf16_dev(case["x"][::-1].copy()) if residual else None
+    ref = moe.moe_layer_forward(layer, x, residual=res)
+    x_h = x.cpu().pin_memory()
+    res_h = res.cpu().pin_memory() if residual else None
+    out_h = moe.moe_layer_forward_host(layer, x_h, residual=res_h)
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out_h.view(torch.int16), ref.cpu().view(torch.int16))
+    # pageable host memory works too
+    out_p = moe.moe_layer_forward_host(layer, x.cpu(), residual=res.cpu() if residual else None,
+                                       out=torch.empty(out_h.shape, dtype=torch.bfloat16))
+    torch.cuda.current_stream().synchronize()
+    assert torch.equal(out_p.view(torch.int16), ref.cpu().view(torch.int16))
+
+
+def test_layer_host_rejects_device_pointers(moe):
+    case = I_.layer_case("tiny", seed=2)
+    layer = gpu_layer(moe, case)
+    x = bf16_dev(case["x"])
+    ws = moe.Workspace(moe.moe_workspace_bytes_host(case["H"], case["E"], case["k"], case["I"], case["T"]))
+    out_h = torch.empty(case["T"], case["H"], dtype=torch.bfloat16)
+    L = moe.lib()
+    st = L.moe_layer_forward_host(ctypes.byref(layer.desc), ctypes.c_void_p(x.data_ptr()), case["T"], None,
+                                  ctypes.c_void_p(out_h.data_ptr()), ws.ptr, ws.nbytes, moe._stream())
+    assert st != 0 and "device memory" in L.moe_last_error_detail().decode()
 
 
 def test_device_status_clean(moe):
