@@ -469,6 +469,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 };
                 for (int kt = 0; kt < k_stages; ++kt) {
                     if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
+                    ptx::fence_proxy_async_smem();  // the activation rows came by cp.async (generic proxy)
                     const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
                     const uint32_t tsfw = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS, tsfact = tsfw + 4 * LY::SFW_STEP_COLS;
                     const int nk = min(4, kb64 - kt * 4);
@@ -497,29 +498,18 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         constexpr int RW = C::ACT_ROWS / 2;      // rows per producer warp
         constexpr int NCR = RW / 4;              // code rows per lane (4 rows per warp instruction)
         constexpr int NSR = RW / 8;              // scale rows per lane (8 rows per warp instruction)
-        // stages whose copies may still be in flight when a newer one is issued: stage i is published
-        // once stage i + LAG is issued and stage i's copies have landed. A deeper lag lets the
-        // copies of more stages overlap but holds each stage back until LAG more slots are free,
-        // i.e. until the MMA has consumed stage i + LAG - STAGES (decode: 2 us slower at 3 than at 1).
-        constexpr int LAG = 1;
+        // Each thread arrives on a stage's full barrier through cp.async.mbarrier.arrive: the arrival
+        // lands when the thread's copies have, so the warp goes straight on to the next free stage
+        // and as many stages' gathers are in flight as the ring has free slots. (The MMA thread
+        // fences the generic-proxy writes of the copies against its tensor-core reads.)
         const int w2 = warp - 2, pt = tid - 64;
         const int chunk = lane & 7, word = lane & 3;
         const uint8_t* cptr[NCR];
         const uint8_t* sptr[NSR];
         uint32_t cvalid = 0, svalid = 0;
-        int s = 0, pub = 0;
-        uint32_t ph = 0, issued = 0, published = 0;
+        int s = 0;
+        uint32_t ph = 0;
         bool ok = true;
-        // publish (arrive on the full barrier of) every stage whose copies are issued: needed before
-        // any wait on other CTAs, which may be waiting for the tile those stages complete
-        auto publish_all = [&]() {
-            ptx::cp_async_wait<0>();
-            ptx::fence_proxy_async_smem();
-            for (; published < issued; ++published) {
-                ptx::mbar_arrive(&st.full[pub]);
-                if (++pub == C::STAGES) pub = 0;
-            }
-        };
         TileCursor tc;
         for (;;) {
             const int L = tile_take(st, tc, total, false);
@@ -530,7 +520,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
             if (ti.ph == 1) {
                 // the down GEMM reads h: wait until every gate/up tile of this token block stored it
-                publish_all();
+                // (the stages already issued complete on their own meanwhile)
                 const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS);
                 if (!spin_until(a.ready + ti.tbg, target)) { set_abort(st, a.status); break; }
             }
@@ -589,21 +579,11 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : P.a_sf, v);
                     }
                 }
-                ptx::cp_async_commit();
-                ++issued;
-                ptx::cp_async_wait<LAG>();
-                if (issued > published + LAG) {
-                    ptx::fence_proxy_async_smem();
-                    for (; published + LAG < issued; ++published) {
-                        ptx::mbar_arrive(&st.full[pub]);
-                        if (++pub == C::STAGES) pub = 0;
-                    }
-                }
+                ptx::cp_async_arrive_noinc(&st.full[s]);
                 if (++s == C::STAGES) { s = 0; ph ^= 1; }
             }
         }
-        // publish the stages still in flight
-        publish_all();
+        ptx::cp_async_wait<0>();  // no copy outlives the role
     } else if constexpr (C::XCHG) {
         // ================================ epilogue through shared memory (32-row token blocks)
         // The two warps of lane quarter 0 copy the tile's accumulator (rows 0..31) to shared memory

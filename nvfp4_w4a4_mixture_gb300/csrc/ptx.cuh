@@ -146,6 +146,13 @@ __device__ __forceinline__ void cp_async_wait()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Arrive once on bar (counted as one of its expected arrivals) when every cp.async this thread has
+// issued so far has landed in shared memory; the thread itself does not wait.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Make generic-proxy writes to shared memory visible to the async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
