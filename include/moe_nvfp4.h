@@ -90,8 +90,11 @@ enum {
      * to FP32 summation order. */
     MOE_GEMM_SCHED_ACT_ON_M = 0x100,     /* 128 token rows x 128 weight rows per tile */
     MOE_GEMM_SCHED_WEIGHTS_ON_M = 0x200, /* 128 weight rows x 32 token rows per tile (small groups) */
-    MOE_GEMM_SCHED_WIDE = 0x400          /* 128 token rows x 256 weight rows per tile (N % 256 == 0,
+    MOE_GEMM_SCHED_WIDE = 0x400,         /* 128 token rows x 256 weight rows per tile (N % 256 == 0,
                                           * else activations on M) */
+    MOE_GEMM_SCHED_WIDE_ROWS = 0x800     /* wide tiles, each CTA taking a whole 128-row token block
+                                          * through every weight block (the activation scales stay
+                                          * in tensor memory); K <= 2048, else wide */
 };
 
 /* ---------------------------------------------------------------------------------------------

@@ -354,12 +354,14 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     if (N < 128 || N % 128 || K < 64 || K % 64 || K > 16384)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d: N must be a multiple of 128, K of 64 (<= 16384)", N, K);
     if (p_max < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "p_max=%lld < 0", (long long)p_max);
-    constexpr int kSchedBits = MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M | MOE_GEMM_SCHED_WIDE;
+    constexpr int kSchedBits =
+        MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M | MOE_GEMM_SCHED_WIDE | MOE_GEMM_SCHED_WIDE_ROWS;
     const int sched_bits = epilogue & kSchedBits;
     if (sched_bits & (sched_bits - 1)) return fail(MOE_ERR_INVALID_ARG, "epilogue=0x%x: pick one schedule flag", epilogue);
     const int schedule = sched_bits == MOE_GEMM_SCHED_ACT_ON_M      ? kSchedActOnM
                          : sched_bits == MOE_GEMM_SCHED_WEIGHTS_ON_M ? kSchedWeightsOnM
                          : sched_bits == MOE_GEMM_SCHED_WIDE         ? kSchedWide
+                         : sched_bits == MOE_GEMM_SCHED_WIDE_ROWS    ? kSchedWideRows
                                                                      : kSchedAuto;
     epilogue &= ~kSchedBits;
     if (epilogue < MOE_EPI_F32 || epilogue > MOE_EPI_SWIGLU_NVFP4) return fail(MOE_ERR_INVALID_ARG, "epilogue=%d", epilogue);
@@ -522,7 +524,8 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     // 256-row weight tiles when H allows (half the MMAs and scale copies per weight byte); else
     // weights on the MMA's M side for few rows per expert (decode), 128 x 128 tiles otherwise
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
-    const int sched = gemm_wide_fits(ga) ? (T <= 32 ? kSchedWideNarrow : kSchedWide)
+    // (token-block units once there are enough of them to keep every SM busy to the end)
+    const int sched = gemm_wide_fits(ga) ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
                                          : small ? kSchedWeightsOnM : kSchedActOnM;
     if (!one_launch_front)  // (the one-launch front half clears them itself)
         MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");

@@ -48,20 +48,20 @@ constexpr int kTileRing = 8;               // tiles handed from the weight produ
 
 // Tile shapes. W_ROWS weight rows (one TMA box) by ACT_ROWS activation rows per tile; ACC_BUFS
 // accumulators of ACC_COLS tensor-memory columns.
-enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3 };
+enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3, kModeWideRows = 4 };
 template <int kMode>
 struct Cfg;
 template <>
 struct Cfg<kModeActM> {                    // activations on the MMA's M side, 128 weight rows on N
     static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false, XCHG = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false;
 };
 template <>
 struct Cfg<kModeSwap> {                    // weights on the MMA's M side, 32 activation rows on N
     static constexpr int ACT_ROWS = 32, W_ROWS = 128, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 32;
-    static constexpr bool SWAP = true, XCHG = false;
+    static constexpr bool SWAP = true, XCHG = false, ROWS = false;
 };
 template <>
 struct Cfg<kModeWide> {                    // activations on M, 256 weight rows on N: half the MMAs and
@@ -69,7 +69,7 @@ struct Cfg<kModeWide> {                    // activations on M, 256 weight rows 
     // one buffer only, so the epilogue frees it as soon as its rows are in registers
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false;
 };
 
 template <>
@@ -80,7 +80,17 @@ struct Cfg<kModeWideNarrow> {              // wide, for token blocks of at most 
     // finish it; four stages keep the ring as fast as five did
     static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = true;
+    static constexpr bool SWAP = false, XCHG = true, ROWS = false;
+};
+template <>
+struct Cfg<kModeWideRows> {                // wide tiles taken a whole token block at a time: one CTA runs
+                                           // every weight block of the token block in turn, and the
+                                           // activation scales of the whole K stay in tensor memory
+                                           // after the first (two scale copies per K-step, not three)
+    static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
+    static constexpr int MMA_M = 128, MMA_N = 256;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = true;
+    static constexpr int MAX_K = 2048;     // resident activation scales: 4 columns per 64 of K
 };
 
 template <int kMode>
@@ -98,8 +108,11 @@ struct Lay {
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
     static constexpr int SF_COL = C::ACC_BUFS * C::ACC_COLS;  // first scale-factor column
     static constexpr int SFW_STEP_COLS = 4 * WB;               // weight scale columns per K-step
-    static constexpr int STAGE_SF_COLS = 4 * (SFW_STEP_COLS + 4);
+    // per stage: 4 K-steps of weight scales, and of activation scales unless they are resident
+    static constexpr int STAGE_SF_COLS = 4 * (SFW_STEP_COLS + (C::ROWS ? 0 : 4));
     static constexpr int TMEM_COLS = 512;
+    // token-block units (ROWS): the activation scales of the whole K, 4 columns per K-step
+    static constexpr int SFA_COL = SF_COL + STAGE_SF_COLS * C::STAGES;
     // epilogue warps that take tiles: with 32-row token blocks on the MMA's M side only lane quarter
     // 0 holds rows, so unless they share the work through shared memory (XCHG) the other quarters'
     // warps stay out (no polling, no arrivals)
@@ -109,6 +122,7 @@ struct Lay {
     static constexpr int ACC_READERS = C::XCHG ? C::EPI_WARPS / 4 : EPI_ACTIVE;
     static constexpr int READY_PER_TILE = EPI_ACTIVE;  // epilogue warp arrivals per gate/up tile
     static_assert(SF_COL + STAGE_SF_COLS * C::STAGES <= TMEM_COLS, "tensor memory budget");
+    static_assert(!C::ROWS || SFA_COL + 4 * (Cfg<kModeWideRows>::MAX_K / 64) <= TMEM_COLS, "resident scales");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
 
@@ -149,7 +163,8 @@ constexpr size_t smem_bytes()
            (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0) + (Cfg<kMode>::XCHG ? sizeof(AccXchg) : 0);
 }
 static_assert(smem_bytes<kModeActM>() <= 232448 && smem_bytes<kModeSwap>() <= 232448 &&
-                  smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448,
+                  smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448 &&
+                  smem_bytes<kModeWideRows>() <= 232448,
               "shared memory per CTA (227 KB)");
 
 struct TileInfo {
@@ -212,6 +227,27 @@ __device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const int32
     ti.tbg = Lp / n_wb;
     ti.nb = Lp - ti.tbg * n_wb;
     int lo = 0, hi = a.G;  // tb_off[lo] <= tbg < tb_off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
+    }
+    ti.g = lo;
+    const int g0 = g_off[lo], g1 = g_off[lo + 1];
+    ti.row0 = g0 + (ti.tbg - tb_off[lo]) * act_rows;
+    ti.rows = min(act_rows, g1 - ti.row0);
+    return ti;
+}
+
+// Work unit L of a launch with token-block units (ROWS): phase-0 token blocks first, then phase 1;
+// nb is left 0 (the unit covers every weight block).
+__device__ __forceinline__ TileInfo unit_info(const int32_t* tb_off, const int32_t* g_off, const GemmArgs& a,
+                                              int act_rows, int units0, int L)
+{
+    TileInfo ti;
+    ti.ph = L >= units0 ? 1 : 0;
+    ti.tbg = L - (ti.ph ? units0 : 0);
+    ti.nb = 0;
+    int lo = 0, hi = a.G;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
@@ -381,8 +417,16 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     const uint32_t tmem = st.tmem_base;
 
     const int nblk = st.tb_off[a.G];
-    const int tiles0 = nblk * (a.p[0].N / W_ROWS);
-    const int total = tiles0 + (a.nphase > 1 ? nblk * (a.p[1].N / W_ROWS) : 0);
+    // the launch's work items: tiles (token block x weight block), or with ROWS whole token blocks
+    // ("units"), each taken through every weight block of its phase
+    const int tiles0 = C::ROWS ? nblk : nblk * (a.p[0].N / W_ROWS);
+    const int total = tiles0 + (a.nphase > 1 ? (C::ROWS ? nblk : nblk * (a.p[1].N / W_ROWS)) : 0);
+    auto tile_at = [&](int L) -> TileInfo {
+        if constexpr (C::ROWS) return unit_info(st.tb_off, st.g_off, a, C::ACT_ROWS, tiles0, L);
+        else return tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+    };
+    // weight blocks a work item runs through
+    auto n_sub = [&](const TileInfo& t) { return C::ROWS ? a.p[t.ph].N / W_ROWS : 1; };
 
     if (warp == 0) {
         // ================================ weight producer
@@ -402,25 +446,28 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 // instead of stalling the ring between tiles (a phase-1 tile is never followed by a
                 // phase-0 claim, so no CTA holds back a tile another CTA waits for)
                 const int L_next = static_cast<int>(gridDim.x) + atomicAdd(a.tile_counter, 1);
-                const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+                const TileInfo ti = tile_at(L);
                 const GemmProblem& P = a.p[ti.ph];
                 const CUtensorMap* tm = ti.ph ? &tmap_w1 : &tmap_w0;
                 const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256, n_blk = P.N / 128;
-                // scale tiles of the tile's 128-row weight blocks: [G][N/128][K/64][512 bytes]
-                const uint8_t* sf_src = P.b_sf + ((static_cast<int64_t>(ti.g) * n_blk + ti.nb * LY::WB) * kb64) * SF_TILE;
-                const int row = ti.nb * W_ROWS;
-                for (int kt = 0; kt < k_stages; ++kt) {
-                    if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
-                    uint8_t* sbase = smem + s * LY::STAGE_BYTES;
-                    const int nat = min(4, kb64 - kt * 4);
-                    ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + LY::WB * nat * SF_TILE);
-                    ptx::tma_load_3d(sbase + LY::OFF_W, tm, &st.full[s], 0, row, ti.g * k_stages + kt);
+                for (int sub = 0; ok && sub < n_sub(ti); ++sub) {
+                    const int nb = C::ROWS ? sub : ti.nb;
+                    // scale tiles of the tile's 128-row weight blocks: [G][N/128][K/64][512 bytes]
+                    const uint8_t* sf_src = P.b_sf + ((static_cast<int64_t>(ti.g) * n_blk + nb * LY::WB) * kb64) * SF_TILE;
+                    const int row = nb * W_ROWS;
+                    for (int kt = 0; kt < k_stages; ++kt) {
+                        if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                        uint8_t* sbase = smem + s * LY::STAGE_BYTES;
+                        const int nat = min(4, kb64 - kt * 4);
+                        ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + LY::WB * nat * SF_TILE);
+                        ptx::tma_load_3d(sbase + LY::OFF_W, tm, &st.full[s], 0, row, ti.g * k_stages + kt);
 #pragma unroll
-                    for (int j = 0; j < LY::WB; ++j)
-                        ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sf_src + static_cast<int64_t>(j) * kb64 * SF_TILE,
-                                       nat * SF_TILE, &st.full[s]);
-                    sf_src += 4 * SF_TILE;
-                    if (++s == C::STAGES) { s = 0; ph ^= 1; }
+                        for (int j = 0; j < LY::WB; ++j)
+                            ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sf_src + static_cast<int64_t>(j) * kb64 * SF_TILE,
+                                           nat * SF_TILE, &st.full[s]);
+                        sf_src += 4 * SF_TILE;
+                        if (++s == C::STAGES) { s = 0; ph ^= 1; }
+                    }
                 }
                 L = L_next;
             }
@@ -439,51 +486,64 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             uint32_t ph = 0, lt = 0;
             bool ok = true;
             TileCursor tc;
-            for (;; ++lt) {
+            for (;;) {
                 const int L = tile_take(st, tc, total, true);
                 if (L >= total || aborted(st)) break;
-                const int kK = a.p[L >= tiles0 ? 1 : 0].K;
+                const int uph = L >= tiles0 ? 1 : 0;
+                const int kK = a.p[uph].K;
                 const int kb64 = kK / 64, k_stages = (kK + 255) / 256;
-                const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
-                if (!ptx::mbar_wait(&st.acc_empty[as], aph ^ 1)) { set_abort(st, a.status); break; }
-                ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem + as * C::ACC_COLS;
-                uint32_t acc = 0;
-                // one K-step: both scale tiles into tensor memory, then the MMA (the tensor pipe runs
-                // them in issue order); the issuing thread's own instruction count bounds the rate,
-                // so full stages take a straight-line path
-                // (a 256-row weight tile has two scale tiles per K-step: rows 128..255 go to the next
-                // four columns)
-                auto kstep = [&](uint64_t so, uint32_t tsfw, uint32_t tsfact, int kk) {
-                    const uint32_t tw = tsfw + kk * LY::SFW_STEP_COLS;
+                const int nsub = C::ROWS ? a.p[uph].N / W_ROWS : 1;
+                for (int sub = 0; ok && sub < nsub; ++sub, ++lt) {
+                    const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
+                    if (!ptx::mbar_wait(&st.acc_empty[as], aph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t d_tmem = tmem + as * C::ACC_COLS;
+                    uint32_t acc = 0;
+                    // one K-step: the scale tiles into tensor memory, then the MMA (the tensor pipe runs
+                    // them in issue order; the copies, not the MMA, bound its rate); the issuing
+                    // thread's own instruction count matters too, so full stages take a straight-line
+                    // path. A 256-row weight tile has two scale tiles per K-step: rows 128..255 go to the
+                    // next four columns. Units keep the activation scales of K-step kg in columns
+                    // SFA_COL + 4 kg, copied during the first weight block.
+                    auto kstep = [&](uint64_t so, uint32_t tsfw, uint32_t tsfact, int kk, int kg) {
+                        const uint32_t tw = tsfw + kk * LY::SFW_STEP_COLS;
 #pragma unroll
-                    for (int j = 0; j < LY::WB; ++j)
-                        ptx::tmem_cp_32x128b_x4(tw + j * 4, dsfw0 + so + kk * kSfAdv + j * (SF_STAGE >> 4));
-                    ptx::tmem_cp_32x128b_x4(tsfact + kk * 4, dsfact0 + so + kk * kSfAdv);
-                    const uint64_t dw = dw0 + so + kk * kOpAdv, dact = dact0 + so + kk * kOpAdv;
-                    if (kSwap)
-                        ptx::mma_nvf4(d_tmem, dw, dact, idesc, tw, tsfact + kk * 4, acc);
-                    else
-                        ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsfact + kk * 4, tw, acc);
-                    acc = 1;
-                };
-                for (int kt = 0; kt < k_stages; ++kt) {
-                    if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
-                    ptx::fence_proxy_async_smem();  // the activation rows came by cp.async (generic proxy)
-                    const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
-                    const uint32_t tsfw = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS, tsfact = tsfw + 4 * LY::SFW_STEP_COLS;
-                    const int nk = min(4, kb64 - kt * 4);
-                    if (nk == 4) {
+                        for (int j = 0; j < LY::WB; ++j)
+                            ptx::tmem_cp_32x128b_x4(tw + j * 4, dsfw0 + so + kk * kSfAdv + j * (SF_STAGE >> 4));
+                        uint32_t tsa;
+                        if constexpr (C::ROWS) {
+                            tsa = tmem + LY::SFA_COL + kg * 4;
+                            if (sub == 0) ptx::tmem_cp_32x128b_x4(tsa, dsfact0 + so + kk * kSfAdv);
+                        } else {
+                            tsa = tsfact + kk * 4;
+                            ptx::tmem_cp_32x128b_x4(tsa, dsfact0 + so + kk * kSfAdv);
+                        }
+                        const uint64_t dw = dw0 + so + kk * kOpAdv, dact = dact0 + so + kk * kOpAdv;
+                        if (kSwap)
+                            ptx::mma_nvf4(d_tmem, dw, dact, idesc, tw, tsa, acc);
+                        else
+                            ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsa, tw, acc);
+                        acc = 1;
+                    };
+                    for (int kt = 0; kt < k_stages; ++kt) {
+                        if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
+                        ptx::fence_proxy_async_smem();  // the activation rows came by cp.async (generic proxy)
+                        const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
+                        const uint32_t tsfw = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS, tsfact = tsfw + 4 * LY::SFW_STEP_COLS;
+                        const int nk = min(4, kb64 - kt * 4);
+                        if (nk == 4) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) kstep(so, tsfw, tsfact, kk);
-                    } else {
-                        for (int kk = 0; kk < nk; ++kk) kstep(so, tsfw, tsfact, kk);
+                            for (int kk = 0; kk < 4; ++kk) kstep(so, tsfw, tsfact, kk, kt * 4 + kk);
+                        } else {
+                            for (int kk = 0; kk < nk; ++kk) kstep(so, tsfw, tsfact, kk, kt * 4 + kk);
+                        }
+                        ptx::tc_commit(&st.empty[s]);
+                        if (++s == C::STAGES) { s = 0; ph ^= 1; }
                     }
-                    ptx::tc_commit(&st.empty[s]);
-                    if (++s == C::STAGES) { s = 0; ph ^= 1; }
+                    if (!ok) break;
+                    ptx::tc_commit(&st.acc_full[as]);
                 }
                 if (!ok) break;
-                ptx::tc_commit(&st.acc_full[as]);
             }
             // every issued tensor-core operation finishes before TMEM is freed
             ptx::tc_commit(&st.drain);
@@ -514,7 +574,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         for (;;) {
             const int L = tile_take(st, tc, total, false);
             if (L >= total || !ok || aborted(st)) break;
-            const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+            const TileInfo ti = tile_at(L);
             const GemmProblem& P = a.p[ti.ph];
             const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
             const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
@@ -549,6 +609,9 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 if (src >= 0) svalid |= 1u << i;
             }
             const uint8_t* sf_tiles = P.a_sf + static_cast<int64_t>(ti.tbg) * kb64 * SF_TILE;
+            // (units: the activation scales go with the first weight block only; the MMA thread
+            // keeps them in tensor memory for the others)
+            for (int sub = 0; ok && sub < n_sub(ti); ++sub)
             for (int kt = 0; kt < k_stages; ++kt) {
                 if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
                 uint8_t* sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
@@ -560,7 +623,8 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     const bool v = ((cvalid >> i) & 1u) && kin;
                     ptx::cp_async_16(sact + r * 128 + ((chunk ^ (r & 7)) * 16), v ? cptr[i] + kt * BK_BYTES : P.a_codes, v);
                 }
-                if (P.a_sf_tiled) {
+                if (C::ROWS && sub > 0) {
+                } else if (P.a_sf_tiled) {
                     // the stage's (up to) 4 scale tiles, 32 lines x 16 bytes each, 2 copies per thread
                     const int nat = min(4, kb64 - kt * 4);
 #pragma unroll
@@ -600,7 +664,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             const int L = tile_take(st, tc, total, false);
             const bool have = L < total && !aborted(st);
             TileInfo ti{};
-            if (have) ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+            if (have) ti = tile_at(L);
             const GemmProblem& P = a.p[ti.ph];
             const int r = lane;  // the tile row of this lane in every slice
             const int64_t p = ti.row0 + r;
@@ -733,10 +797,14 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         uint32_t lt = 0, xt = 0;
         TileCursor tc;
         const bool epi_active = LY::EPI_ACTIVE == C::EPI_WARPS || q == 0;
-        for (; epi_active; ++lt) {
+        bool epi_ok = true;
+        for (; epi_active && epi_ok;) {
             const int L = tile_take(st, tc, total, false);
             if (L >= total || aborted(st)) break;
-            const TileInfo ti = tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
+            const TileInfo tu = tile_at(L);
+            for (int sub = 0; sub < n_sub(tu); ++sub, ++lt) {
+            TileInfo ti = tu;
+            if constexpr (C::ROWS) ti.nb = sub;
             const GemmProblem& P = a.p[ti.ph];
             const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
             // the tile's scales are loaded before waiting for its accumulator, hiding their latency:
@@ -754,7 +822,11 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             }
             const bool got = ptx::mbar_wait(&st.acc_full[as], aph);
             __syncwarp();
-            if (!__all_sync(0xFFFFFFFFu, got)) { set_abort(st, a.status); break; }
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                set_abort(st, a.status);
+                epi_ok = false;
+                break;
+            }
             ptx::tc_fence_after();
             const uint32_t tbase = tmem + as * C::ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
             const int I = P.N / 2;  // h columns (SwiGLU)
@@ -978,6 +1050,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     atomicAdd(a.ready + ti.tbg, 1);
                 }
             }
+            }  // weight blocks of a unit
         }
     }
 
@@ -1016,7 +1089,7 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
     }
     if (a.nphase == 1) tmap[1] = tmap[0];
     const int64_t blocks_ub = (p_max + C::ACT_ROWS - 1) / C::ACT_ROWS + a.G;
-    const int64_t tiles_ub = blocks_ub * (a.p[0].N / C::W_ROWS);
+    const int64_t tiles_ub = blocks_ub * (C::ROWS ? 1 : a.p[0].N / C::W_ROWS);
     const int grid = static_cast<int>(tiles_ub < sms ? (tiles_ub < 1 ? 1 : tiles_ub) : sms);
     // Two phases: CTAs wait on one another's results, so all of them must become resident. The
     // grid is at most one CTA per SM and a CTA needs most of an SM's shared memory, so the whole
@@ -1026,6 +1099,14 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
                       tmap[0], tmap[1], a);
 }
 
+bool gemm_rows_pays(int64_t p_max, int sms)
+{
+    // Token-block units carry six (gate/up) or eight (down) weight blocks each: with fewer than about
+    // eight 128-row blocks per SM the last units leave SMs idle for longer than the saved scale
+    // copies gain (4k tokens: 305 vs 285 us; 16k tokens: 990 vs 1031 us for the expert GEMMs).
+    return p_max >= 8LL * sms * Cfg<kModeWideRows>::ACT_ROWS;
+}
+
 bool gemm_wide_fits(const GemmArgs& a)
 {
     return a.p[0].N % Cfg<kModeWide>::W_ROWS == 0 && (a.nphase < 2 || a.p[1].N % Cfg<kModeWide>::W_ROWS == 0);
@@ -1033,12 +1114,17 @@ bool gemm_wide_fits(const GemmArgs& a)
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream)
 {
-    if ((schedule == kSchedWide || schedule == kSchedWideNarrow) && !gemm_wide_fits(a)) schedule = kSchedActOnM;
+    if ((schedule == kSchedWide || schedule == kSchedWideNarrow || schedule == kSchedWideRows) && !gemm_wide_fits(a))
+        schedule = kSchedActOnM;
     if (schedule == kSchedAuto) schedule = p_max <= 64 ? kSchedWeightsOnM : kSchedActOnM;
     switch (schedule) {
         case kSchedWeightsOnM: return launch_t<kModeSwap>(a, p_max, sms, stream);
         case kSchedWide: return launch_t<kModeWide>(a, p_max, sms, stream);
         case kSchedWideNarrow: return launch_t<kModeWideNarrow>(a, p_max, sms, stream);
+        case kSchedWideRows:
+            if (a.p[0].K <= Cfg<kModeWideRows>::MAX_K && (a.nphase < 2 || a.p[1].K <= Cfg<kModeWideRows>::MAX_K))
+                return launch_t<kModeWideRows>(a, p_max, sms, stream);
+            return launch_t<kModeWide>(a, p_max, sms, stream);
         default: return launch_t<kModeActM>(a, p_max, sms, stream);
     }
 }

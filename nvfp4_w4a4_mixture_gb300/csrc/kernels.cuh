@@ -90,8 +90,10 @@ constexpr int kGemmMaxG = 1025;
 // 256 weight rows per tile (wide: fewer MMAs and scale copies per weight byte; needs N % 256 == 0,
 // else it falls back to activations on M). Auto picks weights-on-M when p_max <= 64.
 // Wide-narrow: the wide shape with 32-row token blocks and a fifth stage (groups of few rows).
-enum GemmSchedule : int { kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2, kSchedWide = 3, kSchedWideNarrow = 4 };
+enum GemmSchedule : int { kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2, kSchedWide = 3, kSchedWideNarrow = 4, kSchedWideRows = 5 };
 bool gemm_wide_fits(const GemmArgs& a);
+// whether a launch of p_max rows is large enough for token-block units (kSchedWideRows)
+bool gemm_rows_pays(int64_t p_max, int sms);
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream);
 int gemm_act_rows(bool weights_on_m);  // token rows per tile of a schedule
 

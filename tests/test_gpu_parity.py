@@ -325,11 +325,12 @@ def _gemm_case(seed, counts, H, I, N_kind):
     return dict(offsets=offsets, P=P, ac=ac, asf=asf, sa=sa, a_row=a_row, bc=bc, bs=bs, bsc=bsc, N=N, K=K)
 
 
-SCHEDS = ["act_on_m", "weights_on_m", "wide"]
+SCHEDS = ["act_on_m", "weights_on_m", "wide", "wide_rows"]
 
 
 def _sched(moe, name):
-    return {"act_on_m": moe.SCHED_ACT_ON_M, "weights_on_m": moe.SCHED_WEIGHTS_ON_M, "wide": moe.SCHED_WIDE}[name]
+    return {"act_on_m": moe.SCHED_ACT_ON_M, "weights_on_m": moe.SCHED_WEIGHTS_ON_M, "wide": moe.SCHED_WIDE,
+            "wide_rows": moe.SCHED_WIDE_ROWS}[name]
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
@@ -453,6 +454,11 @@ def test_layer_decode_full_size(moe):
 
 def test_layer_prefill4k_sampled(moe):
     _check_layer(moe, I_.layer_case("prefill4k", sample=12))
+
+
+def test_layer_prefill16k_sampled(moe):
+    # 16k tokens with a hot expert set: the expert GEMMs take whole token blocks per CTA here
+    _check_layer(moe, I_.layer_case("prefill16k", sample=8))
 
 
 @pytest.mark.parametrize("T", [1, 4, 5, 7, 8, 9, 63, 64, 65, 130])
