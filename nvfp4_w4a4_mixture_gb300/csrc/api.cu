@@ -165,6 +165,16 @@ CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+bool gemm_permute_enabled()
+{
+    // on unless MOE_NVFP4_GEMM_PERMUTE=0
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_NVFP4_GEMM_PERMUTE");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
 bool pdl_enabled()
 {
     // On unless MOE_NVFP4_PDL=0. Each CTA of the front half and of the expert GEMMs allows the next
@@ -454,11 +464,17 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     // token-block counters of the expert GEMMs, then their tile counter (all zeroed before the launch)
     const int n_ready = static_cast<int>((P + 31) / 32 + E + 1);
     const bool one_launch_front = front_fits(T, H, E, k);
+    // small batches on wide-narrow tiles: the front half stops at the top-k and every CTA of the
+    // expert GEMMs builds the permutation from the ids in its own shared memory (off the front
+    // half's single-CTA tail)
+    const bool gemm_permutes = one_launch_front && T <= kRouteMaxT && static_cast<int64_t>(T) * k <= kRouteMaxAssign &&
+                               (2 * I) % 256 == 0 && H % 256 == 0 && gemm_permute_enabled();
     MOE_CUDA(mark(0), "event record");
     if (one_launch_front) {
         // small batch: quantisation, router, top-k, shared gate and permutation in one launch
         MOE_CUDA(launch_front(x, T, H, E, k, L->w_router, L->logit_bias, PF(W.logits), P8(W.x_codes), P8(W.x_sf),
-                              &hdr->s_x, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), P32(W.offsets),
+                              &hdr->s_x, P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g),
+                              gemm_permutes ? nullptr : P32(W.offsets),
                               P32(W.perm_src), P32(W.src_perm), P32(W.row_token), &hdr->ticket, P32(W.ready),
                               n_ready + 1, s),
                  "front");
@@ -521,6 +537,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     ga.ready = P32(W.ready);
     ga.tile_counter = P32(W.ready) + n_ready;
     ga.status = &hdr->status;
+    if (gemm_permutes) ga.route = GemmRoute{P32(W.topk_ids), T, k, E};
     // 256-row weight tiles when H allows (half the MMAs and scale copies per weight byte); else
     // weights on the MMA's M side for few rows per expert (decode), 128 x 128 tiles otherwise
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;

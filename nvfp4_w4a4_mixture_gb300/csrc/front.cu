@@ -46,7 +46,7 @@ struct FrontArgs {
     int32_t* topk_ids;     // [T][k]
     float* topk_w;
     float* shared_g;
-    int32_t* offsets;      // [E+2]
+    int32_t* offsets;      // [E+2]; null: no permutation (the expert GEMMs build it)
     int32_t* perm_src;     // [T*k]
     int32_t* src_perm;
     int32_t* row_token;    // [T*k + T]
@@ -155,8 +155,10 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
     const int n = T * k;
     if (tid < 4) ids_s[n + tid] = INT_MAX;  // pads the ids to a multiple of 4 (n + 4 <= 516)
     __syncthreads();  // ids_s complete
-    // stable permutation (rank by counting; offsets by lower bounds in the ids in position order)
-    block_small_permute<kFrontThreads>(ids_s, n, k, T, E, sorted_s, a.offsets, a.perm_src, a.src_perm, a.row_token);
+    // stable permutation (rank by counting; offsets by lower bounds in the ids in position order),
+    // unless the expert GEMMs build it themselves from the ids (offsets null)
+    if (a.offsets)
+        block_small_permute<kFrontThreads>(ids_s, n, k, T, E, sorted_s, a.offsets, a.perm_src, a.src_perm, a.row_token);
     for (int i = tid; i < a.n_ready; i += kFrontThreads) a.ready[i] = 0;
     if (tid == 0) *a.ticket = 0u;  // every CTA has taken its ticket: ready for the next call
     ptx::griddep_launch_dependents();

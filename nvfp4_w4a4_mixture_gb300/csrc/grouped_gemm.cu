@@ -34,7 +34,10 @@
 // acc_full / acc_empty: MMA <-> epilogue). Every wait is bounded (ptx::mbar_wait, spin_until): on
 // timeout the CTA records kDevTimeoutGemm in the status word, all roles stop, and TMEM is freed
 // after the tensor cores drain.
+#include <climits>
+
 #include "kernels.cuh"
+#include "route.cuh"
 
 namespace moe {
 
@@ -159,11 +162,18 @@ struct AccXchg {
     float v[32][260];
 };
 
+// a launch's own permutation (GemmRoute): permuted row -> source row of x (gate/up gather), and
+// permuted routed row -> assignment t*k + j (down output row)
+struct RouteSmem {
+    int32_t row[kRouteMaxAssign + kRouteMaxT];
+    int32_t perm[kRouteMaxAssign];
+};
+
 template <int kMode>
 constexpr size_t smem_bytes()
 {
     return 1024 + static_cast<size_t>(Cfg<kMode>::STAGES) * Lay<kMode>::STAGE_BYTES + sizeof(Tail<kMode>) +
-           (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0) + (Cfg<kMode>::XCHG ? sizeof(AccXchg) : 0);
+           (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0) + (Cfg<kMode>::XCHG ? sizeof(AccXchg) + sizeof(RouteSmem) : 0);
 }
 static_assert(smem_bytes<kModeActM>() <= 232448 && smem_bytes<kModeSwap>() <= 232448 &&
                   smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448 &&
@@ -175,7 +185,7 @@ struct TileInfo {
 };
 
 // tb_off[g] = sum_{g' < g} ceil(rows_g' / act_rows), g = 0..G (block-wide scan; contains barriers),
-// and g_off = offsets[0..G]
+// and g_off = offsets[0..G] (offsets in global or shared memory; g_off may be offsets itself)
 __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, int act_rows, int32_t* tb_off,
                                   int32_t* g_off, int32_t* wsum)
 {
@@ -184,7 +194,7 @@ __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, in
     const int g0 = min(G, t * per), g1 = min(G, g0 + per);
     int32_t s = 0;
     for (int g = g0; g < g1; ++g) {
-        const int32_t r = __ldg(offsets + g + 1) - __ldg(offsets + g);
+        const int32_t r = offsets[g + 1] - offsets[g];
         s += r > 0 ? (r + act_rows - 1) / act_rows : 0;
     }
     int32_t x = s;
@@ -208,13 +218,13 @@ __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, in
     int32_t run = x - s + (warp > 0 ? wsum[warp - 1] : 0);
     for (int g = g0; g < g1; ++g) {
         tb_off[g] = run;
-        const int32_t o0 = __ldg(offsets + g), r = __ldg(offsets + g + 1) - o0;
-        g_off[g] = o0;
+        const int32_t o0 = offsets[g], r = offsets[g + 1] - o0;
+        if (g_off != offsets) g_off[g] = o0;
         run += r > 0 ? (r + act_rows - 1) / act_rows : 0;
     }
     if (t == nt - 1) {
         tb_off[G] = wsum[nwarps - 1];
-        g_off[G] = __ldg(offsets + G);
+        if (g_off != offsets) g_off[G] = offsets[G];
     }
     __syncthreads();
 }
@@ -413,7 +423,23 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     }
     // everything above overlaps the previous launch; the group offsets and activations come from it
     ptx::griddep_wait();
-    block_tile_prefix(a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.g_off, st.wsum);
+    // a launch given the top-k ids builds its permutation here (stage 0's buffer is scratch until the
+    // producers start): offsets straight into st.g_off, rows into rs
+    RouteSmem* rs = nullptr;
+    if constexpr (C::XCHG) {
+        if (a.route.topk_ids) {
+            rs = reinterpret_cast<RouteSmem*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kMode>) + sizeof(AccXchg));
+            int32_t* ids_s = reinterpret_cast<int32_t*>(smem);          // n + 4 (padded to 16 bytes)
+            int32_t* sorted_s = ids_s + kRouteMaxAssign + 4;             // n
+            const int n = a.route.T * a.route.k;
+            for (int i = tid; i < n + 4; i += LY::THREADS) ids_s[i] = i < n ? a.route.topk_ids[i] : INT_MAX;
+            __syncthreads();
+            block_small_permute<LY::THREADS>(ids_s, n, a.route.k, a.route.T, a.route.E, sorted_s, st.g_off, rs->perm,
+                                             nullptr, rs->row);
+            __syncthreads();
+        }
+    }
+    block_tile_prefix(rs ? st.g_off : a.offsets, a.G, C::ACT_ROWS, st.tb_off, st.g_off, st.wsum);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -606,13 +632,15 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS);
                 if (!spin_until(a.ready + ti.tbg, target)) { set_abort(st, a.status); break; }
             }
-            // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row
+            // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row (a launch
+            // that permutes itself has the gate/up rows in shared memory)
+            const int32_t* a_row = rs && ti.ph == 0 ? rs->row : P.a_row;
             int64_t srcv[(RW + 31) / 32];
 #pragma unroll
             for (int h = 0; h < (RW + 31) / 32; ++h) {
                 const int r = w2 * RW + h * 32 + lane;
                 const int64_t p = ti.row0 + r;
-                srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (P.a_row ? static_cast<int64_t>(__ldg(P.a_row + p)) : p) : -1;
+                srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (a_row ? static_cast<int64_t>(a_row[p]) : p) : -1;
             }
             cvalid = 0;
             svalid = 0;
@@ -712,7 +740,8 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 sb0 = __ldg(P.b_scale + (P.gate_up ? 2 * ti.g : ti.g));
                 sb1 = P.gate_up ? __ldg(P.b_scale + 2 * ti.g + 1) : sb0;
                 S_h = P.epilogue == kEpiSwiGLU ? __ldg(P.epi_scale + ti.g) : 1.0f;
-                if (P.out_row && valid && p < P.out_row_n) po = __ldg(P.out_row + p);
+                const int32_t* out_row = rs && ti.ph == 1 ? rs->perm : P.out_row;
+                if (out_row && valid && p < P.out_row_n) po = out_row[p];
             }
             bool ok = true;
             if (have && q == 0) {

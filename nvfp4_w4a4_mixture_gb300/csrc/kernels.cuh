@@ -75,11 +75,22 @@ struct GemmProblem {
 
 // A launch: one problem, or the gate/up problem (phase 0) followed by the down problem (phase 1)
 // over the same groups; phase-1 tiles of a token block wait for that block's phase-0 tiles.
+// Routing the launch turns into its own permutation (32-row token blocks only): the top-k ids of
+// T <= 32 tokens (T * k <= 512), expert E being the shared one. Each CTA builds the group offsets,
+// the gate/up gather rows and the down output rows in shared memory; offsets and the a_row / out_row
+// indices of the problems are then unused.
+struct GemmRoute {
+    const int32_t* topk_ids;  // [T][k], null: offsets and row indices come from global memory
+    int T, k, E;
+};
+constexpr int kRouteMaxT = 32, kRouteMaxAssign = 512;
+
 struct GemmArgs {
     GemmProblem p[2];
     int nphase;
     const int32_t* offsets;   // [G+1]
     int G;
+    GemmRoute route;
     int32_t* ready;           // [token blocks], zeroed before a two-phase launch
     int32_t* tile_counter;    // tiles handed out beyond the first gridDim.x, zeroed before each launch
     int* status;
