@@ -481,8 +481,12 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         MOE_CUDA(mark(1), "event record");
         MOE_CUDA(mark(2), "event record");
     } else {
+        // the counters the launches below rely on are zeroed first, so no memset sits between two
+        // kernels (each launch overlaps the one before it: programmatic dependent launch)
+        MOE_CUDA(cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(unsigned), s), "clear the tensor-max scratch");
+        MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");
         // W4A4: quantize the layer input once per token (dynamic tensor scale)
-        MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s),
+        MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s, true),
                  "quantize");
         MOE_CUDA(mark(1), "event record");
         // router, softmax, top-k, shared gate
@@ -544,8 +548,6 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     // (token-block units once there are enough of them to keep every SM busy to the end)
     const int sched = gemm_wide_fits(ga) ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
                                          : small ? kSchedWeightsOnM : kSchedActOnM;
-    if (!one_launch_front)  // (the one-launch front half clears them itself)
-        MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");
     MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");
     MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)

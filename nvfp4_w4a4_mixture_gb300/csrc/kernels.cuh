@@ -10,7 +10,8 @@ namespace moe {
 
 // ---- quantize.cu
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes, uint8_t* sf,
-                            float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream);
+                            float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream,
+                            bool amax_zeroed = false);
 cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
                                 uint8_t* sf, float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream);
 

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kPermWarps * 32)
     k_perm_hist(const int32_t* __restrict__ ids, int64_t n, int E, int64_t nchunks, int32_t* __restrict__ hist,
                 int* status)
 {
+    ptx::griddep_wait();  // inputs come from the launch before this one
     extern __shared__ int32_t cnt[];  // [kPermWarps][E]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     int32_t* my = cnt + warp * E;
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(kRowScanThreads)
     k_perm_rowscan(int32_t* __restrict__ hist, int32_t* __restrict__ totals, int64_t nchunks, int E, int T,
                    int with_shared, int32_t* __restrict__ offsets, unsigned* ticket)
 {
+    ptx::griddep_wait();  // inputs come from the launch before this one
     using Scan = cub::BlockScan<int32_t, kRowScanThreads>;
     __shared__ typename Scan::TempStorage tmp;
     __shared__ unsigned last_s;
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(kPermWarps * 32)
                    const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
                    int32_t* __restrict__ src_perm, int32_t* __restrict__ row_token)
 {
+    ptx::griddep_wait();  // inputs come from the launch before this one
     extern __shared__ int32_t base_s[];  // [kPermWarps][E]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // the shared-expert rows: row T*k + t holds token t
@@ -150,6 +153,7 @@ __global__ void __launch_bounds__(kScanThreads)
                  int32_t* __restrict__ perm_src, int32_t* __restrict__ src_perm, int32_t* __restrict__ row_token,
                  int* status)
 {
+    ptx::griddep_wait();  // inputs come from the launch before this one
     using Scan = cub::BlockScan<int32_t, kScanThreads>;
     __shared__ typename Scan::TempStorage tmp;
     __shared__ int32_t ids_s[kSmallPerm];
@@ -201,19 +205,22 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int wit
 {
     const int64_t n = static_cast<int64_t>(T) * k;
     if (n <= kSmallPerm) {
-        k_perm_small<<<1, kScanThreads, 0, stream>>>(topk_ids, static_cast<int>(n), E, k, T, with_shared, offsets,
-                                                     perm_src, src_perm, row_token, status);
-        return cudaGetLastError();
+        return launch_pdl(k_perm_small, dim3(1), dim3(kScanThreads), 0, stream, topk_ids, static_cast<int>(n), E, k, T,
+                          with_shared, offsets, perm_src, src_perm, row_token, status);
     }
     const int64_t nchunks = perm_chunks(n);
     const int blocks = static_cast<int>((nchunks + kPermWarps - 1) / kPermWarps);
     const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
     int32_t* totals = hist + nchunks * E;
-    k_perm_hist<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, nchunks, hist, status);
-    k_perm_rowscan<<<E, kRowScanThreads, 0, stream>>>(hist, totals, nchunks, E, T, with_shared, offsets, ticket);
-    k_perm_scatter<<<blocks, kPermWarps * 32, smem, stream>>>(topk_ids, n, E, k, T, with_shared, nchunks, hist, offsets,
-                                                              perm_src, src_perm, row_token);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(k_perm_hist, dim3(blocks), dim3(kPermWarps * 32), smem, stream, topk_ids, n, E, nchunks, hist,
+                               status);
+    if (e == cudaSuccess)
+        e = launch_pdl(k_perm_rowscan, dim3(E), dim3(kRowScanThreads), 0, stream, hist, totals, nchunks, E, T, with_shared,
+                       offsets, ticket);
+    if (e == cudaSuccess)
+        e = launch_pdl(k_perm_scatter, dim3(blocks), dim3(kPermWarps * 32), smem, stream, topk_ids, n, E, k, T, with_shared,
+                       nchunks, hist, static_cast<const int32_t*>(offsets), perm_src, src_perm, row_token);
+    return e;
 }
 
 }  // namespace moe

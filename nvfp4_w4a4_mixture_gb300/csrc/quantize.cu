@@ -38,6 +38,7 @@ __device__ __forceinline__ uint32_t abs_bits_max(uint32_t m, float f) { return m
 template <typename Tin>
 __global__ void k_amax(const Tin* __restrict__ x, int64_t nblocks, unsigned* __restrict__ amax_bits)
 {
+    ptx::griddep_wait();  // x may come from the launch before this one
     uint32_t m = 0;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
@@ -48,6 +49,7 @@ __global__ void k_amax(const Tin* __restrict__ x, int64_t nblocks, unsigned* __r
     }
     m = __reduce_max_sync(0xFFFFFFFFu, m);
     if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(amax_bits, m);
+    ptx::griddep_launch_dependents();
 }
 
 template <typename Tin>
@@ -55,6 +57,7 @@ __global__ void k_quantize(const Tin* __restrict__ x, int64_t nblocks, const flo
                            const unsigned* __restrict__ amax_bits, uint8_t* __restrict__ codes,
                            uint8_t* __restrict__ sf, float* __restrict__ s_out)
 {
+    ptx::griddep_wait();  // the tensor max comes from the launch before this one
     float S;
     if (s_static) {
         S = *s_static;
@@ -73,6 +76,7 @@ __global__ void k_quantize(const Tin* __restrict__ x, int64_t nblocks, const flo
         *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(lo, hi);
         sf[b] = static_cast<uint8_t>(s);
     }
+    ptx::griddep_launch_dependents();
 }
 
 // Small tensors (<= kSmallBlocks blocks, e.g. a decode batch): one CTA computes the max and encodes,
@@ -85,6 +89,7 @@ __global__ void __launch_bounds__(kSmallThreads)
     k_quantize_small(const Tin* __restrict__ x, int64_t nblocks, const float* __restrict__ s_static,
                      uint8_t* __restrict__ codes, uint8_t* __restrict__ sf, float* __restrict__ s_out)
 {
+    ptx::griddep_wait();  // x may come from the launch before this one
     __shared__ uint32_t wmax[kSmallThreads / 32];
     __shared__ float S_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -122,6 +127,7 @@ __global__ void __launch_bounds__(kSmallThreads)
         *reinterpret_cast<uint2*>(codes + b * 8) = make_uint2(lo, hi);
         sf[b] = static_cast<uint8_t>(s);
     }
+    ptx::griddep_launch_dependents();
 }
 
 static int quant_grid(int64_t nblocks, int sms)
@@ -133,32 +139,35 @@ static int quant_grid(int64_t nblocks, int sms)
 
 template <typename Tin>
 cudaError_t launch_quantize_t(const Tin* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes, uint8_t* sf,
-                              float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
+                              float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream, bool amax_zeroed)
 {
     const int64_t nblocks = rows * K / 16;
-    if (nblocks <= kSmallBlocks) {
-        k_quantize_small<Tin><<<1, kSmallThreads, 0, stream>>>(x, nblocks, s_in, codes, sf, s_out);
-        return cudaGetLastError();
-    }
+    if (nblocks <= kSmallBlocks)
+        return launch_pdl(k_quantize_small<Tin>, dim3(1), dim3(kSmallThreads), 0, stream, x, nblocks, s_in, codes, sf, s_out);
     if (!s_in) {
-        cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), stream);
-        if (e != cudaSuccess) return e;
-        if (nblocks > 0) k_amax<Tin><<<quant_grid(nblocks, sms), 256, 0, stream>>>(x, nblocks, amax_scratch);
+        if (!amax_zeroed) {
+            cudaError_t e = cudaMemsetAsync(amax_scratch, 0, sizeof(unsigned), stream);
+            if (e != cudaSuccess) return e;
+        }
+        if (nblocks > 0) {
+            cudaError_t e = launch_pdl(k_amax<Tin>, dim3(quant_grid(nblocks, sms)), dim3(256), 0, stream, x, nblocks, amax_scratch);
+            if (e != cudaSuccess) return e;
+        }
     }
-    k_quantize<Tin><<<quant_grid(nblocks, sms), 256, 0, stream>>>(x, nblocks, s_in, amax_scratch, codes, sf, s_out);
-    return cudaGetLastError();
+    return launch_pdl(k_quantize<Tin>, dim3(quant_grid(nblocks, sms)), dim3(256), 0, stream, x, nblocks, s_in,
+                      static_cast<const unsigned*>(amax_scratch), codes, sf, s_out);
 }
 
 cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes, uint8_t* sf,
-                            float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
+                            float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream, bool amax_zeroed)
 {
-    return launch_quantize_t<uint16_t>(x, rows, K, s_in, codes, sf, s_out, amax_scratch, sms, stream);
+    return launch_quantize_t<uint16_t>(x, rows, K, s_in, codes, sf, s_out, amax_scratch, sms, stream, amax_zeroed);
 }
 
 cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
                                 uint8_t* sf, float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
 {
-    return launch_quantize_t<float>(x, rows, K, s_in, codes, sf, s_out, amax_scratch, sms, stream);
+    return launch_quantize_t<float>(x, rows, K, s_in, codes, sf, s_out, amax_scratch, sms, stream, false);
 }
 
 }  // namespace moe

@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(kRouterWarps * 32)
     k_router_logits(const uint16_t* __restrict__ x, int T, int H, int E, const uint16_t* __restrict__ w,
                     const float* __restrict__ bias, float* __restrict__ logits)
 {
+    ptx::griddep_wait();  // x may come from the launch before this one
     extern __shared__ __align__(16) uint16_t xs[];  // [kRouterTT][H]
     const int t0 = blockIdx.y * kRouterTT;
     const int nt = min(kRouterTT, T - t0);
@@ -90,6 +91,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     k_topk(const float* __restrict__ logits, int ld, int T, int E, int k, int32_t* __restrict__ topk_ids,
            float* __restrict__ topk_w, float* __restrict__ shared_g, float* __restrict__ logits_out)
 {
+    ptx::griddep_wait();  // the logits come from the launch before this one
     __shared__ uint2 cand_s[kTopkWarps][kTopkCand];
     __shared__ uint2 sel_s[kTopkWarps][32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -123,17 +125,15 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, int E, const u
         attr_set = true;
     }
     dim3 grid((E + 1 + kRouterWarps - 1) / kRouterWarps, (T + kRouterTT - 1) / kRouterTT);
-    k_router_logits<<<grid, kRouterWarps * 32, smem, stream>>>(x, T, H, E, w_router, bias, logits);
-    return cudaGetLastError();
+    return launch_pdl(k_router_logits, grid, dim3(kRouterWarps * 32), smem, stream, x, T, H, E, w_router, bias, logits);
 }
 
 cudaError_t launch_topk(const float* logits, int ld, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                         float* shared_g, float* logits_out, cudaStream_t stream)
 {
     if (T <= 0) return cudaSuccess;
-    k_topk<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, stream>>>(logits, ld, T, E, k, topk_ids, topk_w,
-                                                                             shared_g, logits_out);
-    return cudaGetLastError();
+    return launch_pdl(k_topk, dim3((T + kTopkWarps - 1) / kTopkWarps), dim3(kTopkWarps * 32), 0, stream, logits, ld, T, E, k,
+                      topk_ids, topk_w, shared_g, logits_out);
 }
 
 }  // namespace moe
