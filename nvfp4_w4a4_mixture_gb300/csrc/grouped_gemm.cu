@@ -7,11 +7,15 @@
 // One persistent CTA per SM; the weight producer of each CTA takes output tiles (token block of a
 // group x W_ROWS weight rows) from a global counter, weight blocks fastest, so CTAs working at the
 // same time share a token block's activation rows and one expert's weights stay in L2 across its
-// token blocks. Three tile shapes:
+// token blocks. Tile shapes:
 //   activations on M (large groups): 128 token rows x 128 weight rows, MMA 128 x 128;
 //   weights on M (small groups): 128 weight rows x 32 token rows, MMA 128 x 32;
 //   wide: 128 token rows x 256 weight rows, MMA 128 x 256 (half the MMAs and scale copies per
-//     weight byte; single-buffered accumulator).
+//     weight byte; single-buffered accumulator);
+//   wide-narrow: wide with 32-row token blocks (decode), the accumulator finished through shared
+//     memory by all epilogue warps; given the routing ids, each CTA builds the permutation itself;
+//   wide, token-block units: a CTA takes a whole token block through every weight block of its
+//     phase, keeping the block's activation scales in tensor memory (large batches).
 // A launch can hold two problems (phases) over the same groups: the gate/up GEMM with its SwiGLU
 // epilogue, then the down GEMM reading the intermediate h. All phase-0 tiles are handed out before
 // any phase-1 tile. A down tile of token block b waits (bounded) until every gate/up tile of block
@@ -27,7 +31,9 @@
 //                into tensor memory and one tcgen05.mma into the (double- or single-buffered)
 //                accumulator;
 //   warps 2-3    activation producers: gather the tile's activation rows (row index list) with
-//                cp.async into the swizzled layout, and their scale factors into tile layout;
+//                cp.async into the swizzled layout, and their scale factors into tile layout; a
+//                stage's arrival is tracked by cp.async.mbarrier.arrive (or, for 32-row blocks,
+//                made by the warp once the copies have landed);
 //   warps 4..    epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes 32*(w%4)..+31), apply
 //                the tensor scales and write FP32 / bf16 rows, or SwiGLU + NVFP4 requantisation.
 // Stage hand-over uses mbarriers (full: producers -> MMA; empty: MMA commit -> producers;
@@ -229,6 +235,21 @@ __device__ void block_tile_prefix(const int32_t* __restrict__ offsets, int G, in
     __syncthreads();
 }
 
+// Group, first row and row count of token block ti.tbg (tb_off[g] <= tbg < tb_off[g + 1]).
+__device__ __forceinline__ void place_block(const int32_t* tb_off, const int32_t* g_off, const GemmArgs& a,
+                                            int act_rows, TileInfo& ti)
+{
+    int lo = 0, hi = a.G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
+    }
+    ti.g = lo;
+    const int g0 = g_off[lo], g1 = g_off[lo + 1];
+    ti.row0 = g0 + (ti.tbg - tb_off[lo]) * act_rows;
+    ti.rows = min(act_rows, g1 - ti.row0);
+}
+
 // Tile L of the launch: phase-0 tiles first (token block major, weight block minor), then phase 1.
 __device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const int32_t* g_off, const GemmArgs& a,
                                               int act_rows, int w_rows, int tiles0, int L)
@@ -239,15 +260,7 @@ __device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const int32
     const int n_wb = a.p[ti.ph].N / w_rows;
     ti.tbg = Lp / n_wb;
     ti.nb = Lp - ti.tbg * n_wb;
-    int lo = 0, hi = a.G;  // tb_off[lo] <= tbg < tb_off[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
-    }
-    ti.g = lo;
-    const int g0 = g_off[lo], g1 = g_off[lo + 1];
-    ti.row0 = g0 + (ti.tbg - tb_off[lo]) * act_rows;
-    ti.rows = min(act_rows, g1 - ti.row0);
+    place_block(tb_off, g_off, a, act_rows, ti);
     return ti;
 }
 
@@ -260,15 +273,7 @@ __device__ __forceinline__ TileInfo unit_info(const int32_t* tb_off, const int32
     ti.ph = L >= units0 ? 1 : 0;
     ti.tbg = L - (ti.ph ? units0 : 0);
     ti.nb = 0;
-    int lo = 0, hi = a.G;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (tb_off[mid] <= ti.tbg) lo = mid; else hi = mid;
-    }
-    ti.g = lo;
-    const int g0 = g_off[lo], g1 = g_off[lo + 1];
-    ti.row0 = g0 + (ti.tbg - tb_off[lo]) * act_rows;
-    ti.rows = min(act_rows, g1 - ti.row0);
+    place_block(tb_off, g_off, a, act_rows, ti);
     return ti;
 }
 
