@@ -247,6 +247,7 @@ moe_status_t moe_read_device_status(void* ws, moe_stream_t stream)
     MOE_CUDA(cudaMemset(ws, 0, sizeof(int)), "clear status");
     if (status & kDevTimeoutGemm) return fail(MOE_ERR_DEVICE_TIMEOUT, "device status 0x%x: grouped GEMM wait timed out", status);
     if (status & kDevTimeoutRouter) return fail(MOE_ERR_DEVICE_TIMEOUT, "device status 0x%x: router wait timed out", status);
+    if (status & kDevTimeoutCombine) return fail(MOE_ERR_DEVICE_TIMEOUT, "device status 0x%x: combine wait timed out", status);
     if (status & kDevBadExpertId) return fail(MOE_ERR_INVALID_ARG, "device status 0x%x: expert id outside [0, E)", status);
     return MOE_OK;
 }
@@ -420,7 +421,7 @@ moe_status_t moe_combine(const uint16_t* y, const float* topk_w, const float* sh
     if (!aligned(y, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
         return fail(MOE_ERR_MISALIGNED, "y, out and residual must be 16-byte aligned");
     MOE_TRY(check_device());
-    MOE_CUDA(launch_combine(y, topk_w, shared_g, src_perm, T, k, H, residual, out, static_cast<cudaStream_t>(stream)),
+    MOE_CUDA(launch_combine(y, topk_w, shared_g, src_perm, T, k, H, residual, out, nullptr, static_cast<cudaStream_t>(stream)),
              "combine launch");
     return MOE_OK;
 }
@@ -552,7 +553,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)
     MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), nullptr, T, k,
-                            H, residual, out, s),
+                            H, residual, out, &hdr->status, s),
              "combine");
     MOE_CUDA(mark(5), "event record");
     return MOE_OK;

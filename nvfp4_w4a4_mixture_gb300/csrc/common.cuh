@@ -14,6 +14,7 @@ enum : int {
     kDevTimeoutGemm = 1,   // a bounded wait in the grouped GEMM ran out
     kDevBadExpertId = 2,   // moe_permute met an id outside [0, E)
     kDevTimeoutRouter = 4, // a bounded wait in the tensor-core router ran out
+    kDevTimeoutCombine = 8, // a bounded wait in the streaming combine ran out
 };
 
 // First 256 bytes of every workspace.

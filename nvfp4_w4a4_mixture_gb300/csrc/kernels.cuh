@@ -110,8 +110,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, 
 int gemm_act_rows(bool weights_on_m);  // token rows per tile of a schedule
 
 // ---- combine.cu
+// status: nullable device status word (the streaming variant records kDevTimeoutCombine there)
 cudaError_t launch_combine(const uint16_t* y, const float* topk_w, const float* shared_g, const int32_t* src_perm, int T,
-                           int k, int H, const uint16_t* residual, uint16_t* out, cudaStream_t stream);
+                           int k, int H, const uint16_t* residual, uint16_t* out, int* status, cudaStream_t stream);
 
 // ---- api.cu
 int device_sm_count();
