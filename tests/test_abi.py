@@ -59,6 +59,16 @@ def test_workspace_bytes_grows_with_tokens(L):
     assert L.moe_workspace_bytes(-1, 512, 10, 768, 4) == 0
 
 
+def test_workspace_bytes_host_adds_three_staging_buffers(L):
+    # the host-buffer layer call stages x, the residual and the output (T x H bf16 each, 256-byte
+    # aligned) behind the layer's own workspace
+    for H, T in ((2048, 4), (2048, 4096), (256, 3)):
+        base = L.moe_workspace_bytes(H, 512, 10, 768, T)
+        stage = (T * H * 2 + 255) // 256 * 256
+        assert L.moe_workspace_bytes_host(H, 512, 10, 768, T) == base + 3 * stage
+    assert L.moe_workspace_bytes_host(2048, 512, 10, 768, -1) == 0
+
+
 MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_MISALIGNED = 1, 2, 3, 4
 
 
@@ -103,6 +113,29 @@ def test_layer_validation(L):
     nullbank = m.NvFp4Bank(p, None, p)
     bad = m.LayerDesc(2048, 512, 10, 768, p, None, nullbank, bank, p)
     assert f(ctypes.byref(bad), _fake(p), 4, None, _fake(p + 4096), ws, need, None) == MOE_ERR_INVALID_ARG
+
+
+def test_layer_host_validation(L):
+    # host-side checks of the host-buffer layer call, made before any device is touched
+    import nvfp4_w4a4_mixture_gb300 as m
+
+    p = 0x40000
+    bank = m.NvFp4Bank(p, p, p)
+    good = m.LayerDesc(2048, 512, 10, 768, p, None, bank, bank, p)
+    ws = _fake(0x100000)
+    need = L.moe_workspace_bytes_host(2048, 512, 10, 768, 4)
+    f = L.moe_layer_forward_host
+    x, out = _fake(0x7000000), _fake(0x7100000)
+    assert f(None, x, 4, None, out, ws, need, None) == MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), None, 4, None, out, ws, need, None) == MOE_ERR_INVALID_ARG
+    assert f(ctypes.byref(good), x, -1, None, out, ws, need, None) == MOE_ERR_UNSUPPORTED_SHAPE
+    # out overlapping x (4 tokens x 4 KB) or the residual
+    assert f(ctypes.byref(good), x, 4, None, _fake(0x7000000 + 4096), ws, need, None) == MOE_ERR_INVALID_ARG
+    assert b"overlaps" in L.moe_last_error_detail()
+    assert f(ctypes.byref(good), x, 4, _fake(0x7100000 + 8192), out, ws, need, None) == MOE_ERR_INVALID_ARG
+    # the layer's workspace alone is not enough: the three staging buffers come on top of it
+    small = L.moe_workspace_bytes(2048, 512, 10, 768, 4)
+    assert f(ctypes.byref(good), x, 4, None, out, ws, small, None) == MOE_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_gemm_and_permute_validation(L):
