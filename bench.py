@@ -10,8 +10,11 @@ resident in HBM. The default workload is the Flash-Next-shaped decode call: hidd
 experts, top-10 + 1 shared, intermediate 768, 4 tokens (an MTP K=3 verify window). L2 is flushed
 before every timed step, outside the timed interval: a 256 MiB write, then a 256 MiB read of a
 second buffer, so the write-back of the flushed lines also happens before the step. Each step is
-timed with CUDA events on the launching stream. Under torchrun every rank runs an independent
-replica (weak scaling: per-GPU work fixed); rank 0 prints one JSON line.
+timed with CUDA events on the launching stream. The end-to-end figure ("e2e") goes through the
+library's host-buffer call (moe_layer_forward_host: pinned host input, the copy in, the layer and the
+copy out inside the interval; for the layer stack one copy in and one copy out around the layers).
+Under torchrun every rank runs an independent replica (weak scaling: per-GPU work fixed); rank 0
+prints one JSON line.
 
 --impl reference times the CPU oracle (the plain FP64 reference of the same layer) on the host
 cores, one bounded sample of the workload per step.
