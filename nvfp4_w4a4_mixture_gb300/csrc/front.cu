@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(kFrontThreads) k_decode_front(const FrontArgs 
         return;
     }
 
-    // ---- last CTA: one warp per token (top-k), then the permutation
+    // ---- last CTA: one warp per token (top-k), then the permutation. The next launch may start
+    // now: its CTAs take the SMs the other CTAs have left and run their prologue during this tail
+    // (their dependent reads wait for this grid to complete)
+    ptx::griddep_launch_dependents();
     for (int t = warp; t < T; t += kFrontWarps) {
         const float* l = a.logits + static_cast<int64_t>(t) * (E + 1);
         const float l_gate = lane == 0 ? __ldcg(l + E) : 0.0f;  // shared-gate logit, loaded with the rest
