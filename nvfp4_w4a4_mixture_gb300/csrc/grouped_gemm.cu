@@ -475,7 +475,12 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             while (ok && !aborted(st)) {
                 if (L > total) L = total;
                 if (!tile_publish(st, tc, L)) { set_abort(st, a.status); break; }
-                if (L >= total) break;
+                if (L >= total) {
+                    // this CTA's last tile is loading: the next launch may be scheduled (its CTAs
+                    // start as SMs free up; its dependent reads wait for this grid to complete)
+                    ptx::griddep_launch_dependents();
+                    break;
+                }
                 // claim the next tile now: the atomic's round trip overlaps this tile's stages
                 // instead of stalling the ring between tiles (a phase-1 tile is never followed by a
                 // phase-0 claim, so no CTA holds back a tile another CTA waits for)
