@@ -2,6 +2,7 @@
 // workspace layout, and the launch sequence of the layer forward.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -91,6 +92,20 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     L.y = take(P * H * 2);
     L.total = off;
     return L;
+}
+
+// moe_layer_forward_host: x (and the residual) from page-locked host memory into the staging
+// buffers, 16 bytes per thread (n16 = bytes / 16 of each); the previous launch may still read them
+__global__ void k_stage_in(const uint4* __restrict__ x, uint4* __restrict__ xd, const uint4* __restrict__ r,
+                           uint4* __restrict__ rd, int64_t n16)
+{
+    ptx::griddep_wait();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        xd[i] = x[i];
+        if (r) rd[i] = r[i];
+    }
+    ptx::griddep_launch_dependents();
 }
 
 // one device staging buffer of moe_layer_forward_host: T x H bf16, 256-byte aligned
@@ -583,6 +598,8 @@ moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int
     MOE_TRY(check_device());
     const void* host_ptrs[3] = {x, residual, out};
     const char* names[3] = {"x", "residual", "out"};
+    const uint16_t* in_dev[2] = {nullptr, nullptr};  // page-locked x / residual, as the device addresses them
+    uint16_t* out_dev = nullptr;                      // page-locked out, as the device addresses it
     for (int i = 0; i < 3; ++i) {
         if (!host_ptrs[i]) continue;
         cudaPointerAttributes at{};
@@ -592,6 +609,9 @@ moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int
         }
         if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
             return fail(MOE_ERR_INVALID_ARG, "%s is device memory; moe_layer_forward_host takes host buffers", names[i]);
+        const bool mapped = at.type == cudaMemoryTypeHost && at.devicePointer && aligned(at.devicePointer, 16);
+        if (mapped && i < 2) in_dev[i] = static_cast<const uint16_t*>(at.devicePointer);
+        if (mapped && i == 2) out_dev = static_cast<uint16_t*>(at.devicePointer);
     }
     if (T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -599,10 +619,23 @@ moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int
     uint16_t* xd = reinterpret_cast<uint16_t*>(base + W.total);
     uint16_t* od = reinterpret_cast<uint16_t*>(base + W.total + stage);
     uint16_t* rd = residual ? reinterpret_cast<uint16_t*>(base + W.total + 2 * stage) : nullptr;
-    MOE_CUDA(cudaMemcpyAsync(xd, x, bytes, cudaMemcpyHostToDevice, s), "copy x to the device");
-    if (rd) MOE_CUDA(cudaMemcpyAsync(rd, residual, bytes, cudaMemcpyHostToDevice, s), "copy residual to the device");
-    MOE_TRY(moe_layer_forward_profiled(L, xd, T, rd, od, ws, W.total, stream, nullptr, 0));
-    MOE_CUDA(cudaMemcpyAsync(out, od, bytes, cudaMemcpyDeviceToHost, s), "copy the result to the host");
+    // page-locked inputs come in through one small kernel reading them over the host link (launched
+    // like the layer's kernels, so the front half's prologue overlaps it); others by copy
+    if (in_dev[0] && (!residual || in_dev[1])) {
+        const int64_t n16 = static_cast<int64_t>(bytes / 16);
+        const int grid = static_cast<int>(std::min<int64_t>((n16 + 255) / 256, 4LL * device_sm_count()));
+        MOE_CUDA(launch_pdl(k_stage_in, dim3(grid), dim3(256), 0, s, reinterpret_cast<const uint4*>(in_dev[0]),
+                            reinterpret_cast<uint4*>(xd), reinterpret_cast<const uint4*>(in_dev[1]),
+                            reinterpret_cast<uint4*>(rd), n16),
+                 "stage the inputs in");
+    } else {
+        MOE_CUDA(cudaMemcpyAsync(xd, x, bytes, cudaMemcpyHostToDevice, s), "copy x to the device");
+        if (rd) MOE_CUDA(cudaMemcpyAsync(rd, residual, bytes, cudaMemcpyHostToDevice, s), "copy residual to the device");
+    }
+    // page-locked output: the combine writes it directly over the host link (no separate copy);
+    // otherwise the result is staged on the device and copied back
+    MOE_TRY(moe_layer_forward_profiled(L, xd, T, rd, out_dev ? out_dev : od, ws, W.total, stream, nullptr, 0));
+    if (!out_dev) MOE_CUDA(cudaMemcpyAsync(out, od, bytes, cudaMemcpyDeviceToHost, s), "copy the result to the host");
     return MOE_OK;
 }
 
