@@ -108,6 +108,17 @@ __global__ void k_stage_in(const uint4* __restrict__ x, uint4* __restrict__ xd, 
     ptx::griddep_launch_dependents();
 }
 
+// The layer's counters for the launches that follow (tensor-max scratch, token-block readiness and
+// the tile counter of the expert GEMMs), zeroed by a kernel rather than memsets so that every launch of
+// the layer overlaps the one before it; the previous launch may still use them until it completes.
+__global__ void k_zero_counters(unsigned* __restrict__ amax_bits, int32_t* __restrict__ ready, int n)
+{
+    ptx::griddep_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *amax_bits = 0u;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) ready[i] = 0;
+    ptx::griddep_launch_dependents();
+}
+
 // one device staging buffer of moe_layer_forward_host: T x H bf16, 256-byte aligned
 size_t host_stage_bytes(int64_t H, int64_t T) { return (static_cast<size_t>(T * H * 2) + 255) & ~size_t(255); }
 
@@ -497,10 +508,11 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         MOE_CUDA(mark(1), "event record");
         MOE_CUDA(mark(2), "event record");
     } else {
-        // the counters the launches below rely on are zeroed first, so no memset sits between two
-        // kernels (each launch overlaps the one before it: programmatic dependent launch)
-        MOE_CUDA(cudaMemsetAsync(&hdr->amax_bits, 0, sizeof(unsigned), s), "clear the tensor-max scratch");
-        MOE_CUDA(cudaMemsetAsync(base + W.ready, 0, static_cast<size_t>(n_ready + 1) * 4, s), "clear ready counters");
+        // the counters the launches below rely on, zeroed first by a kernel (no memset between two
+        // kernels: each launch overlaps the one before it, programmatic dependent launch)
+        MOE_CUDA(launch_pdl(k_zero_counters, dim3((n_ready + 1 + 255) / 256), dim3(256), 0, s, &hdr->amax_bits, P32(W.ready),
+                            n_ready + 1),
+                 "clear the layer's counters");
         // W4A4: quantize the layer input once per token (dynamic tensor scale)
         MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s, true),
                  "quantize");
