@@ -5,8 +5,8 @@
 // from a sequential FP32 sum by rounding only (the top-k decision is unaffected unless two logits lie
 // within that rounding of each other).
 //
-// One CTA per output tile of 128 tokens x 176 router rows (three tiles cover E + 1 = 513), adjacent
-// CTAs share the token block. Warp 0 loads 64-column K-slices of both operands by TMA (128-byte
+// One CTA per output tile of 128 tokens x kN router rows (176: three tiles cover E + 1 = 513; for
+// fewer tokens 96 or 64, so that more CTAs share the work), adjacent CTAs share the token block. Warp 0 loads 64-column K-slices of both operands by TMA (128-byte
 // swizzle) into a 5-deep ring, warp 1 owns tensor memory and issues four K=16 MMAs per slice, warps
 // 2-5 read the accumulator (one TMEM lane quarter each) and store FP32 rows of stride ld.
 #include "kernels.cuh"
@@ -15,10 +15,14 @@ namespace moe {
 
 namespace {
 
-constexpr int kRtM = 128, kRtN = 176, kRtStages = 5;
-constexpr int kRtABytes = kRtM * 128, kRtBBytes = kRtN * 128, kRtStageBytes = kRtABytes + kRtBBytes;
+constexpr int kRtM = 128, kRtStages = 5;
+constexpr int kRtABytes = kRtM * 128;
 constexpr int kRtThreads = 192;
-static_assert(kRtStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
+template <int kN>
+struct RtShape {
+    static constexpr int B_BYTES = kN * 128, STAGE_BYTES = kRtABytes + B_BYTES;
+    static_assert(STAGE_BYTES % 1024 == 0 && kN % 16 == 0 && kN <= 256, "tile shape");
+};
 
 struct RtTail {
     uint64_t full[kRtStages];
@@ -28,12 +32,19 @@ struct RtTail {
     int abort;
 };
 
-constexpr size_t kRtSmem = 1024 + static_cast<size_t>(kRtStages) * kRtStageBytes + sizeof(RtTail);
+template <int kN>
+constexpr size_t rt_smem()
+{
+    return 1024 + static_cast<size_t>(kRtStages) * RtShape<kN>::STAGE_BYTES + sizeof(RtTail);
+}
 
+template <int kN>
 __global__ void __launch_bounds__(kRtThreads, 1)
     k_router_tc(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w, int T, int H,
                 int E, const float* __restrict__ bias, float* __restrict__ logits, int ld, int n_ntiles, int* status)
 {
+    constexpr int kRtN = kN, kRtBBytes = RtShape<kN>::B_BYTES, kRtStageBytes = RtShape<kN>::STAGE_BYTES;
+    (void)kRtBBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     RtTail& st = *reinterpret_cast<RtTail*>(smem + kRtStages * kRtStageBytes);
@@ -151,25 +162,39 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 
 int router_tc_ld(int E) { return (E + 1 + 15) / 16 * 16; }
 
-cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
-                                    float* logits, int ld, int* status, cudaStream_t stream)
+template <int kN>
+static cudaError_t launch_tc(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
+                             float* logits, int ld, int* status, cudaStream_t stream)
 {
-    if (T <= 0) return cudaSuccess;
-    if (H % 64 != 0 || ld % 16 != 0 || ld < E + 1) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kRtSmem));
+        cudaError_t e = cudaFuncSetAttribute(k_router_tc<kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(rt_smem<kN>()));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     CUtensorMap tx, tw;
     if (encode_tmap_2d_bf16(&tx, x, static_cast<uint64_t>(H), static_cast<uint64_t>(T), 64, kRtM) != CUDA_SUCCESS ||
-        encode_tmap_2d_bf16(&tw, w_router, static_cast<uint64_t>(H), static_cast<uint64_t>(E + 1), 64, kRtN) != CUDA_SUCCESS)
+        encode_tmap_2d_bf16(&tw, w_router, static_cast<uint64_t>(H), static_cast<uint64_t>(E + 1), 64, kN) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const int n_ntiles = (E + 1 + kRtN - 1) / kRtN;
+    const int n_ntiles = (E + 1 + kN - 1) / kN;
     const int n_tb = (T + kRtM - 1) / kRtM;
-    return launch_pdl(k_router_tc, dim3(n_tb * n_ntiles), dim3(kRtThreads), kRtSmem, stream, tx, tw, T, H, E, bias, logits,
-                      ld, n_ntiles, status);
+    return launch_pdl(k_router_tc<kN>, dim3(n_tb * n_ntiles), dim3(kRtThreads), rt_smem<kN>(), stream, tx, tw, T, H, E, bias,
+                      logits, ld, n_ntiles, status);
+}
+
+cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
+                                    float* logits, int ld, int* status, cudaStream_t stream)
+{
+    if (T <= 0) return cudaSuccess;
+    if (H % 64 != 0 || ld % 16 != 0 || ld < E + 1) return cudaErrorInvalidValue;
+    // the narrowest tile whose CTAs still fit in one wave (more CTAs share the work, each streaming
+    // less); beyond one wave the widest (a partial second wave costs more: 4096 tokens took 37 us
+    // with 96-row tiles against 29 us with 176)
+    const int n_tb = (T + kRtM - 1) / kRtM, sms = device_sm_count();
+    if (n_tb * ((E + 1 + 63) / 64) <= sms) return launch_tc<64>(x, T, H, E, w_router, bias, logits, ld, status, stream);
+    if (n_tb * ((E + 1 + 95) / 96) <= sms) return launch_tc<96>(x, T, H, E, w_router, bias, logits, ld, status, stream);
+    return launch_tc<176>(x, T, H, E, w_router, bias, logits, ld, status, stream);
 }
 
 }  // namespace moe
