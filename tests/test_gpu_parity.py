@@ -521,5 +521,23 @@ def test_layer_host_rejects_device_pointers(moe):
     assert st != 0 and "device memory" in L.moe_last_error_detail().decode()
 
 
+@pytest.mark.parametrize("T,k,E", [(3, 2, 8), (300, 4, 16)])
+def test_permute_reports_bad_expert_ids(moe, T, k, E):
+    # an id outside [0, E) is dropped on the device and reported through the workspace's status word
+    # (the path a bounded wait that ran out takes as well); the valid ids are still placed stably
+    rng = np.random.default_rng(T)
+    ids = rng.integers(0, E, (T, k)).astype(np.int32)
+    ids[0, 0] = E + 5
+    ids[-1, -1] = -2
+    ws = moe.Workspace(moe.moe_workspace_bytes(128, E, k, 128, T))
+    off, ps, sp, rt = moe.moe_permute(dev(ids), E, ws=ws)
+    with pytest.raises(moe.MoeError, match="outside"):
+        moe.moe_read_device_status(ws=ws)
+    moe.moe_read_device_status(ws=ws)  # reading it cleared it
+    valid = ids[(ids >= 0) & (ids < E)]
+    want = np.concatenate([[0], np.cumsum(np.bincount(valid, minlength=E))])
+    np.testing.assert_array_equal(off.cpu().numpy()[: E + 1], want)
+
+
 def test_device_status_clean(moe):
     moe.moe_read_device_status()
