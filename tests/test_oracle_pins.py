@@ -382,7 +382,7 @@ def _make_layer(orc, rng, T, H, E, k, I):
     return x, w_r, wgu, wd, s_mid
 
 
-def _per_token_layer(orc, x, w_r, k, wgu, wd, s_mid):
+def _per_token_layer(orc, x, w_r, k, wgu, wd, s_mid, bias=None, residual=None):
     """Independent restatement: loop over tokens and their experts, no permutation."""
     T, H = x.shape
     E = w_r.shape[0] - 1
@@ -390,7 +390,9 @@ def _per_token_layer(orc, x, w_r, k, wgu, wd, s_mid):
     xc, xs, Sx = orc.quantize_nvfp4(x)
     X = _np_decode(xc, xs, Sx)
     lg = x.astype(np.float64) @ w_r[:E].astype(np.float64).T
-    out = np.zeros((T, H))
+    if bias is not None:
+        lg = lg + np.asarray(bias, np.float64)[None, :]
+    out = np.zeros((T, H)) if residual is None else residual.astype(np.float64).copy()
     for t in range(T):
         order = sorted(range(E), key=lambda e: (-lg[t, e], e))[:k]
         p = np.exp(lg[t] - lg[t].max())
@@ -429,3 +431,21 @@ def test_layer_sampled_rows_equal_full_call(orc):
     rows = np.array([3, 7, 11])
     sub = orc.layer_forward(x[rows], w_r, 2, wgu, wd, s_mid, x_scale=full["x_scale"])
     np.testing.assert_array_equal(sub["out_f64"], full["out_f64"][rows])
+
+
+def test_layer_bias_and_residual_equal_per_token_restatement(orc):
+    """The workload's logit bias moves selection and weights alike; the residual is added once, in FP64."""
+    T, H, E, k, I = 6, 32, 6, 2, 16
+    rng = np.random.default_rng(33)
+    x, w_r, wgu, wd, s_mid = _make_layer(orc, rng, T, H, E, k, I)
+    bias = -1.1 * np.log(np.arange(E) + 1.0)  # the Zipf workload's bias
+    res = rng.standard_normal((T, H)).astype(np.float32)
+    r = orc.layer_forward(x, w_r, k, wgu, wd, s_mid, bias=bias, residual=res)
+    ref = _per_token_layer(orc, x, w_r, k, wgu, wd, s_mid, bias=bias, residual=res)
+    np.testing.assert_allclose(r["out_f64"], ref, rtol=1e-12, atol=1e-12)
+    # without the bias the selection differs for some token (the bias is not a no-op here)
+    plain = orc.layer_forward(x, w_r, k, wgu, wd, s_mid, residual=res)
+    assert not np.allclose(plain["out_f64"], r["out_f64"])
+    # without the residual the output drops exactly the residual
+    nores = orc.layer_forward(x, w_r, k, wgu, wd, s_mid, bias=bias)
+    np.testing.assert_allclose(r["out_f64"] - nores["out_f64"], res.astype(np.float64), rtol=0, atol=1e-12)
