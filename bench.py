@@ -213,7 +213,8 @@ def launches_per_layer(c):
         return 3  # front half (quantize + route + permute), expert GEMMs, combine
     quant = 1 if T * H // 16 <= 4096 else 2
     perm = 1 if T * k <= 512 else 3
-    return quant + 2 + perm + 1 + 1  # quantize, logits + top-k, permute, expert GEMMs (one launch), combine
+    # the layer's counters zeroed, quantize, logits + top-k, permute, expert GEMMs (one launch), combine
+    return 1 + quant + 2 + perm + 1 + 1
 
 
 def distinct_experts(m, layer, x):
