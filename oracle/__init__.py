@@ -1,6 +1,6 @@
 """CPU oracle of the NVFP4 (W4A4) routed-MoE layer forward -- TEST INFRASTRUCTURE.
 
-Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline and reference legs of ``bench.py`` may import
 this package. It is a plain, slow, FP64-accumulating restatement of the layer (see
 ``moe_oracle.c`` for the definition of every step and the readings taken where the capy-flash
 pages are silent). It shares no code with the GPU library and never calls it.
@@ -11,7 +11,8 @@ Parity status of each function (how it is pinned, in ``tests/test_oracle_pins.py
   permute           -- bijection, stability, offsets = scan(histogram), brute force
   grouped_gemm      -- numpy float64 matmul of the dequantized operands; all-ones closed form
   swiglu / combine  -- closed forms on crafted inputs
-  layer_forward     -- an independent per-token nested-loop layer; k = E and E = 1 special cases
+  layer_forward     -- an independent per-token nested-loop layer; k = E and E = 1 special cases;
+                       with the Zipf logit bias and a residual
 """
 import ctypes
 import os
