@@ -36,6 +36,10 @@
  *   - Scratch comes from a caller workspace of moe_workspace_bytes() bytes (256-byte aligned).
  *     Its first 256 bytes (status word and launch counters) must be zero before its first use;
  *     the calls leave the counters at zero. One workspace serves one stream at a time.
+ *   - An empty batch (T = 0) is valid. moe_route_topk, moe_combine, moe_layer_forward and
+ *     moe_layer_forward_host then return MOE_OK after checking the shape alone: they read and write
+ *     nothing, so their pointers may be NULL. moe_permute still writes its offsets (all zero), and
+ *     moe_layer_forward_profiled given events checks its arguments as for T > 0 and records each event.
  *     Kernels record device-side failures (a bounded wait that ran out) in a status word in the
  *     workspace; moe_read_device_status() synchronises `stream` and returns it.
  *   - Shapes: H and I multiples of 128; 1 <= k <= min(E, 32); 1 <= E <= 1024; T >= 0.

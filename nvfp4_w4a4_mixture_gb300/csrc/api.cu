@@ -324,13 +324,13 @@ moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int3
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     MOE_TRY(check_layer_shape(L->H, L->E, L->k, L->I));
     if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    if (T == 0) return MOE_OK;  // an empty batch: nothing is read or written, the pointers may be NULL
     if (!x || !L->w_router || !topk_ids || !topk_w) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     if (!aligned(x, 16) || !aligned(L->w_router, 16)) return fail(MOE_ERR_MISALIGNED, "x and w_router must be 16-byte aligned");
     const WsLayout W = ws_layout(L->H, L->E, L->k, L->I, T);
     const int ld = router_tc_ld(L->E);
     MOE_TRY(check_ws(ws, ws_bytes, W.logits + static_cast<size_t>(T) * ld * 4));
     MOE_TRY(check_device());
-    if (T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* logits = reinterpret_cast<float*>(static_cast<char*>(ws) + W.logits);
     MOE_CUDA(route_logits(x, T, L, logits, reinterpret_cast<WsHeader*>(ws), s), "router launch");
@@ -443,6 +443,7 @@ moe_status_t moe_combine(const uint16_t* y, const float* topk_w, const float* sh
                          int k, int H, const uint16_t* residual, uint16_t* out, moe_stream_t stream)
 {
     if (T < 0 || k < 1 || k > 32 || H < 8 || H % 8) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d k=%d H=%d", T, k, H);
+    if (T == 0) return MOE_OK;  // an empty batch: nothing is read or written, the pointers may be NULL
     if (!y || !topk_w || !src_perm || !out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     if (!aligned(y, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
         return fail(MOE_ERR_MISALIGNED, "y, out and residual must be 16-byte aligned");
@@ -465,6 +466,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     const int H = L->H, E = L->E, k = L->k, I = L->I;
     MOE_TRY(check_layer_shape(H, E, k, I));
     if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    if (T == 0 && n_events == 0) return MOE_OK;  // an empty batch: nothing is read or written, the pointers may be NULL
     if (!x || !out || !L->w_router || !L->s_mid) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     if (!aligned(x, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)) || !aligned(L->w_router, 16))
         return fail(MOE_ERR_MISALIGNED, "x, out, residual and w_router must be 16-byte aligned");
@@ -474,7 +476,11 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     const WsLayout W = ws_layout(H, E, k, I, T);
     MOE_TRY(check_ws(ws, ws_bytes, W.total));
     MOE_TRY(check_device());
-    if (T == 0) return MOE_OK;
+    if (T == 0) {  // an empty batch with events: each is recorded, so every stage reads zero time
+        for (int i = 0; i < n_events; ++i)
+            MOE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(events[i]), static_cast<cudaStream_t>(stream)), "event record");
+        return MOE_OK;
+    }
 
     char* base = static_cast<char*>(ws);
     WsHeader* hdr = reinterpret_cast<WsHeader*>(base + W.hdr);
@@ -598,6 +604,7 @@ moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int
     if (!L) return fail(MOE_ERR_INVALID_ARG, "layer is NULL");
     MOE_TRY(check_layer_shape(L->H, L->E, L->k, L->I));
     if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    if (T == 0) return MOE_OK;  // an empty batch: nothing is read or written, the pointers may be NULL
     if (!x || !out) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     const size_t bytes = static_cast<size_t>(T) * L->H * 2;
     const char *xb = reinterpret_cast<const char*>(x), *ob = reinterpret_cast<const char*>(out);
@@ -625,7 +632,6 @@ moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int
         if (mapped && i < 2) in_dev[i] = static_cast<const uint16_t*>(at.devicePointer);
         if (mapped && i == 2) out_dev = static_cast<uint16_t*>(at.devicePointer);
     }
-    if (T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     char* base = static_cast<char*>(ws);
     uint16_t* xd = reinterpret_cast<uint16_t*>(base + W.total);

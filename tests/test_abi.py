@@ -166,3 +166,20 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         m.lib()
+
+
+def test_empty_batch_is_a_no_op(L):
+    # T = 0: the shape is checked, nothing is read, written or launched, so NULL buffers are accepted;
+    # a bad shape is still refused
+    import nvfp4_w4a4_mixture_gb300 as m
+
+    p = 0x40000
+    bank = m.NvFp4Bank(p, p, p)
+    good = m.LayerDesc(2048, 512, 10, 768, p, None, bank, bank, p)
+    assert L.moe_layer_forward(ctypes.byref(good), None, 0, None, None, None, 0, None) == 0
+    assert L.moe_layer_forward_host(ctypes.byref(good), None, 0, None, None, None, 0, None) == 0
+    assert L.moe_route_topk(None, 0, ctypes.byref(good), None, None, None, None, None, 0, None) == 0
+    assert L.moe_combine(None, None, None, None, 0, 10, 2048, None, None, None) == 0
+    bad = m.LayerDesc(2050, 512, 10, 768, p, None, bank, bank, p)
+    assert L.moe_layer_forward(ctypes.byref(bad), None, 0, None, None, None, 0, None) == MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_combine(None, None, None, None, 0, 33, 2048, None, None, None) == MOE_ERR_UNSUPPORTED_SHAPE
