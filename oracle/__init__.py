@@ -8,6 +8,7 @@ pages are silent). It shares no code with the GPU library and never calls it.
 Parity status of each function (how it is pinned, in ``tests/test_oracle_pins.py``):
   formats / encode  -- exhaustive closed-form tables, hand-worked blocks (tests/golden), round trips
   router            -- brute-force sort, sum of weights, crafted exact ties, bias invariance
+  route_from_logits -- closed-form softmax weights on crafted logits, ties, the router's own logits
   permute           -- bijection, stability, offsets = scan(histogram), brute force
   grouped_gemm      -- numpy float64 matmul of the dequantized operands; all-ones closed form
   swiglu / combine  -- closed forms on crafted inputs
@@ -51,6 +52,8 @@ def lib():
         L.orc_router.restype = None
         L.orc_router.argtypes = [p, p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_int, p, p, p, p]
+        L.orc_route_from_logits.restype = None
+        L.orc_route_from_logits.argtypes = [p, p, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, p]
         L.orc_permute.restype = ctypes.c_int
         L.orc_permute.argtypes = [p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, p, p, p]
         L.orc_grouped_gemm.restype = None
@@ -150,6 +153,20 @@ def router(x, w_router, k, has_shared=True, bias=None, want_logits=False):
     lib().orc_router(_ptr(x), _ptr(w), _ptr(b), T, H, E, k, int(has_shared), _ptr(ids), _ptr(tw),
                      _ptr(g), _ptr(lg))
     return ids, tw, g, lg
+
+
+def route_from_logits(logits, k, gate_logit=None):
+    """The routing decision on given logits [T][E] (any float dtype, taken as FP64): FP64 softmax
+    over all E, top k by (logit desc, index asc), weights renormalised over the k.
+    Returns (topk_ids int32 [T][k], topk_w float64 [T][k], shared_g float64 [T] or None)."""
+    lg = _c(logits, np.float64)
+    T, E = lg.shape
+    ids = np.zeros((T, k), np.int32)
+    tw = np.zeros((T, k), np.float64)
+    gl = _c(gate_logit, np.float64) if gate_logit is not None else None
+    g = np.zeros(T, np.float64) if gl is not None else None
+    lib().orc_route_from_logits(_ptr(lg), _ptr(gl), T, E, k, _ptr(ids), _ptr(tw), _ptr(g))
+    return ids, tw, g
 
 
 def permute(topk_ids, E, with_shared=True):

@@ -182,26 +182,17 @@ void orc_dequantize_nvfp4(const uint8_t* codes, const uint8_t* sf, float S, int6
 /* Router: logits, FP64 softmax, top-k, renormalised weights, shared gate (R6)                  */
 /* ------------------------------------------------------------------------------------------ */
 
-/* x: [T][H]; w_router: [E + has_shared][H] (the last row is the shared-expert gate when
- * has_shared); bias: nullable [E], added to the routed logits.
- * Outputs: topk_ids [T][k] in routing order, topk_w [T][k], shared_g [T] (if has_shared),
- * logits [T][E] (nullable). */
-void orc_router(const float* x, const float* w_router, const double* bias, int T, int H, int E,
-                int k, int has_shared, int32_t* topk_ids, double* topk_w, double* shared_g,
-                double* logits)
+/* Routing decision from given logits (R6): softmax over all E logits in FP64, the top k by
+ * (logit desc, index asc), their probabilities renormalised to sum 1; the shared gate is the
+ * sigmoid of the gate logit. logits: [T][E]; gate_logit: nullable [T].
+ * Outputs: topk_ids [T][k] in routing order, topk_w [T][k], shared_g [T] (if gate_logit). */
+void orc_route_from_logits(const double* logits, const double* gate_logit, int T, int E, int k,
+                           int32_t* topk_ids, double* topk_w, double* shared_g)
 {
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for schedule(dynamic, 16)
     for (int t = 0; t < T; ++t) {
-        double* l = (double*)malloc(sizeof(double) * (size_t)E);
+        const double* l = logits + (int64_t)t * E;
         unsigned char* taken = (unsigned char*)calloc((size_t)E, 1);
-        const float* xt = x + (int64_t)t * H;
-        for (int e = 0; e < E; ++e) {
-            const float* we = w_router + (int64_t)e * H;
-            double s = 0.0;
-            for (int h = 0; h < H; ++h) s += (double)xt[h] * (double)we[h];
-            l[e] = s + (bias ? bias[e] : 0.0);
-            if (logits) logits[(int64_t)t * E + e] = l[e];
-        }
         /* softmax over all E experts */
         double mx = l[0];
         for (int e = 1; e < E; ++e)
@@ -223,15 +214,40 @@ void orc_router(const float* x, const float* w_router, const double* bias, int T
             psum += p;
         }
         for (int j = 0; j < k; ++j) topk_w[(int64_t)t * k + j] /= psum;
-        if (has_shared) {
-            const float* wg = w_router + (int64_t)E * H;
-            double s = 0.0;
-            for (int h = 0; h < H; ++h) s += (double)xt[h] * (double)wg[h];
-            shared_g[t] = 1.0 / (1.0 + exp(-s));
-        }
-        free(l);
+        if (gate_logit) shared_g[t] = 1.0 / (1.0 + exp(-gate_logit[t]));
         free(taken);
     }
+}
+
+/* x: [T][H]; w_router: [E + has_shared][H] (the last row is the shared-expert gate when
+ * has_shared); bias: nullable [E], added to the routed logits.
+ * Outputs: topk_ids [T][k] in routing order, topk_w [T][k], shared_g [T] (if has_shared),
+ * logits [T][E] (nullable). The logits are FP64 dot products of the bf16 values; the routing
+ * decision is orc_route_from_logits on them. */
+void orc_router(const float* x, const float* w_router, const double* bias, int T, int H, int E,
+                int k, int has_shared, int32_t* topk_ids, double* topk_w, double* shared_g,
+                double* logits)
+{
+    double* l = (double*)malloc(sizeof(double) * (size_t)T * (size_t)E);
+    double* lg = has_shared ? (double*)malloc(sizeof(double) * (size_t)T) : NULL;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+        const float* xt = x + (int64_t)t * H;
+        for (int e = 0; e < E + (has_shared ? 1 : 0); ++e) {
+            const float* we = w_router + (int64_t)e * H;
+            double s = 0.0;
+            for (int h = 0; h < H; ++h) s += (double)xt[h] * (double)we[h];
+            if (e == E) {
+                lg[t] = s;
+            } else {
+                l[(int64_t)t * E + e] = s + (bias ? bias[e] : 0.0);
+                if (logits) logits[(int64_t)t * E + e] = l[(int64_t)t * E + e];
+            }
+        }
+    }
+    orc_route_from_logits(l, lg, T, E, k, topk_ids, topk_w, shared_g);
+    free(l);
+    free(lg);
 }
 
 /* ------------------------------------------------------------------------------------------ */

@@ -256,6 +256,40 @@ def test_router_shared_gate_closed_form(orc):
     assert abs(g[1] - 0.75) < 1e-7  # sigmoid(ln 3) = 3/4 (x rounded to float32)
 
 
+def test_route_from_logits_closed_forms(orc):
+    # logits ln 1 .. ln 4 (+ a far-away fifth): softmax ∝ 1, 2, 3, 4, so the top two are experts 3
+    # then 2 with renormalised weights 4/7 and 3/7 whatever the other terms of the denominator
+    lg = np.log(np.array([[1.0, 2.0, 3.0, 4.0, 1e-9]]))
+    ids, tw, g = orc.route_from_logits(lg, 2, gate_logit=np.array([math.log(3.0)]))
+    assert ids.tolist() == [[3, 2]]
+    np.testing.assert_allclose(tw[0], [4 / 7, 3 / 7], rtol=1e-14)
+    assert abs(g[0] - 0.75) < 1e-15
+    # k = 1: the single weight is exactly 1; exact ties go to the lowest id, in id order
+    ids, tw, g = orc.route_from_logits(np.array([[0.5, 2.0, 2.0, -1.0, 2.0]]), 3)
+    assert ids.tolist() == [[1, 2, 4]] and g is None
+    np.testing.assert_allclose(tw[0], [1 / 3] * 3, rtol=1e-14)
+    ids, tw, _ = orc.route_from_logits(np.array([[7.0, -3.0]]), 1)
+    assert ids.tolist() == [[0]] and tw[0, 0] == 1.0
+
+
+def test_route_from_logits_is_the_routers_decision(orc):
+    # the router's selection and weights are route_from_logits applied to its own logits (a
+    # logit shift by a constant leaves both unchanged: the softmax is shift-invariant)
+    rng = np.random.default_rng(12)
+    T, H, E, k = 6, 40, 9, 4
+    x = rng.standard_normal((T, H)).astype(np.float32)
+    w = (rng.standard_normal((E + 1, H)) * 0.3).astype(np.float32)
+    ids, tw, g, lg = orc.router(x, w, k, want_logits=True)
+    gate = x.astype(np.float64) @ w[E].astype(np.float64)
+    ids2, tw2, g2 = orc.route_from_logits(lg + 5.0, k, gate_logit=gate)
+    assert np.array_equal(ids, ids2)
+    np.testing.assert_allclose(tw2, tw, rtol=1e-12)
+    np.testing.assert_allclose(g2, g, rtol=1e-12)
+    rids, rtw, _ = _numpy_router(x, w, k)
+    assert np.array_equal(ids2, rids)
+    np.testing.assert_allclose(tw2, rtw, rtol=1e-12)
+
+
 # ------------------------------------------------------------------------------------------------
 # permute
 # ------------------------------------------------------------------------------------------------
