@@ -244,12 +244,65 @@ moe_status_t moe_layer_forward_host(const moe_layer_t* L, const uint16_t* x, int
  *   fixed array inside the library (64 tokens x 1025 FP32 = 262,400 bytes of device memory on
  *   every GPU that loads the library, held until the process exits); it allocates nothing.
  *   Limits: T <= 64, E <= 1024; larger calls return MOE_ERR_UNSUPPORTED_SHAPE (use
- *   moe_route_topk). The first call on a device looks up the array's device address (a host-side
- *   set-up step); make that first call before capturing any stream. Every call shares the one
+ *   moe_route_topk). The first call with T > 0 on a device looks up the array's device address (a
+ *   host-side set-up step); make that first call before capturing any stream. The checks run in
+ *   moe_route_topk's order, so an empty batch (T = 0) returns MOE_OK with NULL buffers allowed. Every call shares the one
  *   array: calls that overlap on the GPU (other streams or host threads) race on it.
  * ------------------------------------------------------------------------------------------- */
 moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids,
                                     float* topk_w, float* shared_g, float* logits_out, moe_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_layer_workspace_view -- where moe_layer_forward leaves the layer's intermediate results in
+ *   its workspace, so a caller can inspect them after the call (for example to check each step
+ *   against a reference implementation). The pages have no counterpart; the results themselves
+ *   are the steps listed at the top of this header. Every field is a BYTE OFFSET from the start
+ *   of the workspace, valid for a forward of T tokens through a layer of L's shape on the current
+ *   device, once `stream` has passed that forward and until the next call that uses the workspace:
+ *     x_scale         FP32 scalar: the tensor scale S_x of x
+ *     x_codes, x_sf   NVFP4 x: codes u8 [T][H/2], block scales u8 [T][H/16]
+ *     logits          FP32 [T][logits_ld]: column e < E = the routed logit (bias included),
+ *                     column E = the shared-gate logit
+ *     topk_ids/_w     int32 / FP32 [T][k] in routing order; shared_g FP32 [T]
+ *     expert_offsets  int32 [E+2]; perm_src, src_perm int32 [T*k]; row_token int32 [T*k + T]
+ *                     (as moe_permute) -- only when permutation_in_workspace is 1; for small
+ *                     batches the expert GEMMs build the permutation in on-chip memory instead
+ *                     (permutation_in_workspace 0) and these bytes are not written
+ *     h_codes         the requantised intermediate, u8 [T*k + T][I/2], rows in permuted order
+ *                     (expert groups ascending, the shared expert's T rows last)
+ *     h_sf            its block scales in 512-byte tiles [token block][I/64][512]: the rows of
+ *                     each expert group are cut into blocks of h_block_rows (the last one ragged),
+ *                     numbered across the groups in order; row r of a block, scale column c is
+ *                     byte (r % 32) * 16 + (r / 32) * 4 + c % 4 of tile c / 4
+ *     y               bf16 [T*k + T][H]: the down projection of row (t, j) at row t*k + j (the
+ *                     assignment order), of the shared expert for token t at row T*k + t
+ *   bytes = moe_workspace_bytes(H, E, k, I, T). The view depends on the device (its SM count
+ *   picks the tile schedule), so query it on the device that runs the forward.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+    int64_t bytes;
+    int64_t x_scale, x_codes, x_sf;
+    int64_t logits, logits_ld;
+    int64_t topk_ids, topk_w, shared_g;
+    int64_t permutation_in_workspace, expert_offsets, perm_src, src_perm, row_token;
+    int64_t h_codes, h_sf, h_block_rows;
+    int64_t y;
+} moe_layer_view_t;
+
+moe_status_t moe_layer_workspace_view(const moe_layer_t* L, int T, moe_layer_view_t* view);
+
+/* ---------------------------------------------------------------------------------------------
+ * moe_set_wait_test_hook -- test hook of the failure path (the pages' engine fails one request,
+ *   not the server: capy-flash README v0.7.7, "What's new"). Every device-side wait of the library
+ *   is bounded; this makes one of them run out on purpose, with no fault: the expert GEMMs' wait
+ *   for a token block's intermediate then gives up after wait_limit_us microseconds (0: the
+ *   default, 1 s) and needs ready_extra more completions than exist (0: the real count), so
+ *   with ready_extra > 0 every down tile of moe_layer_forward times out; the launch stops, frees
+ *   its tensor memory and records MOE_ERR_DEVICE_TIMEOUT for moe_read_device_status(). Another
+ *   call with (0, 0) restores normal operation. The values are written into the workspace header
+ *   in stream order (a one-thread kernel on `stream`).
+ * ------------------------------------------------------------------------------------------- */
+moe_status_t moe_set_wait_test_hook(void* ws, unsigned wait_limit_us, int ready_extra, moe_stream_t stream);
 
 /* Workspace bytes for any call above with these sizes (T tokens). */
 size_t moe_workspace_bytes(int H, int E, int k, int I, int T);

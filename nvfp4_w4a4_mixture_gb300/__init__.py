@@ -19,7 +19,8 @@ ENTRY_POINTS = (
     "moe_quantize_nvfp4", "moe_quantize_nvfp4_f32", "moe_route_topk", "moe_permute", "moe_prepack_nvfp4",
     "moe_grouped_gemm_nvfp4", "moe_combine", "moe_layer_forward", "moe_layer_forward_profiled", "moe_workspace_bytes",
     "moe_read_device_status", "moe_status_string", "moe_last_error_detail", "moe_route_topk_noalloc",
-    "moe_layer_forward_host", "moe_workspace_bytes_host",
+    "moe_layer_forward_host", "moe_workspace_bytes_host", "moe_layer_workspace_view",
+    "moe_set_wait_test_hook",
 )
 
 
@@ -37,6 +38,13 @@ class LayerDesc(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int), ("I", ctypes.c_int),
                 ("w_router", ctypes.c_void_p), ("logit_bias", ctypes.c_void_p),
                 ("w_gate_up", NvFp4Bank), ("w_down", NvFp4Bank), ("s_mid", ctypes.c_void_p)]
+
+
+class LayerView(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "bytes", "x_scale", "x_codes", "x_sf", "logits", "logits_ld", "topk_ids", "topk_w", "shared_g",
+        "permutation_in_workspace", "expert_offsets", "perm_src", "src_perm", "row_token", "h_codes", "h_sf",
+        "h_block_rows", "y")]
 
 
 _lib = None
@@ -81,6 +89,10 @@ def lib():
         L.moe_layer_forward.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp]
         L.moe_layer_forward_host.restype = i32
         L.moe_layer_forward_host.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp]
+        L.moe_set_wait_test_hook.restype = i32
+        L.moe_set_wait_test_hook.argtypes = [vp, ctypes.c_uint, i32, vp]
+        L.moe_layer_workspace_view.restype = i32
+        L.moe_layer_workspace_view.argtypes = [ctypes.POINTER(LayerDesc), i32, ctypes.POINTER(LayerView)]
         L.moe_layer_forward_profiled.restype = i32
         L.moe_layer_forward_profiled.argtypes = [ctypes.POINTER(LayerDesc), vp, i32, vp, vp, vp, sz, vp,
                                                  ctypes.POINTER(vp), i32]
@@ -135,6 +147,12 @@ def _ws(nbytes):
         w = Workspace(nbytes)
         _default_ws[dev] = w
     return w
+
+
+def moe_set_wait_test_hook(ws, wait_limit_us, ready_extra):
+    """Test hook: the expert GEMMs' wait for a token block's intermediate gives up after
+    wait_limit_us (0: default) and needs ready_extra more completions (0: none); (0, 0) restores."""
+    _check(lib().moe_set_wait_test_hook(ws.ptr, int(wait_limit_us), int(ready_extra), _stream()))
 
 
 def moe_read_device_status(ws=None):
@@ -291,6 +309,51 @@ def moe_layer_forward_host(layer, x, residual=None, out=None, ws=None):
     ws = ws or _ws(moe_workspace_bytes_host(layer.H, layer.E, layer.k, layer.I, T))
     _check(lib().moe_layer_forward_host(ctypes.byref(layer.desc), _p(x), T, _p(residual), _p(out), ws.ptr, ws.nbytes,
                                         _stream()))
+    return out
+
+
+def moe_layer_workspace_view(layer, T):
+    """The byte offsets of the layer's intermediate results in a forward's workspace (LayerView)."""
+    v = LayerView()
+    _check(lib().moe_layer_workspace_view(ctypes.byref(layer.desc), T, ctypes.byref(v)))
+    return v
+
+
+def layer_intermediates(layer, T, ws):
+    """Views (no copies, no arithmetic) of the intermediate results that the last moe_layer_forward of
+    T tokens left in workspace `ws`, at the offsets moe_layer_workspace_view reports. Read them once
+    the forward's stream has passed it. Keys: x_scale, x_codes, x_sf, logits [T][E+1] (column E: the
+    shared-gate logit), topk_ids, topk_w, shared_g, h_codes, h_sf (tiles), y; with the permutation
+    in the workspace also expert_offsets, perm_src, src_perm, row_token."""
+    v = moe_layer_workspace_view(layer, T)
+    H, E, k, I = layer.H, layer.E, layer.k, layer.I
+    buf = ws.tensor
+    assert buf.numel() >= v.bytes
+
+    def at(off, nbytes, dtype, shape):
+        return buf[off: off + nbytes].view(dtype).reshape(shape)
+
+    P = T * k + T
+    n_blocks_max = (P + v.h_block_rows - 1) // v.h_block_rows + E + 1
+    out = dict(
+        x_scale=at(v.x_scale, 4, torch.float32, (1,)),
+        x_codes=at(v.x_codes, T * H // 2, torch.uint8, (T, H // 2)),
+        x_sf=at(v.x_sf, T * H // 16, torch.uint8, (T, H // 16)),
+        logits=at(v.logits, T * v.logits_ld * 4, torch.float32, (T, v.logits_ld))[:, : E + 1],
+        topk_ids=at(v.topk_ids, T * k * 4, torch.int32, (T, k)),
+        topk_w=at(v.topk_w, T * k * 4, torch.float32, (T, k)),
+        shared_g=at(v.shared_g, T * 4, torch.float32, (T,)),
+        h_codes=at(v.h_codes, P * I // 2, torch.uint8, (P, I // 2)),
+        h_sf=at(v.h_sf, n_blocks_max * (I // 64) * 512, torch.uint8, (n_blocks_max, I // 64, 512)),
+        h_block_rows=int(v.h_block_rows),
+        y=at(v.y, P * H * 2, torch.bfloat16, (P, H)),
+        permutation_in_workspace=bool(v.permutation_in_workspace),
+    )
+    if v.permutation_in_workspace:
+        out.update(expert_offsets=at(v.expert_offsets, (E + 2) * 4, torch.int32, (E + 2,)),
+                   perm_src=at(v.perm_src, T * k * 4, torch.int32, (T * k,)),
+                   src_perm=at(v.src_perm, T * k * 4, torch.int32, (T * k,)),
+                   row_token=at(v.row_token, P * 4, torch.int32, (P,)))
     return out
 
 

@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cstdarg>
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
@@ -117,6 +118,13 @@ __global__ void k_zero_counters(unsigned* __restrict__ amax_bits, int32_t* __res
     if (blockIdx.x == 0 && threadIdx.x == 0) *amax_bits = 0u;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) ready[i] = 0;
     ptx::griddep_launch_dependents();
+}
+
+// moe_set_wait_test_hook: the two test fields of a workspace header, written in stream order
+__global__ void k_set_wait_hook(WsHeader* hdr, unsigned wait_us, int ready_extra)
+{
+    hdr->test_wait_us = wait_us;
+    hdr->test_ready_extra = ready_extra;
 }
 
 // one device staging buffer of moe_layer_forward_host: T x H bf16, 256-byte aligned
@@ -311,6 +319,41 @@ moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, con
 // Router logits into the workspace: tensor cores above kRouterTcMinT tokens (rows router_tc_ld(E)
 // apart), else the CUDA-core kernel with its fixed summation order (rows E + 1 apart).
 constexpr int kRouterTcMinT = 64;
+
+// How moe_layer_forward runs a batch of T tokens: which front half, whether the expert GEMMs
+// build the permutation themselves, their tile schedule and token-block height, and the row
+// stride of the logits it leaves in the workspace.
+struct LayerPlan {
+    bool one_launch_front;  // quantise + route (+ permute) in one launch (small batches)
+    bool gemm_permutes;     // the expert GEMMs rank the ids in shared memory (offsets etc. not stored)
+    int sched;              // GemmSchedule of the expert-GEMM launch
+    int block_rows;         // token rows per block of that schedule (h's scale tiles)
+    int logits_ld;          // floats between two tokens' logits in the workspace
+    int n_ready;            // token-block counters of the expert GEMMs
+};
+
+static LayerPlan layer_plan(int H, int E, int k, int I, int T, int sms)
+{
+    LayerPlan p{};
+    const int64_t P = static_cast<int64_t>(T) * k + T;
+    p.n_ready = static_cast<int>((P + 31) / 32 + E + 1);
+    p.one_launch_front = front_fits(T, H, E, k);
+    // small batches on wide-narrow tiles: the front half stops at the top-k and every CTA of the
+    // expert GEMMs builds the permutation from the ids in its own shared memory (off the front
+    // half's single-CTA tail)
+    p.gemm_permutes = p.one_launch_front && T <= kRouteMaxT && static_cast<int64_t>(T) * k <= kRouteMaxAssign &&
+                      (2 * I) % 256 == 0 && H % 256 == 0 && gemm_permute_enabled();
+    // 256-row weight tiles when H allows (half the MMAs and scale copies per weight byte); else
+    // weights on the MMA's M side for few rows per expert (decode), 128 x 128 tiles otherwise
+    // (token-block units once there are enough of them to keep every SM busy to the end)
+    const bool wide = (2 * I) % 256 == 0 && H % 256 == 0;
+    const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
+    p.sched = wide ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
+                   : small ? kSchedWeightsOnM : kSchedActOnM;
+    p.block_rows = gemm_schedule_rows(p.sched);
+    p.logits_ld = (!p.one_launch_front && T > kRouterTcMinT) ? router_tc_ld(E) : E + 1;
+    return p;
+}
 cudaError_t route_logits(const uint16_t* x, int T, const moe_layer_t* L, float* logits, WsHeader* hdr, cudaStream_t s)
 {
     if (T > kRouterTcMinT)
@@ -494,14 +537,11 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         return n_events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
     };
 
+    const LayerPlan plan = layer_plan(H, E, k, I, T, sms);
     // token-block counters of the expert GEMMs, then their tile counter (all zeroed before the launch)
-    const int n_ready = static_cast<int>((P + 31) / 32 + E + 1);
-    const bool one_launch_front = front_fits(T, H, E, k);
-    // small batches on wide-narrow tiles: the front half stops at the top-k and every CTA of the
-    // expert GEMMs builds the permutation from the ids in its own shared memory (off the front
-    // half's single-CTA tail)
-    const bool gemm_permutes = one_launch_front && T <= kRouteMaxT && static_cast<int64_t>(T) * k <= kRouteMaxAssign &&
-                               (2 * I) % 256 == 0 && H % 256 == 0 && gemm_permute_enabled();
+    const int n_ready = plan.n_ready;
+    const bool one_launch_front = plan.one_launch_front;
+    const bool gemm_permutes = plan.gemm_permutes;
     MOE_CUDA(mark(0), "event record");
     if (one_launch_front) {
         // small batch: quantisation, router, top-k, shared gate and permutation in one launch
@@ -525,7 +565,7 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         MOE_CUDA(mark(1), "event record");
         // router, softmax, top-k, shared gate
         MOE_CUDA(route_logits(x, T, L, PF(W.logits), hdr, s), "router");
-        MOE_CUDA(launch_topk(PF(W.logits), T > kRouterTcMinT ? router_tc_ld(E) : E + 1, T, E, k, P32(W.topk_ids),
+        MOE_CUDA(launch_topk(PF(W.logits), plan.logits_ld, T, E, k, P32(W.topk_ids),
                              PF(W.topk_w), PF(W.shared_g), nullptr, s),
                  "top-k");
         MOE_CUDA(mark(2), "event record");
@@ -575,20 +615,57 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     ga.ready = P32(W.ready);
     ga.tile_counter = P32(W.ready) + n_ready;
     ga.status = &hdr->status;
+    ga.hooks = hdr;
     if (gemm_permutes) ga.route = GemmRoute{P32(W.topk_ids), T, k, E};
-    // 256-row weight tiles when H allows (half the MMAs and scale copies per weight byte); else
-    // weights on the MMA's M side for few rows per expert (decode), 128 x 128 tiles otherwise
-    const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
-    // (token-block units once there are enough of them to keep every SM busy to the end)
-    const int sched = gemm_wide_fits(ga) ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
-                                         : small ? kSchedWeightsOnM : kSchedActOnM;
-    MOE_CUDA(launch_grouped_gemm(ga, P, sched, sms, s), "expert GEMMs");
+    MOE_CUDA(launch_grouped_gemm(ga, P, plan.sched, sms, s), "expert GEMMs");
     MOE_CUDA(mark(4), "event record");
     // weighted combine (+ residual)
     MOE_CUDA(launch_combine(reinterpret_cast<const uint16_t*>(base + W.y), PF(W.topk_w), PF(W.shared_g), nullptr, T, k,
                             H, residual, out, &hdr->status, s),
              "combine");
     MOE_CUDA(mark(5), "event record");
+    return MOE_OK;
+}
+
+moe_status_t moe_set_wait_test_hook(void* ws, unsigned wait_limit_us, int ready_extra, moe_stream_t stream)
+{
+    if (!ws) return fail(MOE_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(MOE_ERR_MISALIGNED, "workspace %p not 256-byte aligned", ws);
+    if (ready_extra < 0) return fail(MOE_ERR_INVALID_ARG, "ready_extra=%d < 0", ready_extra);
+    MOE_TRY(check_device());
+    k_set_wait_hook<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<WsHeader*>(ws), wait_limit_us, ready_extra);
+    MOE_CUDA(cudaGetLastError(), "test hook launch");
+    return MOE_OK;
+}
+
+moe_status_t moe_layer_workspace_view(const moe_layer_t* L, int T, moe_layer_view_t* view)
+{
+    if (!L || !view) return fail(MOE_ERR_INVALID_ARG, "layer or view is NULL");
+    MOE_TRY(check_layer_shape(L->H, L->E, L->k, L->I));
+    if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
+    MOE_TRY(check_device());
+    const WsLayout W = ws_layout(L->H, L->E, L->k, L->I, T);
+    const LayerPlan plan = layer_plan(L->H, L->E, L->k, L->I, T, device_sm_count());
+    moe_layer_view_t v{};
+    v.bytes = static_cast<int64_t>(W.total);
+    v.x_scale = static_cast<int64_t>(W.hdr + offsetof(WsHeader, s_x));
+    v.x_codes = static_cast<int64_t>(W.x_codes);
+    v.x_sf = static_cast<int64_t>(W.x_sf);
+    v.logits = static_cast<int64_t>(W.logits);
+    v.logits_ld = plan.logits_ld;
+    v.topk_ids = static_cast<int64_t>(W.topk_ids);
+    v.topk_w = static_cast<int64_t>(W.topk_w);
+    v.shared_g = static_cast<int64_t>(W.shared_g);
+    v.permutation_in_workspace = plan.gemm_permutes ? 0 : 1;
+    v.expert_offsets = static_cast<int64_t>(W.offsets);
+    v.perm_src = static_cast<int64_t>(W.perm_src);
+    v.src_perm = static_cast<int64_t>(W.src_perm);
+    v.row_token = static_cast<int64_t>(W.row_token);
+    v.h_codes = static_cast<int64_t>(W.h_codes);
+    v.h_sf = static_cast<int64_t>(W.h_sf);
+    v.h_block_rows = plan.block_rows;
+    v.y = static_cast<int64_t>(W.y);
+    *view = v;
     return MOE_OK;
 }
 

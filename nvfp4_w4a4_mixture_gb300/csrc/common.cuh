@@ -25,7 +25,12 @@ struct WsHeader {
     unsigned ticket;       // CTAs of the one-launch front half that finished (zero between calls)
     int gemm_tiles;        // tile counter of a standalone grouped GEMM (cleared before its launch)
     unsigned perm_ticket;  // row-scan CTAs of the permutation that finished (zero between calls)
-    int pad[58];
+    // test hook of the expert GEMMs' wait for a token block's intermediate (both zero in normal
+    // use): a wait limit in microseconds instead of the default, and an amount added to the count
+    // that wait needs, so a test can make the wait run out without any fault
+    unsigned test_wait_us;
+    int test_ready_extra;
+    int pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 

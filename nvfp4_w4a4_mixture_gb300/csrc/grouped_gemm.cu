@@ -328,13 +328,13 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p)
     return v;
 }
 
-// Wait (bounded) until *p >= target; false on timeout.
-__device__ __forceinline__ bool spin_until(const int32_t* p, int target)
+// Wait (bounded by limit_ns) until *p >= target; false on timeout.
+__device__ __forceinline__ bool spin_until(const int32_t* p, int target, uint64_t limit_ns)
 {
     if (ld_acquire(p) >= target) return true;
     const uint64_t t0 = ptx::globaltimer();
     while (ld_acquire(p) < target) {
-        if (ptx::globaltimer() - t0 > ptx::kWaitLimitNs) return false;
+        if (ptx::globaltimer() - t0 > limit_ns) return false;
         __nanosleep(64);
     }
     return true;
@@ -621,6 +621,14 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         };
         const int w2 = warp - 2, pt = tid - 64;
         const int chunk = lane & 7, word = lane & 3;
+        // the wait for a token block's h: default limit, unless a test set the workspace hooks
+        uint64_t ready_limit_ns = ptx::kWaitLimitNs;
+        int ready_extra = 0;
+        if (a.hooks) {
+            const unsigned us = *reinterpret_cast<const volatile unsigned*>(&a.hooks->test_wait_us);
+            ready_extra = *reinterpret_cast<const volatile int*>(&a.hooks->test_ready_extra);
+            if (us) ready_limit_ns = static_cast<uint64_t>(us) * 1000u;
+        }
         const uint8_t* cptr[NCR];
         const uint8_t* sptr[NSR];
         uint32_t cvalid = 0, svalid = 0;
@@ -639,8 +647,8 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 // the down GEMM reads h: wait until every gate/up tile of this token block stored it
                 // (the stages already issued complete on their own meanwhile)
                 if constexpr (LY::PUBLISH) publish_all();
-                const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS);
-                if (!spin_until(a.ready + ti.tbg, target)) { set_abort(st, a.status); break; }
+                const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS) + ready_extra;
+                if (!spin_until(a.ready + ti.tbg, target, ready_limit_ns)) { set_abort(st, a.status); break; }
             }
             // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row (a launch
             // that permutes itself has the gate/up rows in shared memory)
@@ -1140,7 +1148,16 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     ptx::griddep_launch_dependents();  // the next launch may start its prologue on this SM
 }
 
-int gemm_act_rows(bool weights_on_m) { return weights_on_m ? Cfg<kModeSwap>::ACT_ROWS : Cfg<kModeActM>::ACT_ROWS; }
+int gemm_schedule_rows(int schedule)
+{
+    switch (schedule) {
+        case kSchedWeightsOnM: return Cfg<kModeSwap>::ACT_ROWS;
+        case kSchedWide: return Cfg<kModeWide>::ACT_ROWS;
+        case kSchedWideNarrow: return Cfg<kModeWideNarrow>::ACT_ROWS;
+        case kSchedWideRows: return Cfg<kModeWideRows>::ACT_ROWS;
+        default: return Cfg<kModeActM>::ACT_ROWS;
+    }
+}
 
 template <int kMode>
 static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStream_t stream)

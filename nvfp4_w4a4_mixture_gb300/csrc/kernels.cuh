@@ -95,6 +95,7 @@ struct GemmArgs {
     int32_t* ready;           // [token blocks], zeroed before a two-phase launch
     int32_t* tile_counter;    // tiles handed out beyond the first gridDim.x, zeroed before each launch
     int* status;
+    const WsHeader* hooks;    // nullable: the workspace header whose test_* fields the waits read
 };
 constexpr int kGemmMaxG = 1025;
 // Tile schedules: activations on the MMA's M side (128-row token blocks x 128 weight rows),
@@ -107,7 +108,7 @@ bool gemm_wide_fits(const GemmArgs& a);
 // whether a launch of p_max rows is large enough for token-block units (kSchedWideRows)
 bool gemm_rows_pays(int64_t p_max, int sms);
 cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, int sms, cudaStream_t stream);
-int gemm_act_rows(bool weights_on_m);  // token rows per tile of a schedule
+int gemm_schedule_rows(int schedule);  // token rows per block of a (resolved) schedule
 
 // ---- combine.cu
 // status: nullable device status word (the streaming variant records kDevTimeoutCombine there)

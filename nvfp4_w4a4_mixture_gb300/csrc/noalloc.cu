@@ -46,12 +46,18 @@ using namespace moe;
 extern "C" moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids,
                                                float* topk_w, float* shared_g, float* logits_out, moe_stream_t stream)
 {
+    // the checks of moe_route_topk, in its order: the layer's shape, the token count, then an empty
+    // batch returns before anything is read (its pointers may be NULL), then this call's own limit
     if (!L) return noalloc_fail(MOE_ERR_INVALID_ARG, "layer is NULL");
-    if (L->H < 128 || L->H > 8192 || L->H % 128 || L->E < 1 || L->E > kNoallocMaxExperts || L->k < 1 || L->k > 32 ||
-        L->k > L->E)
-        return noalloc_fail(MOE_ERR_UNSUPPORTED_SHAPE, "H, E or k outside the supported range (E <= 1024)");
-    if (T < 0 || T > kNoallocMaxTokens)
-        return noalloc_fail(MOE_ERR_UNSUPPORTED_SHAPE, "T outside [0, 64]: the no-allocation router holds logits for at most 64 tokens");
+    if (L->H < 128 || L->H > 8192 || L->H % 128 || L->I < 128 || L->I > 8192 || L->I % 128 || L->E < 1 ||
+        L->E > kNoallocMaxExperts || L->k < 1 || L->k > 32 || L->k > L->E)
+        return noalloc_fail(MOE_ERR_UNSUPPORTED_SHAPE,
+                            "H, I, E or k outside the supported range (H, I multiples of 128 in [128, 8192]; "
+                            "1 <= k <= min(E, 32); E <= 1024)");
+    if (T < 0) return noalloc_fail(MOE_ERR_UNSUPPORTED_SHAPE, "T < 0");
+    if (T == 0) return MOE_OK;
+    if (T > kNoallocMaxTokens)
+        return noalloc_fail(MOE_ERR_UNSUPPORTED_SHAPE, "T > 64: the no-allocation router holds logits for at most 64 tokens");
     if (!x || !L->w_router || !topk_ids || !topk_w) return noalloc_fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
     if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(L->w_router)) % 16)
         return noalloc_fail(MOE_ERR_MISALIGNED, "x and w_router must be 16-byte aligned");
@@ -78,7 +84,6 @@ extern "C" moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const m
         }
         scratch = g_scratch_ptr[dev];
     }
-    if (T == 0) return MOE_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_router_logits(x, T, L->H, L->E, L->w_router, L->logit_bias, scratch, s) != cudaSuccess ||
         launch_topk(scratch, L->E + 1, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s) != cudaSuccess)

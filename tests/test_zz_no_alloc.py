@@ -2,9 +2,11 @@
 (their device memory belongs to another allocator, or their decode loop cannot afford the device
 synchronisation of a cudaMalloc). It keeps its logits scratch in a fixed array inside the library.
 
-Checked through the C ABI against moe_route_topk (the workspace-based call) on two calls in a row,
-so the second call runs on the array the first one left behind; and the size limit (64 tokens) is
-refused with a clear error. This file is collected last on purpose.
+Checked through the C ABI against moe_route_topk (the workspace-based call) and against the CPU
+oracle's router on calls in a row: 4, then 64, then 7 tokens, so later calls run on the array the
+earlier ones left behind (the last one on an array holding 64 tokens' stale rows); an empty batch
+returns before anything is read; and the size limit (64 tokens) is refused with a clear error.
+This file is collected last on purpose.
 """
 import ctypes
 
@@ -12,7 +14,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from nvfp4_w4a4_mixture_gb300 import workloads as wl
+from tests import inputs as I_
 
 pytestmark = pytest.mark.gpu
 
@@ -52,16 +56,27 @@ def _noalloc(m, layer, x):
     return ids.cpu().numpy(), w.cpu().numpy(), g.cpu().numpy()
 
 
-def test_noalloc_router_matches_workspace_router_twice(moe):
+def test_noalloc_router_matches_workspace_router_and_oracle(moe):
     H, E, k = 2048, 512, 10
     layer = _layer(moe, H, E, k, seed=0)
-    for call, T in enumerate((4, 64)):  # two calls in a row on the shared scratch array
-        x = torch.from_numpy(wl.gen_x(100 + call, T, H)).to(torch.bfloat16).cuda()
+    w_r = wl.gen_router(0, E, H)
+    for call, T in enumerate((4, 64, 7)):  # calls in a row on the shared scratch array
+        x_np, _ = I_.draw_x(100 + call, T, H, w_r, k)  # gap rule: no near-ties at the top-k edge
+        x = torch.from_numpy(x_np).to(torch.bfloat16).cuda()
         ids_ref, w_ref, g_ref, _ = moe.moe_route_topk(x, layer)
         ids, w, g = _noalloc(moe, layer, x)
         np.testing.assert_array_equal(ids, ids_ref.cpu().numpy())
         assert np.max(np.abs(w - w_ref.cpu().numpy())) <= W_TOL
         assert np.max(np.abs(g - g_ref.cpu().numpy())) <= W_TOL
+        ids_orc, _, _, _ = oracle.router(x_np, w_r, k)
+        np.testing.assert_array_equal(ids, ids_orc)
+
+
+def test_noalloc_router_empty_batch(moe):
+    # T = 0: the shape is checked, then nothing is read or written (NULL buffers accepted)
+    layer = _layer(moe, 256, 16, 2, seed=2)
+    rc = moe.lib().moe_route_topk_noalloc(None, 0, ctypes.byref(layer.desc), None, None, None, None, None)
+    assert rc == 0
 
 
 def test_noalloc_router_refuses_more_than_64_tokens(moe):
