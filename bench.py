@@ -1,20 +1,32 @@
 #!/usr/bin/env python3
 """Benchmark of the NVFP4 W4A4 routed-MoE layer forward (tokens/s per layer on one GB300).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config decode|prefill4k|prefill16k|stack48|tiny]
-                    [--impl ours|reference] [--no-graph] [--no-cpu-baseline]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill16k|decode|prefill4k|stack48|tiny]
+                    [--impl ours|reference] [--no-graph] [--no-cpu-baseline] [--no-extra]
 
 A step is one whole layer forward (router, W4A4 quantisation, permutation, gate/up GEMM with fused
 SwiGLU + requantisation, down GEMM, combine) over one batch of synthetic tokens whose inputs are
-resident in HBM. The default workload is the Flash-Next-shaped decode call: hidden 2048, 512
-experts, top-10 + 1 shared, intermediate 768, 4 tokens (an MTP K=3 verify window). L2 is flushed
-before every timed step, outside the timed interval: a 256 MiB write, then a 256 MiB read of a
-second buffer, so the write-back of the flushed lines also happens before the step. Each step is
-timed with CUDA events on the launching stream. The end-to-end figure ("e2e") goes through the
-library's host-buffer call (moe_layer_forward_host: pinned host input, the copy in, the layer and the
-copy out inside the interval; for the layer stack one copy in and one copy out around the layers).
-Under torchrun every rank runs an independent replica (weak scaling: per-GPU work fixed); rank 0
-prints one JSON line.
+resident in HBM. The headline workload (default) is the long prefill chunk: hidden 2048, 512
+experts, top-10 + 1 shared, intermediate 768, 16,384 tokens with 10 % of the experts taking half of
+the assignments -- the largest single-layer configuration. Unless --no-extra is given, the same
+JSON line also carries the 4-token decode call (an MTP K=3 verify window) and the 48-layer stack
+(2,048 tokens, residual add between layers) under the keys "decode" and "stack48", each measured
+the same way with its own steps, roofline and clock record.
+
+L2 is flushed before every timed step, outside the timed interval: a 256 MiB write, then a 256 MiB
+read of a second buffer, so the write-back of the flushed lines also happens before the step. Each
+step is timed with CUDA events on the launching stream. The end-to-end figure ("e2e") goes through
+the library's host-buffer call (moe_layer_forward_host: pinned host input, the copy in, the layer
+and the copy out inside the interval; for the layer stack one copy in and one copy out around the
+layers). Under torchrun every rank runs an independent replica (weak scaling: per-GPU work fixed);
+rank 0 prints one JSON line.
+
+Roofline (per workload): the algorithmic bytes are the routed experts the batch touches plus the
+shared expert (3 H I x 0.5625 + 12 bytes each: E2M1 codes, UE4M3 scales, FP32 scales), the router
+matrix, x in and the output out (and the residual in the stack); the FP4 work is
+2 T (k+1) 3 H I FLOP. Intermediates (x codes, h, y) are reported separately as overhead bytes. The
+bound is whichever of the two times at the measured peaks is longer (HBM copy bandwidth; FP4 dense
+rate = measured bf16 burst x 6, the nominal FP4:BF16 ratio).
 
 --impl reference times the CPU oracle (the plain FP64 reference of the same layer) on the host
 cores, one bounded sample of the workload per step.
@@ -34,7 +46,9 @@ sys.path.insert(0, ROOT)
 from nvfp4_w4a4_mixture_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (NVFP4 W4A4) at 1 GB300; % of FP4-TC / HBM roofline"
-DEFAULT_STEPS = {"tiny": 2000, "decode": 3000, "prefill4k": 300, "prefill16k": 100, "stack48": 10}
+DEFAULT_CONFIG = "prefill16k"
+EXTRA_CONFIGS = ("decode", "stack48")
+DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "prefill4k": 600, "prefill16k": 400, "stack48": 30}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor-core ratio
@@ -46,12 +60,14 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode", choices=sorted(wl.CONFIGS))
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-graph", action="store_true", help="launch the layer directly instead of a CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="measure only --config (no decode / stack48 keys)")
     a = ap.parse_args()
+    a.steps_given = a.steps is not None
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.config]
     a.warmup = max(a.warmup, 3)
@@ -328,19 +344,53 @@ def run_reference(args, c, d):
 
 
 # ------------------------------------------------------------------------------------------------
+# roofline arithmetic (algorithmic work of one layer call)
+# ------------------------------------------------------------------------------------------------
+
+def expert_bytes(H, I):
+    """Bytes of one expert: gate, up and down matrices as E2M1 codes + UE4M3 block scales, 3 FP32 scales."""
+    return 3 * H * I * 9 // 16 + 12
+
+
+def algorithmic_work(c, U):
+    """Per layer call: bytes the method must move (touched routed experts + the shared one, router,
+    x, out, residual in a stack) split into weights / activations, FP4 FLOPs of the expert GEMMs,
+    bf16 FLOPs of the router, and the intermediates' traffic reported as overhead."""
+    H, E, k, I, T = c["H"], c["E"], c["k"], c["I"], c["T"]
+    P = T * (k + 1)
+    weights = (U + 1) * expert_bytes(H, I)
+    router = (E + 1) * H * 2
+    io = T * H * 2 * (3 if c["layers"] > 1 else 2)  # x, out (+ residual)
+    overhead = {"x_codes_written_read": 2 * T * H * 9 // 16, "h_written_read": 2 * P * I * 9 // 16,
+                "y_written_read": 2 * P * H * 2}
+    return {"weights": weights, "router": router, "io": io, "layer_bytes": weights + router + io,
+            "kernel_bytes": weights + io, "flops_fp4": 2.0 * P * 3 * H * I, "flops_bf16": 2.0 * T * H * (E + 1),
+            "overhead_bytes": overhead}
+
+
+def roofline(bytes_, flops, seconds, hbm_gbs, fp4_tflops):
+    """Bound = the longer of the two times at the peaks; achieved and frac against that peak."""
+    t_hbm = bytes_ / (hbm_gbs * 1e9)
+    t_fp4 = flops / (fp4_tflops * 1e12)
+    hbm_ach = bytes_ / seconds / 1e9
+    fp4_ach = flops / seconds / 1e12
+    if t_fp4 > t_hbm:
+        return {"bound": "tensor", "achieved": fp4_ach, "peak": fp4_tflops, "unit": "TFLOP/s",
+                "frac": fp4_ach / fp4_tflops, "hbm_frac": hbm_ach / hbm_gbs, "fp4_tc_frac": fp4_ach / fp4_tflops}
+    return {"bound": "hbm", "achieved": hbm_ach, "peak": hbm_gbs, "unit": "GB/s", "frac": hbm_ach / hbm_gbs,
+            "hbm_frac": hbm_ach / hbm_gbs, "fp4_tc_frac": fp4_ach / fp4_tflops}
+
+
+# ------------------------------------------------------------------------------------------------
 # our arm
 # ------------------------------------------------------------------------------------------------
 
-def run_ours(args, c, d):
+def measure(m, name, K, W, args, d):
+    """One workload: timed steps (CUDA graph replay, L2 flushed before each), per-stage stream events,
+    the end-to-end host-buffer call, roofline. Frees its device memory before returning."""
     import torch
 
-    import nvfp4_w4a4_mixture_gb300 as m
-    from nvfp4_w4a4_mixture_gb300 import build
-
-    if d.local == 0 or not os.path.exists(m.LIB_PATH):
-        build.build()
-    d.barrier()
-    m.lib()
+    c = wl.CONFIGS[name]
     H, E, k, I, T, L = c["H"], c["E"], c["k"], c["I"], c["T"], c["layers"]
     s_mid = s_mid_value(c)
     layers = [make_device_layer(m, c, args.seed + 1000 * d.rank, li, s_mid) for li in range(L)]
@@ -385,7 +435,6 @@ def run_ours(args, c, d):
         run = forward
 
     # ---- timed region: K steps, L2 flushed before each, CUDA events on the launching stream
-    K, W = args.steps, args.warmup
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     with torch.cuda.stream(stream):
         for _ in range(W):
@@ -395,8 +444,7 @@ def run_ours(args, c, d):
     d.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(d.local)
-    t_wall = time.perf_counter()
-    torch.cuda.nvtx.range_push("timed")
+    torch.cuda.nvtx.range_push("timed " + name)
     with torch.cuda.stream(stream):
         for i in range(K):
             flush_l2()
@@ -405,14 +453,12 @@ def run_ours(args, c, d):
             ev[i][1].record(stream)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_pop()
-    t_wall = time.perf_counter() - t_wall
     d.barrier()
     torch.cuda.synchronize()
     clk = clocks.stop()
     m.moe_read_device_status(ws)
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms_local = statistics.mean(step_ms)
-    ms = d.max(ms_local)
+    ms = d.max(statistics.mean(step_ms))
     value = d.world * T / (ms / 1000.0)
 
     # ---- per-stage durations of the same launch sequence (CUDA events at the stage boundaries). A
@@ -428,7 +474,7 @@ def run_ours(args, c, d):
             m.moe_layer_forward_profiled(layers[0], x, st_ev[i], residual=x if L > 1 else None, out=bufs[0], ws=ws)
     torch.cuda.synchronize()
     durs = [[e[j].elapsed_time(e[j + 1]) for e in st_ev] for j in range(len(m.LAYER_STAGES))]
-    stage_us = {name: 1000.0 * statistics.mean(durs[j]) for j, name in enumerate(m.LAYER_STAGES)}
+    stage_us = {sn: 1000.0 * statistics.mean(durs[j]) for j, sn in enumerate(m.LAYER_STAGES)}
     if one_launch_front(c):
         # one launch covers the first three stages: events 1..3 follow it back to back
         stage_us = {"front": sum(stage_us.pop(n) for n in ("quantize", "route", "permute")), **stage_us}
@@ -462,42 +508,37 @@ def run_ours(args, c, d):
     e2e_ms = d.max(statistics.mean(a.elapsed_time(b) for a, b in ee))
     m.moe_read_device_status(ws_h or ws)
 
-    # ---- roofline of the dominant kernel (the expert GEMMs, one launch) and of the whole layer
+    # ---- roofline of the dominant kernel (the expert GEMMs, one launch) and of the whole step
     hbm, bf16_burst, bf16_sus, peak_src = measured_peaks()
-    U = distinct_experts(m, layers[0], x)  # routed experts touched by this batch
-    per_gu = 2 * I * H // 2 + 2 * I * H // 16 + 8
-    per_dn = H * I // 2 + H * I // 16 + 4
-    P = T * k + T
-    # weights of the touched experts + shared expert, x codes read once, h written and read once,
-    # y written once
-    exp_bytes = ((U + 1) * (per_gu + per_dn) + T * H * (1 / 2 + 1 / 16) + 2 * P * I * (1 / 2 + 1 / 16)
-                 + P * H * 2)
-    exp_us = stage_us["experts"]
-    achieved = exp_bytes / (exp_us * 1e-6) / 1e9
-    layer_bytes = L * ((U + 1) * (per_gu + per_dn) + (E + 1) * H * 2 + 2 * T * H * 2 + (T * H * 2 if L > 1 else 0))
-    layer_flops = L * 2.0 * T * (k + 1) * 3 * H * I
     fp4_peak = bf16_burst * FP4_OVER_BF16
+    U = distinct_experts(m, layers[0], x)  # routed experts touched by this batch (first layer)
+    work = algorithmic_work(c, U)
+    exp_us = stage_us["experts"]
+    kern = roofline(work["kernel_bytes"], work["flops_fp4"], exp_us * 1e-6, hbm, fp4_peak)
+    kern.update({
+        "traffic": recorded_traffic("experts/" + name),
+        "kernel": "k_grouped_gemm_nvf4 (gate/up + SwiGLU + NVFP4 requant + down, one launch)",
+        "algorithmic_bytes_per_launch": work["kernel_bytes"],
+        "algorithmic_bytes": "touched routed experts + shared expert (%d x %d B) + x + out%s" % (
+            U + 1, expert_bytes(H, I), " + residual" if L > 1 else ""),
+        "flops_fp4_per_launch": work["flops_fp4"], "overhead_bytes_per_launch": work["overhead_bytes"],
+        "avg_launch_us": exp_us, "timed_by": "stream events around the launch (includes its launch gap)",
+        "peak_source": "%s hbm_gbs; FP4 = %s bf16 burst x %.0f (nominal FP4:BF16)" % (peak_src, peak_src, FP4_OVER_BF16)})
     t_s = ms / 1000.0  # per-replica step time
-    hbm_frac = layer_bytes / t_s / 1e9 / hbm
-    fp4_frac = layer_flops / t_s / 1e12 / fp4_peak
-    line = {
+    step_roof = roofline(L * work["layer_bytes"], L * work["flops_fp4"], t_s, hbm, fp4_peak)
+    step_roof.update({"bytes": L * work["layer_bytes"], "flops_fp4": L * work["flops_fp4"],
+                      "overhead_bytes": {kk: L * v for kk, v in work["overhead_bytes"].items()},
+                      "fp4_peak_tflops": fp4_peak, "hbm_peak_gbs": hbm})
+    res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": d.world, "steps": K, "warmup": W,
-        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4",
-        "data": "synthetic: seeded torch RNG on the device; x ~ N(0,1) bf16, router N(0,0.02) bf16, experts "
-                "N(0,0.02) fp32 quantised to NVFP4 by the library",
-        "config": {"workload": workload_name(c, args.config), "tokens": T, "layers": L,
+        "ms_per_step": ms, "per_layer_us": 1000.0 * ms / L,
+        "config": {"workload": workload_name(c, name), "tokens": T, "layers": L,
                    "distinct_routed_experts": U, "cuda_graph": use_graph,
                    "l2": "flushed before every timed step (256 MiB write, then 256 MiB read of another "
                          "buffer; outside the timed interval)",
                    "parallelism": "replicas" if d.world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "traffic": recorded_traffic("experts/" + args.config),
-                     "kernel": "k_grouped_gemm_nvf4 (gate/up + SwiGLU + NVFP4 requant + down, one launch)",
-                     "algorithmic_bytes_per_launch": exp_bytes, "avg_launch_us": exp_us,
-                     "peak_source": peak_src + " hbm_gbs"},
-        "layer_roofline": {"bytes": layer_bytes, "flops_fp4": layer_flops, "hbm_frac": hbm_frac,
-                           "fp4_tc_frac": fp4_frac, "fp4_peak_tflops": fp4_peak,
-                           "fp4_peak_source": "%s bf16 burst x %.0f (nominal FP4:BF16)" % (peak_src, FP4_OVER_BF16)},
+        "roofline": kern,
+        "layer_roofline": step_roof,
         "stages_us": stage_us,
         "stages_timed_by": "stream events at the stage boundaries, each step queued behind a spin kernel",
         "step_ms_median": statistics.median(step_ms),
@@ -506,6 +547,33 @@ def run_ours(args, c, d):
         "gpu_launches": K * L * launches_per_layer(c),
         "clocks": clk,
     }
+    del layers, run
+    if use_graph:
+        del graph
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, c, d):
+    import nvfp4_w4a4_mixture_gb300 as m
+    from nvfp4_w4a4_mixture_gb300 import build
+
+    if d.local == 0 or not os.path.exists(m.LIB_PATH):
+        build.build()
+    d.barrier()
+    m.lib()
+    head = measure(m, args.config, args.steps, args.warmup, args, d)
+    line = {"metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": d.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "nvfp4",
+            "data": "synthetic: seeded torch RNG on the device; x ~ N(0,1) bf16, router N(0,0.02) bf16, experts "
+                    "N(0,0.02) fp32 quantised to NVFP4 by the library"}
+    line.update({kk: v for kk, v in head.items() if kk not in line and kk != "metric"})
+    if not args.no_extra:
+        for name in EXTRA_CONFIGS:
+            if name != args.config:
+                line[name] = measure(m, name, DEFAULT_STEPS[name], args.warmup, args, d)
     return line
 
 

@@ -135,6 +135,10 @@ moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int3
 
 /* ---------------------------------------------------------------------------------------------
  * moe_permute -- stable counting sort of the T*k assignments f = t*k + j by expert id.
+ *   The layer's step "permute tokens by expert id" between routing and the grouped GEMMs: the
+ *   pages (article "What shipped": 10 routed + 1 shared expert per token) give no order, so this
+ *   library takes the plainest deterministic one -- stable, rows of one expert in ascending f --
+ *   and appends the shared expert as group E with one row per token.
  *   expert_offsets: int32 [E+2]: rows of expert e are [off[e], off[e+1]) (e < E); the shared
  *   expert's group is [off[E], off[E+1]) = [T*k, T*k + T) when with_shared, else empty.
  *   perm_src: int32 [T*k], perm_src[p] = f; src_perm: int32 [T*k], src_perm[f] = p;
@@ -163,6 +167,11 @@ moe_status_t moe_prepack_nvfp4(const uint8_t* codes, const uint8_t* sf, int G, i
 /* ---------------------------------------------------------------------------------------------
  * moe_grouped_gemm_nvfp4 -- block-scaled grouped GEMM on the tcgen05 tensor cores
  *   (kind::mxf4nvf4: E2M1 x E2M1 products, UE4M3 scale per 16 along K, FP32 accumulation in TMEM).
+ *   The expert GEMMs of the layer: NVFP4 weights "as published" with E2M1 codes, UE4M3 block
+ *   scales and an FP32 per-expert scale (article, "What shipped") against NVFP4 activations (W4A4,
+ *   capy-flash README v0.5.4, "What it does"); accumulation in FP32 ("Why it matters"). The block
+ *   length of 16 along K and the SwiGLU + static-scale requantisation of the intermediate are this
+ *   library's readings (the pages print no formula).
  *   For every group g < G and row p in [group_offsets[g], group_offsets[g+1]):
  *     acc[p][n] = sum_k A_hat[src(p)][k] * B_hat[g][n][k],  src(p) = a_row_index ? a_row_index[p] : p
  *   A: codes [*][K/2], sf [*][K/16] (row-major), tensor scale a_scale[a_scale_per_group ? g : 0].
