@@ -96,9 +96,13 @@ enum {
     MOE_GEMM_SCHED_WEIGHTS_ON_M = 0x200, /* 128 weight rows x 32 token rows per tile (small groups) */
     MOE_GEMM_SCHED_WIDE = 0x400,         /* 128 token rows x 256 weight rows per tile (N % 256 == 0,
                                           * else activations on M) */
-    MOE_GEMM_SCHED_WIDE_ROWS = 0x800     /* wide tiles, each CTA taking a whole 128-row token block
+    MOE_GEMM_SCHED_WIDE_ROWS = 0x800,    /* wide tiles, each CTA taking a whole 128-row token block
                                           * through every weight block (the activation scales stay
                                           * in tensor memory); K <= 2048, else wide */
+    MOE_GEMM_SCHED_ROWS_RESIDENT = 0x1000 /* a whole 128-row token block per CTA, its activation rows
+                                          * gathered once into shared memory and its scales kept in
+                                          * tensor memory, 128 weight rows per MMA into two
+                                          * alternating accumulators; K <= 2048, else activations on M */
 };
 
 /* ---------------------------------------------------------------------------------------------

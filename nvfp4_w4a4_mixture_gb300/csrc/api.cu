@@ -348,8 +348,9 @@ static LayerPlan layer_plan(int H, int E, int k, int I, int T, int sms)
     // (token-block units once there are enough of them to keep every SM busy to the end)
     const bool wide = (2 * I) % 256 == 0 && H % 256 == 0;
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
-    p.sched = wide ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
+    p.sched = wide ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedRowsRes : kSchedWide)
                    : small ? kSchedWeightsOnM : kSchedActOnM;
+    if (p.sched == kSchedRowsRes && (H > 2048 || I > 2048)) p.sched = kSchedWideRows;
     p.block_rows = gemm_schedule_rows(p.sched);
     p.logits_ld = (!p.one_launch_front && T > kRouterTcMinT) ? router_tc_ld(E) : E + 1;
     return p;
@@ -434,14 +435,15 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
     if (N < 128 || N % 128 || K < 64 || K % 64 || K > 16384)
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d: N must be a multiple of 128, K of 64 (<= 16384)", N, K);
     if (p_max < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "p_max=%lld < 0", (long long)p_max);
-    constexpr int kSchedBits =
-        MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M | MOE_GEMM_SCHED_WIDE | MOE_GEMM_SCHED_WIDE_ROWS;
+    constexpr int kSchedBits = MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M | MOE_GEMM_SCHED_WIDE |
+                               MOE_GEMM_SCHED_WIDE_ROWS | MOE_GEMM_SCHED_ROWS_RESIDENT;
     const int sched_bits = epilogue & kSchedBits;
     if (sched_bits & (sched_bits - 1)) return fail(MOE_ERR_INVALID_ARG, "epilogue=0x%x: pick one schedule flag", epilogue);
     const int schedule = sched_bits == MOE_GEMM_SCHED_ACT_ON_M      ? kSchedActOnM
                          : sched_bits == MOE_GEMM_SCHED_WEIGHTS_ON_M ? kSchedWeightsOnM
                          : sched_bits == MOE_GEMM_SCHED_WIDE         ? kSchedWide
                          : sched_bits == MOE_GEMM_SCHED_WIDE_ROWS    ? kSchedWideRows
+                         : sched_bits == MOE_GEMM_SCHED_ROWS_RESIDENT ? kSchedRowsRes
                                                                      : kSchedAuto;
     epilogue &= ~kSchedBits;
     if (epilogue < MOE_EPI_F32 || epilogue > MOE_EPI_SWIGLU_NVFP4) return fail(MOE_ERR_INVALID_ARG, "epilogue=%d", epilogue);

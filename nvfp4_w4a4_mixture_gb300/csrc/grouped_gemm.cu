@@ -15,7 +15,11 @@
 //   wide-narrow: wide with 32-row token blocks (decode), the accumulator finished through shared
 //     memory by all epilogue warps; given the routing ids, each CTA builds the permutation itself;
 //   wide, token-block units: a CTA takes a whole token block through every weight block of its
-//     phase, keeping the block's activation scales in tensor memory (large batches).
+//     phase, keeping the block's activation scales in tensor memory;
+//   resident token-block units (large batches): a whole token block per CTA as well, its activation
+//     rows gathered once into shared memory and kept there while 128-row weight blocks stream
+//     past them into a double-buffered 128 x 128 accumulator; the activation scales stay in tensor
+//     memory, so each K-step copies one scale tile (the weights').
 // A launch can hold two problems (phases) over the same groups: the gate/up GEMM with its SwiGLU
 // epilogue, then the down GEMM reading the intermediate h. All phase-0 tiles are handed out before
 // any phase-1 tile. A down tile of token block b waits (bounded) until every gate/up tile of block
@@ -57,20 +61,22 @@ constexpr int kTileRing = 8;               // tiles handed from the weight produ
 
 // Tile shapes. W_ROWS weight rows (one TMA box) by ACT_ROWS activation rows per tile; ACC_BUFS
 // accumulators of ACC_COLS tensor-memory columns.
-enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3, kModeWideRows = 4 };
+enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3, kModeWideRows = 4, kModeRowsRes = 5 };
 template <int kMode>
 struct Cfg;
 template <>
 struct Cfg<kModeActM> {                    // activations on the MMA's M side, 128 weight rows on N
     static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, RES = false;
+    static constexpr int MAX_K = 16384;
 };
 template <>
 struct Cfg<kModeSwap> {                    // weights on the MMA's M side, 32 activation rows on N
     static constexpr int ACT_ROWS = 32, W_ROWS = 128, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 32;
-    static constexpr bool SWAP = true, XCHG = false, ROWS = false;
+    static constexpr bool SWAP = true, XCHG = false, ROWS = false, RES = false;
+    static constexpr int MAX_K = 16384;
 };
 template <>
 struct Cfg<kModeWide> {                    // activations on M, 256 weight rows on N: half the MMAs and
@@ -78,7 +84,8 @@ struct Cfg<kModeWide> {                    // activations on M, 256 weight rows 
     // one buffer only, so the epilogue frees it as soon as its rows are in registers
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, RES = false;
+    static constexpr int MAX_K = 16384;
 };
 
 template <>
@@ -89,7 +96,8 @@ struct Cfg<kModeWideNarrow> {              // wide, for token blocks of at most 
     // finish it; four stages keep the ring as fast as five did
     static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = true, ROWS = false;
+    static constexpr bool SWAP = false, XCHG = true, ROWS = false, RES = false;
+    static constexpr int MAX_K = 16384;
 };
 template <>
 struct Cfg<kModeWideRows> {                // wide tiles taken a whole token block at a time: one CTA runs
@@ -98,8 +106,20 @@ struct Cfg<kModeWideRows> {                // wide tiles taken a whole token blo
                                            // after the first (two scale copies per K-step, not three)
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = true;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = true, RES = false;
     static constexpr int MAX_K = 2048;     // resident activation scales: 4 columns per 64 of K
+};
+template <>
+struct Cfg<kModeRowsRes> {                 // token-block units with the block's activation rows resident
+                                           // in shared memory (gathered once per block, slab by slab:
+                                           // 256 K-values of 128 rows per slab) and its activation
+                                           // scales in tensor memory; 128-row weight blocks stream
+                                           // through the stages into two 128-column accumulators, so
+                                           // the epilogue of one weight block overlaps the next
+    static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
+    static constexpr int MMA_M = 128, MMA_N = 128;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = true, RES = true;
+    static constexpr int MAX_K = 2048;     // activation slabs (8 x 18 KB) and scales (128 columns)
 };
 
 template <int kMode>
@@ -107,13 +127,21 @@ struct Lay {
     using C = Cfg<kMode>;
     static constexpr int WB = C::W_ROWS / 128;  // 128-row weight blocks per tile (scale tiles per K-step)
     static constexpr int W_BYTES = C::W_ROWS * BK_BYTES;
-    static constexpr int ACT_BYTES = C::ACT_ROWS * BK_BYTES;
+    // activation bytes per stage (resident units keep the activations in their own region)
+    static constexpr int ACT_BYTES = C::RES ? 0 : C::ACT_ROWS * BK_BYTES;
     // activation rows first, so an MMA reading MMA_M > ACT_ROWS rows from them stays inside the stage
     static constexpr bool ACT_FIRST = C::ACT_ROWS < C::MMA_M && !C::SWAP;
     static_assert(!ACT_FIRST || (C::MMA_M - C::ACT_ROWS) * BK_BYTES <= W_BYTES, "A rows read past the activations");
     static constexpr int OFF_ACT = ACT_FIRST ? 0 : W_BYTES, OFF_W = ACT_FIRST ? ACT_BYTES : 0;
     static constexpr int OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + WB * SF_STAGE;
-    static constexpr int STAGE_BYTES = OFF_SFACT + SF_STAGE;
+    static constexpr int STAGE_BYTES = OFF_SFACT + (C::RES ? 0 : SF_STAGE);
+    // resident activations (RES): MAX_SLABS slabs of ACT_ROWS x 128 bytes (256 K-values, 128-byte
+    // swizzle, as a stage's activation region) after the stages, then each slab's 4 scale tiles
+    static constexpr int MAX_SLABS = C::RES ? C::MAX_K / 256 : 0;
+    static constexpr int A_SLAB = C::ACT_ROWS * BK_BYTES;
+    static constexpr int A_OFF = C::STAGES * STAGE_BYTES;
+    static constexpr int A_SF_OFF = A_OFF + MAX_SLABS * A_SLAB;
+    static constexpr int TAIL_OFF = A_SF_OFF + MAX_SLABS * SF_STAGE;
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
     static constexpr int SF_COL = C::ACC_BUFS * C::ACC_COLS;  // first scale-factor column
     static constexpr int SFW_STEP_COLS = 4 * WB;               // weight scale columns per K-step
@@ -134,7 +162,8 @@ struct Lay {
     // cp.async-tracked arrivals
     static constexpr bool PUBLISH = C::ACT_ROWS <= 32;
     static_assert(SF_COL + STAGE_SF_COLS * C::STAGES <= TMEM_COLS, "tensor memory budget");
-    static_assert(!C::ROWS || SFA_COL + 4 * (Cfg<kModeWideRows>::MAX_K / 64) <= TMEM_COLS, "resident scales");
+    static_assert(!C::ROWS || SFA_COL + 4 * (C::MAX_K / 64) <= TMEM_COLS, "resident scales");
+    static_assert(A_OFF % 1024 == 0 && A_SLAB % 1024 == 0, "resident slabs keep 1024-byte alignment");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
 
@@ -147,6 +176,8 @@ struct Tail {
     uint64_t drain;
     uint64_t xchg_full;   // weights-on-M SwiGLU: up values written (64 arrivals)
     uint64_t xchg_empty;  // weights-on-M SwiGLU: up values consumed (64 arrivals)
+    uint64_t a_full[8];   // resident activation slab gathered (act producer arrivals)
+    uint64_t a_empty[8];  // resident activation slab no longer read (MMA commit)
     uint64_t tile_full[kTileRing];   // tile index written (1 arrival)
     uint64_t tile_empty[kTileRing];  // tile index read by the act producers, MMA and epilogue warps
     int32_t tile_L[kTileRing];
@@ -178,12 +209,12 @@ struct RouteSmem {
 template <int kMode>
 constexpr size_t smem_bytes()
 {
-    return 1024 + static_cast<size_t>(Cfg<kMode>::STAGES) * Lay<kMode>::STAGE_BYTES + sizeof(Tail<kMode>) +
+    return 1024 + static_cast<size_t>(Lay<kMode>::TAIL_OFF) + sizeof(Tail<kMode>) +
            (Cfg<kMode>::SWAP ? sizeof(SwapXchg) : 0) + (Cfg<kMode>::XCHG ? sizeof(AccXchg) + sizeof(RouteSmem) : 0);
 }
 static_assert(smem_bytes<kModeActM>() <= 232448 && smem_bytes<kModeSwap>() <= 232448 &&
                   smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448 &&
-                  smem_bytes<kModeWideRows>() <= 232448,
+                  smem_bytes<kModeWideRows>() <= 232448 && smem_bytes<kModeRowsRes>() <= 232448,
               "shared memory per CTA (227 KB)");
 
 struct TileInfo {
@@ -397,14 +428,18 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     constexpr int W_ROWS = C::W_ROWS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Tail<kMode>& st = *reinterpret_cast<Tail<kMode>*>(smem + C::STAGES * LY::STAGE_BYTES);
+    Tail<kMode>& st = *reinterpret_cast<Tail<kMode>*>(smem + LY::TAIL_OFF);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
 
     // ---- setup
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            ptx::mbar_init(&st.full[s], 1 + kNumActProducers);
+            ptx::mbar_init(&st.full[s], C::RES ? 1 : 1 + kNumActProducers);
             ptx::mbar_init(&st.empty[s], 1);
+        }
+        for (int i = 0; i < LY::MAX_SLABS; ++i) {
+            ptx::mbar_init(&st.a_full[i], kNumActProducers);
+            ptx::mbar_init(&st.a_empty[i], 1);
         }
         for (int s = 0; s < C::ACC_BUFS; ++s) {
             ptx::mbar_init(&st.acc_full[s], 1);
@@ -433,7 +468,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     RouteSmem* rs = nullptr;
     if constexpr (C::XCHG) {
         if (a.route.topk_ids) {
-            rs = reinterpret_cast<RouteSmem*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kMode>) + sizeof(AccXchg));
+            rs = reinterpret_cast<RouteSmem*>(smem + LY::TAIL_OFF + sizeof(Tail<kMode>) + sizeof(AccXchg));
             int32_t* ids_s = reinterpret_cast<int32_t*>(smem);          // n + 4 (padded to 16 bytes)
             int32_t* sorted_s = ids_s + kRouteMaxAssign + 4;             // n
             const int n = a.route.T * a.route.k;
@@ -513,7 +548,75 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         }
     } else if (warp == 1) {
         // ================================ MMA issuer
-        if (lane == 0) {
+        if constexpr (C::RES) {
+            if (lane == 0) {
+                // Resident units: per weight block, K-stage by K-stage, the weights' scale tile of
+                // each K-step into tensor memory and one 128 x 128 x 64 MMA reading the token block's
+                // slab kt from the resident region. The first weight block of a unit also waits for
+                // each slab's gather and copies its activation scales into tensor memory (kept for
+                // the unit's other weight blocks); the last one commits each slab free once its MMAs
+                // are issued, so the next unit's gather of that slab overlaps the remaining slabs.
+                const uint32_t idesc = ptx::idesc_nvf4(C::MMA_M, C::MMA_N);
+                const uint32_t s0 = ptx::smem_u32(smem);
+                const uint64_t dw0 = ptx::sdesc_sw128(s0 + LY::OFF_W), dsfw0 = ptx::sdesc_sf(s0 + LY::OFF_SFW);
+                const uint64_t da0 = ptx::sdesc_sw128(s0 + LY::A_OFF), dsfa0 = ptx::sdesc_sf(s0 + LY::A_SF_OFF);
+                constexpr uint64_t kStageAdv = LY::STAGE_BYTES >> 4, kOpAdv = 32 >> 4, kSfAdv = SF_TILE >> 4;
+                constexpr uint64_t kSlabAdv = LY::A_SLAB >> 4, kSfSlabAdv = SF_STAGE >> 4;
+                int s = 0;
+                uint32_t ph = 0, lt = 0, aph = 0;  // aph: phase bit of each slab's gather barrier
+                bool ok = true;
+                TileCursor tc;
+                for (;;) {
+                    const int L = tile_take(st, tc, total, true);
+                    if (L >= total || aborted(st)) break;
+                    const int uph = L >= tiles0 ? 1 : 0;
+                    const int kK = a.p[uph].K;
+                    const int kb64 = kK / 64, k_stages = (kK + 255) / 256;
+                    const int nsub = a.p[uph].N / W_ROWS;
+                    for (int sub = 0; ok && sub < nsub; ++sub, ++lt) {
+                        const uint32_t as = lt % C::ACC_BUFS, acc_ph = (lt / C::ACC_BUFS) & 1;
+                        if (!ptx::mbar_wait(&st.acc_empty[as], acc_ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                        ptx::tc_fence_after();
+                        const uint32_t d_tmem = tmem + as * C::ACC_COLS;
+                        uint32_t acc = 0;
+                        for (int kt = 0; kt < k_stages; ++kt) {
+                            if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
+                            if (sub == 0) {
+                                if (!ptx::mbar_wait(&st.a_full[kt], (aph >> kt) & 1u)) { set_abort(st, a.status); ok = false; break; }
+                                aph ^= 1u << kt;
+                                ptx::fence_proxy_async_smem();  // the slab came by cp.async (generic proxy)
+                            }
+                            const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
+                            const uint64_t sa = static_cast<uint64_t>(kt) * kSlabAdv;
+                            const uint32_t tsfw = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS;
+                            const int nk = min(4, kb64 - kt * 4);
+                            auto kstep = [&](int kk) {
+                                const uint32_t tw = tsfw + kk * LY::SFW_STEP_COLS;
+                                const uint32_t tsa = tmem + LY::SFA_COL + (kt * 4 + kk) * 4;
+                                ptx::tmem_cp_32x128b_x4(tw, dsfw0 + so + kk * kSfAdv);
+                                if (sub == 0) ptx::tmem_cp_32x128b_x4(tsa, dsfa0 + kt * kSfSlabAdv + kk * kSfAdv);
+                                ptx::mma_nvf4(d_tmem, da0 + sa + kk * kOpAdv, dw0 + so + kk * kOpAdv, idesc, tsa, tw, acc);
+                                acc = 1;
+                            };
+                            if (nk == 4) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) kstep(kk);
+                            } else {
+                                for (int kk = 0; kk < nk; ++kk) kstep(kk);
+                            }
+                            ptx::tc_commit(&st.empty[s]);
+                            if (sub == nsub - 1) ptx::tc_commit(&st.a_empty[kt]);
+                            if (++s == C::STAGES) { s = 0; ph ^= 1; }
+                        }
+                        if (!ok) break;
+                        ptx::tc_commit(&st.acc_full[as]);
+                    }
+                    if (!ok) break;
+                }
+                ptx::tc_commit(&st.drain);
+                if (!ptx::mbar_wait(&st.drain, 0)) set_abort(st, a.status);
+            }
+        } else if (lane == 0) {
             const uint32_t idesc = ptx::idesc_nvf4(C::MMA_M, C::MMA_N);
             // descriptors of stage 0; stage s adds s * STAGE_BYTES to the start address field and
             // K-step kk adds 32 bytes (operands) or one 512-byte scale tile
@@ -633,7 +736,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         const uint8_t* sptr[NSR];
         uint32_t cvalid = 0, svalid = 0;
         int s = 0;
-        uint32_t ph = 0;
+        uint32_t ph = 0, a_ph = 0;  // a_ph: phase bit of each resident slab's free barrier
         bool ok = true;
         TileCursor tc;
         for (;;) {
@@ -678,12 +781,22 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             }
             const uint8_t* sf_tiles = P.a_sf + static_cast<int64_t>(ti.tbg) * kb64 * SF_TILE;
             // (units: the activation scales go with the first weight block only; the MMA thread
-            // keeps them in tensor memory for the others)
-            for (int sub = 0; ok && sub < n_sub(ti); ++sub)
+            // keeps them in tensor memory for the others. Resident units gather each K-slab once,
+            // into the resident region, when the MMA thread has freed it.)
+            for (int sub = 0; ok && sub < (C::RES ? 1 : n_sub(ti)); ++sub)
             for (int kt = 0; kt < k_stages; ++kt) {
-                if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
-                uint8_t* sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
-                uint8_t* ssf = smem + s * LY::STAGE_BYTES + LY::OFF_SFACT;
+                uint8_t* sact;
+                uint8_t* ssf;
+                if constexpr (C::RES) {
+                    if (!ptx::mbar_wait(&st.a_empty[kt], ((a_ph >> kt) & 1u) ^ 1u)) { set_abort(st, a.status); ok = false; break; }
+                    a_ph ^= 1u << kt;
+                    sact = smem + LY::A_OFF + kt * LY::A_SLAB;
+                    ssf = smem + LY::A_SF_OFF + kt * SF_STAGE;
+                } else {
+                    if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                    sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
+                    ssf = smem + s * LY::STAGE_BYTES + LY::OFF_SFACT;
+                }
                 const bool kin = static_cast<int64_t>(kt) * BK_BYTES + chunk * 16 < a_ld;
 #pragma unroll
                 for (int i = 0; i < NCR; ++i) {
@@ -711,7 +824,10 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : P.a_sf, v);
                     }
                 }
-                if constexpr (LY::PUBLISH) {
+                if constexpr (C::RES) {
+                    ptx::cp_async_arrive_noinc(&st.a_full[kt]);
+                    continue;
+                } else if constexpr (LY::PUBLISH) {
                     ptx::cp_async_commit();
                     ++issued;
                     ptx::cp_async_wait<LAG>();
@@ -737,7 +853,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         // (16 gate and 16 up columns), or 32 output columns. The per-tile loop of the epilogue
         // warps is kept in step by two barriers; the first also ends it for all of them at once.
         static_assert(!kSwap && C::ACT_ROWS == 32 && W_ROWS == 256 && C::EPI_WARPS == 8, "XCHG epilogue shape");
-        AccXchg& xb = *reinterpret_cast<AccXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kMode>));
+        AccXchg& xb = *reinterpret_cast<AccXchg*>(smem + LY::TAIL_OFF + sizeof(Tail<kMode>));
         const int ew = warp - 4;
         const int q = warp & 3;
         uint32_t lt = 0;
@@ -1051,7 +1167,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 const int nv = ti.rows;
                 if (P.epilogue == kEpiSwiGLU) {
                     // interleaved gate/up block: lanes 0..63 gate rows, 64..127 the matching up rows
-                    SwapXchg& xg = *reinterpret_cast<SwapXchg*>(smem + C::STAGES * LY::STAGE_BYTES + sizeof(Tail<kMode>));
+                    SwapXchg& xg = *reinterpret_cast<SwapXchg*>(smem + LY::TAIL_OFF + sizeof(Tail<kMode>));
                     const float sg = sa * sb0, su = sa * sb1;
                     const uint32_t xph = xt & 1;
                     ++xt;
@@ -1155,6 +1271,7 @@ int gemm_schedule_rows(int schedule)
         case kSchedWide: return Cfg<kModeWide>::ACT_ROWS;
         case kSchedWideNarrow: return Cfg<kModeWideNarrow>::ACT_ROWS;
         case kSchedWideRows: return Cfg<kModeWideRows>::ACT_ROWS;
+        case kSchedRowsRes: return Cfg<kModeRowsRes>::ACT_ROWS;
         default: return Cfg<kModeActM>::ACT_ROWS;
     }
 }
@@ -1208,6 +1325,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, 
 {
     if ((schedule == kSchedWide || schedule == kSchedWideNarrow || schedule == kSchedWideRows) && !gemm_wide_fits(a))
         schedule = kSchedActOnM;
+    if (schedule == kSchedRowsRes &&
+        (a.p[0].K > Cfg<kModeRowsRes>::MAX_K || (a.nphase > 1 && a.p[1].K > Cfg<kModeRowsRes>::MAX_K)))
+        schedule = kSchedActOnM;  // the resident region holds K <= 2048
     if (schedule == kSchedAuto) schedule = p_max <= 64 ? kSchedWeightsOnM : kSchedActOnM;
     switch (schedule) {
         case kSchedWeightsOnM: return launch_t<kModeSwap>(a, p_max, sms, stream);
@@ -1217,6 +1337,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, 
             if (a.p[0].K <= Cfg<kModeWideRows>::MAX_K && (a.nphase < 2 || a.p[1].K <= Cfg<kModeWideRows>::MAX_K))
                 return launch_t<kModeWideRows>(a, p_max, sms, stream);
             return launch_t<kModeWide>(a, p_max, sms, stream);
+        case kSchedRowsRes: return launch_t<kModeRowsRes>(a, p_max, sms, stream);
         default: return launch_t<kModeActM>(a, p_max, sms, stream);
     }
 }

@@ -326,12 +326,12 @@ def _gemm_case(seed, counts, H, I, N_kind):
     return dict(offsets=offsets, P=P, ac=ac, asf=asf, sa=sa, a_row=a_row, bc=bc, bs=bs, bsc=bsc, N=N, K=K)
 
 
-SCHEDS = ["act_on_m", "weights_on_m", "wide", "wide_rows"]
+SCHEDS = ["act_on_m", "weights_on_m", "wide", "wide_rows", "rows_resident"]
 
 
 def _sched(moe, name):
     return {"act_on_m": moe.SCHED_ACT_ON_M, "weights_on_m": moe.SCHED_WEIGHTS_ON_M, "wide": moe.SCHED_WIDE,
-            "wide_rows": moe.SCHED_WIDE_ROWS}[name]
+            "wide_rows": moe.SCHED_WIDE_ROWS, "rows_resident": moe.SCHED_ROWS_RESIDENT}[name]
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
