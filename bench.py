@@ -9,9 +9,11 @@ SwiGLU + requantisation, down GEMM, combine) over one batch of synthetic tokens 
 resident in HBM. The headline workload (default) is the long prefill chunk: hidden 2048, 512
 experts, top-10 + 1 shared, intermediate 768, 16,384 tokens with 10 % of the experts taking half of
 the assignments -- the largest single-layer configuration. Unless --no-extra is given, the same
-JSON line also carries the 4-token decode call (an MTP K=3 verify window) and the 48-layer stack
-(2,048 tokens, residual add between layers) under the keys "decode" and "stack48", each measured
-the same way with its own steps, roofline and clock record.
+JSON line also carries the 4-token decode call (an MTP K=3 verify window), the same decode call
+through a 48-layer stack captured in one graph (per-layer start-up and tail overlap across layer
+boundaries), and the 48-layer stack at 2,048 tokens (residual add between layers), under the keys
+"decode", "decode_stack48" and "stack48", each measured the same way with its own steps, roofline
+and clock record.
 
 L2 is flushed before every timed step, outside the timed interval: a 256 MiB write, then a 256 MiB
 read of a second buffer, so the write-back of the flushed lines also happens before the step. Each
@@ -47,8 +49,9 @@ from nvfp4_w4a4_mixture_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "MoE-layer tokens/s (NVFP4 W4A4) at 1 GB300; % of FP4-TC / HBM roofline"
 DEFAULT_CONFIG = "prefill16k"
-EXTRA_CONFIGS = ("decode", "stack48")
-DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "prefill4k": 600, "prefill16k": 400, "stack48": 30}
+EXTRA_CONFIGS = ("decode", "decode_stack48", "stack48")
+DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "prefill4k": 600, "prefill16k": 400, "stack48": 30,
+                 "decode_stack48": 200}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor-core ratio

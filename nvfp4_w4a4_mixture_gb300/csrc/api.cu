@@ -348,9 +348,8 @@ static LayerPlan layer_plan(int H, int E, int k, int I, int T, int sms)
     // (token-block units once there are enough of them to keep every SM busy to the end)
     const bool wide = (2 * I) % 256 == 0 && H % 256 == 0;
     const bool small = static_cast<int64_t>(T) * k <= 16LL * E;
-    p.sched = wide ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedRowsRes : kSchedWide)
+    p.sched = wide ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
                    : small ? kSchedWeightsOnM : kSchedActOnM;
-    if (p.sched == kSchedRowsRes && (H > 2048 || I > 2048)) p.sched = kSchedWideRows;
     p.block_rows = gemm_schedule_rows(p.sched);
     p.logits_ld = (!p.one_launch_front && T > kRouterTcMinT) ? router_tc_ld(E) : E + 1;
     return p;

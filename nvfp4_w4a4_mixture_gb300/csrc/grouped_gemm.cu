@@ -391,6 +391,44 @@ __device__ __forceinline__ bool epi_bar_any(bool pred, int n)
 
 __device__ __forceinline__ void epi_bar(int n) { asm volatile("bar.sync 2, %0;" ::"r"(32 * n) : "memory"); }
 
+// 8 x 8 transpose of 16-byte chunks within each group of 8 lanes (three butterfly exchanges): lane
+// 8g + i holds chunks 0..7 of its own row on entry and chunk i of the group's rows 0..7 on return, so
+// the group can store one row's 128 contiguous bytes per instruction (a warp: 4 rows x 128 bytes,
+// whole sectors) instead of 32 rows x 16 bytes. Every lane of the warp must call it.
+__device__ __forceinline__ void transpose_chunks8(uint4 (&x)[8], int lane)
+{
+#pragma unroll
+    for (int b = 4; b >= 1; b >>= 1) {
+        const bool hi = (lane & b) != 0;
+#pragma unroll
+        for (int c0 = 0; c0 < 8; ++c0) {
+            if (c0 & b) continue;
+            const int c1 = c0 | b;
+            const uint4 snd = hi ? x[c0] : x[c1];
+            uint4 rcv;
+            rcv.x = __shfl_xor_sync(0xFFFFFFFFu, snd.x, b);
+            rcv.y = __shfl_xor_sync(0xFFFFFFFFu, snd.y, b);
+            rcv.z = __shfl_xor_sync(0xFFFFFFFFu, snd.z, b);
+            rcv.w = __shfl_xor_sync(0xFFFFFFFFu, snd.w, b);
+            if (hi) x[c0] = rcv;
+            else x[c1] = rcv;
+        }
+    }
+}
+
+// Store a warp's 32 rows x 128 bytes through transpose_chunks8: chunk c of lane l's row goes to
+// dst(l) + 16 c bytes; rows whose lane has valid == false are skipped.
+__device__ __forceinline__ void store_rows128(uint4 (&x)[8], uint8_t* dst, bool valid, int lane)
+{
+    transpose_chunks8(x, lane);
+    const int g0 = lane & ~7, ci = lane & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint8_t* d = reinterpret_cast<uint8_t*>(__shfl_sync(0xFFFFFFFFu, reinterpret_cast<uintptr_t>(dst), g0 + j));
+        if (__shfl_sync(0xFFFFFFFFu, valid, g0 + j)) *reinterpret_cast<uint4*>(d + ci * 16) = x[j];
+    }
+}
+
 // NVFP4 encoding of the intermediate h (16 values, static tensor scale S): the same rule as the
 // activation quantizer, with the two divisions replaced by multiplications with correctly rounded
 // reciprocals (the requantised intermediate is compared by agreement rate, not bit for bit).
@@ -1116,42 +1154,55 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         }
                     }
                 } else if (any) {
+                    // a round's 64 tile columns are 64 consecutive output columns of one scale (a
+                    // gate/up bank's round lies in its gate or its up half); written 128 bytes per row
+                    // and instruction through an in-warp transpose
+                    static_assert(GPR == 4, "rounds of 64 columns");
 #pragma unroll
                     for (int rd = 0; rd < NR; ++rd) {
                         uint32_t v[GPR][16];
                         load_round(rd, v);
                         if (rd == NR - 1) release();
+                        const int c0 = half * CPW + rd * GPR * 16;  // first tile column of the round
+                        int col;
+                        float sb;
+                        if (P.gate_up) {
+                            const int cc = c0 & 127, upper = cc >= 64;
+                            col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
+                            sb = upper ? sb1 : sb0;
+                        } else {
+                            col = ti.nb * W_ROWS + c0;
+                            sb = sb0;
+                        }
+                        const float sc = sa * sb;
+                        if (P.epilogue == kEpiF32) {
+                            // 64 FP32 = two rows of 128 bytes: chunk c = columns 4c .. 4c + 3
 #pragma unroll
-                        for (int g = 0; g < GPR; ++g) {
-                            const int c0 = half * CPW + (rd * GPR + g) * 16;  // tile column
-                            int col;
-                            float sb;
-                            if (P.gate_up) {
-                                const int cc = c0 & 127, upper = cc >= 64;
-                                col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
-                                sb = upper ? sb1 : sb0;
-                            } else {
-                                col = ti.nb * W_ROWS + c0;
-                                sb = sb0;
-                            }
-                            const float sc = sa * sb;
-                            if (valid) {
-                                if (P.epilogue == kEpiF32) {
-                                    float4* o = reinterpret_cast<float4*>(static_cast<float*>(P.out) + po * P.N + col);
+                            for (int hh = 0; hh < 2; ++hh) {
+                                uint4 x[8];
 #pragma unroll
-                                    for (int j = 0; j < 4; ++j)
-                                        o[j] = make_float4(__uint_as_float(v[g][4 * j]) * sc, __uint_as_float(v[g][4 * j + 1]) * sc,
-                                                           __uint_as_float(v[g][4 * j + 2]) * sc, __uint_as_float(v[g][4 * j + 3]) * sc);
-                                } else {
-                                    uint32_t w[8];
-#pragma unroll
-                                    for (int j = 0; j < 8; ++j)
-                                        w[j] = pack_bf16x2(__uint_as_float(v[g][2 * j]) * sc, __uint_as_float(v[g][2 * j + 1]) * sc);
-                                    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(P.out) + po * P.N + col);
-                                    o[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                                    o[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                                for (int c = 0; c < 8; ++c) {
+                                    const int g = (hh * 32 + 4 * c) >> 4, e = (4 * c) & 15;
+                                    x[c] = make_uint4(__float_as_uint(__uint_as_float(v[g][e]) * sc),
+                                                      __float_as_uint(__uint_as_float(v[g][e + 1]) * sc),
+                                                      __float_as_uint(__uint_as_float(v[g][e + 2]) * sc),
+                                                      __float_as_uint(__uint_as_float(v[g][e + 3]) * sc));
                                 }
+                                store_rows128(x, reinterpret_cast<uint8_t*>(static_cast<float*>(P.out) + po * P.N + col + hh * 32),
+                                              valid, lane);
                             }
+                        } else {
+                            // 64 bf16 = one row of 128 bytes: chunk c = columns 8c .. 8c + 7
+                            uint4 x[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const int g = c >> 1, e = (c & 1) * 8;
+                                x[c] = make_uint4(pack_bf16x2(__uint_as_float(v[g][e]) * sc, __uint_as_float(v[g][e + 1]) * sc),
+                                                  pack_bf16x2(__uint_as_float(v[g][e + 2]) * sc, __uint_as_float(v[g][e + 3]) * sc),
+                                                  pack_bf16x2(__uint_as_float(v[g][e + 4]) * sc, __uint_as_float(v[g][e + 5]) * sc),
+                                                  pack_bf16x2(__uint_as_float(v[g][e + 6]) * sc, __uint_as_float(v[g][e + 7]) * sc));
+                            }
+                            store_rows128(x, reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(P.out) + po * P.N + col), valid, lane);
                         }
                     }
                 } else {

@@ -31,6 +31,8 @@ CONFIGS = {
     "prefill16k": dict(H=2048, E=512, k=10, I=768, T=16384, router="hot", layers=1),
     # 48 MoE-only layers with a residual add between them
     "stack48": dict(H=2048, E=512, k=10, I=768, T=2048, router="uniform", layers=48),
+    # the decode call through the same 48-layer stack: 4 tokens per layer, one graph for all layers
+    "decode_stack48": dict(H=2048, E=512, k=10, I=768, T=4, router="uniform", layers=48),
 }
 
 CALIBRATION_FILE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),

@@ -50,4 +50,4 @@ def test_roofline_picks_the_longer_time():
 
 def test_default_workload_is_the_largest_single_layer_config():
     assert bench.DEFAULT_CONFIG == "prefill16k"
-    assert set(bench.EXTRA_CONFIGS) == {"decode", "stack48"}
+    assert set(bench.EXTRA_CONFIGS) == {"decode", "decode_stack48", "stack48"}
