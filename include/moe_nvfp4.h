@@ -99,9 +99,9 @@ enum {
     MOE_GEMM_SCHED_WIDE_ROWS = 0x800,    /* wide tiles, each CTA taking a whole 128-row token block
                                           * through every weight block (the activation scales stay
                                           * in tensor memory); K <= 2048, else wide */
-    MOE_GEMM_SCHED_ROWS_RESIDENT = 0x1000 /* a whole 128-row token block per CTA, its activation rows
-                                          * gathered once into shared memory and its scales kept in
-                                          * tensor memory, 128 weight rows per MMA into two
+    MOE_GEMM_SCHED_WEIGHTS_RESIDENT = 0x1000 /* one group's 128-row weight block (all of K) kept in shared
+                                          * memory, its scales in tensor memory, while up to 16 of the
+                                          * group's 128-row token blocks stream past it into two
                                           * alternating accumulators; K <= 2048, else activations on M */
 };
 

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libmoe_nvfp4.so")
 
 EPI_F32, EPI_BF16, EPI_SWIGLU_NVFP4 = 0, 1, 2
 SCHED_AUTO, SCHED_ACT_ON_M, SCHED_WEIGHTS_ON_M, SCHED_WIDE, SCHED_WIDE_ROWS = 0, 0x100, 0x200, 0x400, 0x800
-SCHED_ROWS_RESIDENT = 0x1000
+SCHED_WEIGHTS_RESIDENT = 0x1000
 
 ENTRY_POINTS = (
     "moe_quantize_nvfp4", "moe_quantize_nvfp4_f32", "moe_route_topk", "moe_permute", "moe_prepack_nvfp4",

@@ -435,14 +435,14 @@ moe_status_t moe_grouped_gemm_nvfp4(const uint8_t* a_codes, const uint8_t* a_sf,
         return fail(MOE_ERR_UNSUPPORTED_SHAPE, "N=%d K=%d: N must be a multiple of 128, K of 64 (<= 16384)", N, K);
     if (p_max < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "p_max=%lld < 0", (long long)p_max);
     constexpr int kSchedBits = MOE_GEMM_SCHED_ACT_ON_M | MOE_GEMM_SCHED_WEIGHTS_ON_M | MOE_GEMM_SCHED_WIDE |
-                               MOE_GEMM_SCHED_WIDE_ROWS | MOE_GEMM_SCHED_ROWS_RESIDENT;
+                               MOE_GEMM_SCHED_WIDE_ROWS | MOE_GEMM_SCHED_WEIGHTS_RESIDENT;
     const int sched_bits = epilogue & kSchedBits;
     if (sched_bits & (sched_bits - 1)) return fail(MOE_ERR_INVALID_ARG, "epilogue=0x%x: pick one schedule flag", epilogue);
     const int schedule = sched_bits == MOE_GEMM_SCHED_ACT_ON_M      ? kSchedActOnM
                          : sched_bits == MOE_GEMM_SCHED_WEIGHTS_ON_M ? kSchedWeightsOnM
                          : sched_bits == MOE_GEMM_SCHED_WIDE         ? kSchedWide
                          : sched_bits == MOE_GEMM_SCHED_WIDE_ROWS    ? kSchedWideRows
-                         : sched_bits == MOE_GEMM_SCHED_ROWS_RESIDENT ? kSchedRowsRes
+                         : sched_bits == MOE_GEMM_SCHED_WEIGHTS_RESIDENT ? kSchedWeightsResident
                                                                      : kSchedAuto;
     epilogue &= ~kSchedBits;
     if (epilogue < MOE_EPI_F32 || epilogue > MOE_EPI_SWIGLU_NVFP4) return fail(MOE_ERR_INVALID_ARG, "epilogue=%d", epilogue);

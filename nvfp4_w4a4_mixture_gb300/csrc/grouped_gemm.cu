@@ -16,10 +16,11 @@
 //     memory by all epilogue warps; given the routing ids, each CTA builds the permutation itself;
 //   wide, token-block units: a CTA takes a whole token block through every weight block of its
 //     phase, keeping the block's activation scales in tensor memory;
-//   resident token-block units (large batches): a whole token block per CTA as well, its activation
-//     rows gathered once into shared memory and kept there while 128-row weight blocks stream
-//     past them into a double-buffered 128 x 128 accumulator; the activation scales stay in tensor
-//     memory, so each K-step copies one scale tile (the weights').
+//   weight-resident units (large batches): a CTA keeps one expert's 128-row weight block (all of K)
+//     in shared memory and its scales in tensor memory, and streams up to 16 of the expert's token
+//     blocks past it into a double-buffered 128 x 128 accumulator: each weight byte is read from
+//     memory once, the streamed activation rows are L2-resident, and each K-step copies one scale
+//     tile (the activations').
 // A launch can hold two problems (phases) over the same groups: the gate/up GEMM with its SwiGLU
 // epilogue, then the down GEMM reading the intermediate h. All phase-0 tiles are handed out before
 // any phase-1 tile. A down tile of token block b waits (bounded) until every gate/up tile of block
@@ -61,21 +62,21 @@ constexpr int kTileRing = 8;               // tiles handed from the weight produ
 
 // Tile shapes. W_ROWS weight rows (one TMA box) by ACT_ROWS activation rows per tile; ACC_BUFS
 // accumulators of ACC_COLS tensor-memory columns.
-enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3, kModeWideRows = 4, kModeRowsRes = 5 };
+enum : int { kModeActM = 0, kModeSwap = 1, kModeWide = 2, kModeWideNarrow = 3, kModeWideRows = 4, kModeWRes = 5 };
 template <int kMode>
 struct Cfg;
 template <>
 struct Cfg<kModeActM> {                    // activations on the MMA's M side, 128 weight rows on N
     static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false, RES = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = false;
     static constexpr int MAX_K = 16384;
 };
 template <>
 struct Cfg<kModeSwap> {                    // weights on the MMA's M side, 32 activation rows on N
     static constexpr int ACT_ROWS = 32, W_ROWS = 128, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 32;
-    static constexpr bool SWAP = true, XCHG = false, ROWS = false, RES = false;
+    static constexpr bool SWAP = true, XCHG = false, ROWS = false, WRES = false;
     static constexpr int MAX_K = 16384;
 };
 template <>
@@ -84,7 +85,7 @@ struct Cfg<kModeWide> {                    // activations on M, 256 weight rows 
     // one buffer only, so the epilogue frees it as soon as its rows are in registers
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false, RES = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = false;
     static constexpr int MAX_K = 16384;
 };
 
@@ -96,7 +97,7 @@ struct Cfg<kModeWideNarrow> {              // wide, for token blocks of at most 
     // finish it; four stages keep the ring as fast as five did
     static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = true, ROWS = false, RES = false;
+    static constexpr bool SWAP = false, XCHG = true, ROWS = false, WRES = false;
     static constexpr int MAX_K = 16384;
 };
 template <>
@@ -106,50 +107,50 @@ struct Cfg<kModeWideRows> {                // wide tiles taken a whole token blo
                                            // after the first (two scale copies per K-step, not three)
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = true, RES = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = true, WRES = false;
     static constexpr int MAX_K = 2048;     // resident activation scales: 4 columns per 64 of K
 };
 template <>
-struct Cfg<kModeRowsRes> {                 // token-block units with the block's activation rows resident
-                                           // in shared memory (gathered once per block, slab by slab:
-                                           // 256 K-values of 128 rows per slab) and its activation
-                                           // scales in tensor memory; 128-row weight blocks stream
-                                           // through the stages into two 128-column accumulators, so
-                                           // the epilogue of one weight block overlaps the next
-    static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
+struct Cfg<kModeWRes> {                    // weight-resident units: one expert's 128-row weight block in
+                                           // shared memory (8 slabs of 256 K-values) with its scales in
+                                           // tensor memory; up to 16 of the expert's token blocks stream
+                                           // through the stages (activations only) into two 128-column
+                                           // accumulators, so the epilogue of one block overlaps the next
+    static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 3, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = true, RES = true;
-    static constexpr int MAX_K = 2048;     // activation slabs (8 x 18 KB) and scales (128 columns)
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = true;
+    static constexpr int MAX_K = 2048;     // weight slabs (8 x 18 KB) and their scales (128 columns)
 };
 
 template <int kMode>
 struct Lay {
     using C = Cfg<kMode>;
     static constexpr int WB = C::W_ROWS / 128;  // 128-row weight blocks per tile (scale tiles per K-step)
-    static constexpr int W_BYTES = C::W_ROWS * BK_BYTES;
-    // activation bytes per stage (resident units keep the activations in their own region)
-    static constexpr int ACT_BYTES = C::RES ? 0 : C::ACT_ROWS * BK_BYTES;
+    static constexpr int W_BYTES = C::W_ROWS * BK_BYTES;  // one weight K-stage (a TMA box)
+    // weight bytes per stage (weight-resident units keep the weights in their own region)
+    static constexpr int STAGE_W = C::WRES ? 0 : W_BYTES;
+    static constexpr int ACT_BYTES = C::ACT_ROWS * BK_BYTES;
     // activation rows first, so an MMA reading MMA_M > ACT_ROWS rows from them stays inside the stage
     static constexpr bool ACT_FIRST = C::ACT_ROWS < C::MMA_M && !C::SWAP;
     static_assert(!ACT_FIRST || (C::MMA_M - C::ACT_ROWS) * BK_BYTES <= W_BYTES, "A rows read past the activations");
-    static constexpr int OFF_ACT = ACT_FIRST ? 0 : W_BYTES, OFF_W = ACT_FIRST ? ACT_BYTES : 0;
-    static constexpr int OFF_SFW = W_BYTES + ACT_BYTES, OFF_SFACT = OFF_SFW + WB * SF_STAGE;
-    static constexpr int STAGE_BYTES = OFF_SFACT + (C::RES ? 0 : SF_STAGE);
-    // resident activations (RES): MAX_SLABS slabs of ACT_ROWS x 128 bytes (256 K-values, 128-byte
-    // swizzle, as a stage's activation region) after the stages, then each slab's 4 scale tiles
-    static constexpr int MAX_SLABS = C::RES ? C::MAX_K / 256 : 0;
-    static constexpr int A_SLAB = C::ACT_ROWS * BK_BYTES;
-    static constexpr int A_OFF = C::STAGES * STAGE_BYTES;
-    static constexpr int A_SF_OFF = A_OFF + MAX_SLABS * A_SLAB;
-    static constexpr int TAIL_OFF = A_SF_OFF + MAX_SLABS * SF_STAGE;
+    static constexpr int OFF_ACT = ACT_FIRST ? 0 : STAGE_W, OFF_W = ACT_FIRST ? ACT_BYTES : 0;
+    static constexpr int OFF_SFW = STAGE_W + ACT_BYTES, OFF_SFACT = OFF_SFW + (C::WRES ? 0 : WB * SF_STAGE);
+    static constexpr int STAGE_BYTES = OFF_SFACT + SF_STAGE;
+    // resident weights (WRES): MAX_SLABS slabs of W_ROWS x 128 bytes (256 K-values, 128-byte swizzle,
+    // as a stage's weight box) after the stages, then each slab's 4 scale tiles
+    static constexpr int MAX_SLABS = C::WRES ? C::MAX_K / 256 : 0;
+    static constexpr int B_OFF = C::STAGES * STAGE_BYTES;
+    static constexpr int B_SF_OFF = B_OFF + MAX_SLABS * W_BYTES;
+    static constexpr int TAIL_OFF = B_SF_OFF + MAX_SLABS * WB * SF_STAGE;
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
     static constexpr int SF_COL = C::ACC_BUFS * C::ACC_COLS;  // first scale-factor column
     static constexpr int SFW_STEP_COLS = 4 * WB;               // weight scale columns per K-step
     // per stage: 4 K-steps of weight scales, and of activation scales unless they are resident
-    static constexpr int STAGE_SF_COLS = 4 * (SFW_STEP_COLS + (C::ROWS ? 0 : 4));
+    static constexpr int STAGE_SF_COLS = 4 * ((C::WRES ? 0 : SFW_STEP_COLS) + (C::ROWS ? 0 : 4));
     static constexpr int TMEM_COLS = 512;
-    // token-block units (ROWS): the activation scales of the whole K, 4 columns per K-step
-    static constexpr int SFA_COL = SF_COL + STAGE_SF_COLS * C::STAGES;
+    // resident scales of the whole K: the activations' (ROWS, 4 columns per K-step) or the weights'
+    // (WRES, 4 columns per K-step and 128 rows)
+    static constexpr int RES_SF_COL = SF_COL + STAGE_SF_COLS * C::STAGES;
     // epilogue warps that take tiles: with 32-row token blocks on the MMA's M side only lane quarter
     // 0 holds rows, so unless they share the work through shared memory (XCHG) the other quarters'
     // warps stay out (no polling, no arrivals)
@@ -162,8 +163,9 @@ struct Lay {
     // cp.async-tracked arrivals
     static constexpr bool PUBLISH = C::ACT_ROWS <= 32;
     static_assert(SF_COL + STAGE_SF_COLS * C::STAGES <= TMEM_COLS, "tensor memory budget");
-    static_assert(!C::ROWS || SFA_COL + 4 * (C::MAX_K / 64) <= TMEM_COLS, "resident scales");
-    static_assert(A_OFF % 1024 == 0 && A_SLAB % 1024 == 0, "resident slabs keep 1024-byte alignment");
+    static_assert(!(C::ROWS || C::WRES) || RES_SF_COL + 4 * (C::WRES ? WB : 1) * (C::MAX_K / 64) <= TMEM_COLS,
+                  "resident scales");
+    static_assert(B_OFF % 1024 == 0 && W_BYTES % 1024 == 0, "resident slabs keep 1024-byte alignment");
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
 
@@ -176,8 +178,8 @@ struct Tail {
     uint64_t drain;
     uint64_t xchg_full;   // weights-on-M SwiGLU: up values written (64 arrivals)
     uint64_t xchg_empty;  // weights-on-M SwiGLU: up values consumed (64 arrivals)
-    uint64_t a_full[8];   // resident activation slab gathered (act producer arrivals)
-    uint64_t a_empty[8];  // resident activation slab no longer read (MMA commit)
+    uint64_t r_full[8];   // resident weight slab loaded (TMA bytes)
+    uint64_t r_empty[8];  // resident weight slab no longer read (MMA commit)
     uint64_t tile_full[kTileRing];   // tile index written (1 arrival)
     uint64_t tile_empty[kTileRing];  // tile index read by the act producers, MMA and epilogue warps
     int32_t tile_L[kTileRing];
@@ -186,6 +188,7 @@ struct Tail {
     int32_t wsum[32];
     int32_t tb_off[kGemmMaxG + 1];
     int32_t g_off[kGemmMaxG + 1];  // the group offsets, so a tile's rows need no global load
+    int32_t ur_off[Cfg<kMode>::WRES ? kGemmMaxG + 1 : 1];  // weight-resident units: runs before group order s
 };
 
 // up-projection values handed from TMEM lanes 64..127 to lanes 0..63 (weights-on-M SwiGLU)
@@ -214,11 +217,12 @@ constexpr size_t smem_bytes()
 }
 static_assert(smem_bytes<kModeActM>() <= 232448 && smem_bytes<kModeSwap>() <= 232448 &&
                   smem_bytes<kModeWide>() <= 232448 && smem_bytes<kModeWideNarrow>() <= 232448 &&
-                  smem_bytes<kModeWideRows>() <= 232448 && smem_bytes<kModeRowsRes>() <= 232448,
+                  smem_bytes<kModeWideRows>() <= 232448 && smem_bytes<kModeWRes>() <= 232448,
               "shared memory per CTA (227 KB)");
 
 struct TileInfo {
     int ph, g, nb, tbg, row0, rows;
+    int nbk;  // token blocks of a weight-resident unit (from tbg / row0 on), else 1
 };
 
 // tb_off[g] = sum_{g' < g} ceil(rows_g' / act_rows), g = 0..G (block-wide scan; contains barriers),
@@ -291,7 +295,41 @@ __device__ __forceinline__ TileInfo tile_info(const int32_t* tb_off, const int32
     const int n_wb = a.p[ti.ph].N / w_rows;
     ti.tbg = Lp / n_wb;
     ti.nb = Lp - ti.tbg * n_wb;
+    ti.nbk = 1;
     place_block(tb_off, g_off, a, act_rows, ti);
+    return ti;
+}
+
+// Weight-resident units: the groups are taken in the order G - 1 (the largest one in a layer: the
+// shared expert, one row per token), 0, 1, ..., G - 2, and each group's token blocks in runs of at
+// most kWresRun; ur_off[s] counts the runs of the groups before order position s.
+constexpr int kWresRun = 16;
+__device__ __forceinline__ int wres_group(int s, int G) { return s == 0 ? G - 1 : s - 1; }
+
+// Work unit L of a weight-resident launch: phase-0 units first, then phase 1; within a phase the
+// runs in group order, each run's 128-row weight blocks fastest (CTAs working at the same time
+// stream the same activation rows from L2).
+__device__ __forceinline__ TileInfo wres_unit_info(const int32_t* tb_off, const int32_t* g_off, const int32_t* ur_off,
+                                                   const GemmArgs& a, int units0, int L)
+{
+    TileInfo ti;
+    ti.ph = L >= units0 ? 1 : 0;
+    const int Lp = L - (ti.ph ? units0 : 0);
+    const int n_wb = a.p[ti.ph].N / 128;
+    const int ur = Lp / n_wb;
+    ti.nb = Lp - ur * n_wb;
+    int lo = 0, hi = a.G;  // the last order position whose runs start at or before ur
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ur_off[mid] <= ur) lo = mid; else hi = mid;
+    }
+    const int g = wres_group(lo, a.G);
+    const int b0 = (ur - ur_off[lo]) * kWresRun;
+    ti.g = g;
+    ti.nbk = min(kWresRun, tb_off[g + 1] - tb_off[g] - b0);
+    ti.tbg = tb_off[g] + b0;
+    ti.row0 = g_off[g] + b0 * 128;
+    ti.rows = min(128, g_off[g + 1] - ti.row0);
     return ti;
 }
 
@@ -304,6 +342,7 @@ __device__ __forceinline__ TileInfo unit_info(const int32_t* tb_off, const int32
     ti.ph = L >= units0 ? 1 : 0;
     ti.tbg = L - (ti.ph ? units0 : 0);
     ti.nb = 0;
+    ti.nbk = 1;
     place_block(tb_off, g_off, a, act_rows, ti);
     return ti;
 }
@@ -472,12 +511,12 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     // ---- setup
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            ptx::mbar_init(&st.full[s], C::RES ? 1 : 1 + kNumActProducers);
+            ptx::mbar_init(&st.full[s], C::WRES ? kNumActProducers : 1 + kNumActProducers);
             ptx::mbar_init(&st.empty[s], 1);
         }
         for (int i = 0; i < LY::MAX_SLABS; ++i) {
-            ptx::mbar_init(&st.a_full[i], kNumActProducers);
-            ptx::mbar_init(&st.a_empty[i], 1);
+            ptx::mbar_init(&st.r_full[i], 1);
+            ptx::mbar_init(&st.r_empty[i], 1);
         }
         for (int s = 0; s < C::ACC_BUFS; ++s) {
             ptx::mbar_init(&st.acc_full[s], 1);
@@ -523,23 +562,63 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = st.tmem_base;
 
+    if constexpr (C::WRES) {
+        // runs of at most kWresRun token blocks per group, counted in the units' group order
+        if (warp == 0) {
+            const int per = (a.G + 31) / 32;
+            const int s_lo = min(a.G, lane * per), s_hi = min(a.G, s_lo + per);
+            int32_t sum = 0;
+            for (int q = s_lo; q < s_hi; ++q) {
+                const int g = wres_group(q, a.G);
+                sum += (st.tb_off[g + 1] - st.tb_off[g] + kWresRun - 1) / kWresRun;
+            }
+            int32_t x = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o) x += y;
+            }
+            int32_t run = x - sum;
+            for (int q = s_lo; q < s_hi; ++q) {
+                st.ur_off[q] = run;
+                const int g = wres_group(q, a.G);
+                run += (st.tb_off[g + 1] - st.tb_off[g] + kWresRun - 1) / kWresRun;
+            }
+            if (lane == 31) st.ur_off[a.G] = x;
+        }
+        __syncthreads();
+    }
     const int nblk = st.tb_off[a.G];
-    // the launch's work items: tiles (token block x weight block), or with ROWS whole token blocks
-    // ("units"), each taken through every weight block of its phase
-    const int tiles0 = C::ROWS ? nblk : nblk * (a.p[0].N / W_ROWS);
-    const int total = tiles0 + (a.nphase > 1 ? (C::ROWS ? nblk : nblk * (a.p[1].N / W_ROWS)) : 0);
+    // the launch's work items: tiles (token block x weight block), with ROWS whole token blocks
+    // ("units", each taken through every weight block of its phase), with WRES runs of token blocks
+    // of one group taken through one weight block
+    const int nrun = C::WRES ? st.ur_off[C::WRES ? a.G : 0] : 0;
+    const int tiles0 = C::ROWS ? nblk : (C::WRES ? nrun : nblk) * (a.p[0].N / W_ROWS);
+    const int total = tiles0 + (a.nphase > 1 ? (C::ROWS ? nblk : (C::WRES ? nrun : nblk) * (a.p[1].N / W_ROWS)) : 0);
     auto tile_at = [&](int L) -> TileInfo {
         if constexpr (C::ROWS) return unit_info(st.tb_off, st.g_off, a, C::ACT_ROWS, tiles0, L);
+        else if constexpr (C::WRES) return wres_unit_info(st.tb_off, st.g_off, st.ur_off, a, tiles0, L);
         else return tile_info(st.tb_off, st.g_off, a, C::ACT_ROWS, W_ROWS, tiles0, L);
     };
-    // weight blocks a work item runs through
-    auto n_sub = [&](const TileInfo& t) { return C::ROWS ? a.p[t.ph].N / W_ROWS : 1; };
+    // the tiles a work item runs through: weight blocks (ROWS), token blocks (WRES)
+    auto n_sub = [&](const TileInfo& t) { return C::ROWS ? a.p[t.ph].N / W_ROWS : t.nbk; };
+    // tile sub of work item t (WRES: the sub-th token block of the run)
+    auto sub_tile = [&](const TileInfo& t, int sub) {
+        TileInfo ti = t;
+        if constexpr (C::ROWS) ti.nb = sub;
+        if constexpr (C::WRES) {
+            ti.tbg = t.tbg + sub;
+            ti.row0 = t.row0 + sub * C::ACT_ROWS;
+            ti.rows = min(C::ACT_ROWS, st.g_off[t.g + 1] - ti.row0);
+        }
+        return ti;
+    };
 
     if (warp == 0) {
         // ================================ weight producer
         if (lane == 0) {
             int s = 0;
-            uint32_t ph = 0;
+            uint32_t ph = 0, rph = 0;  // rph: phase bit of each resident slab's free barrier
             bool ok = true;
             // tiles in the order the CTAs come for them (phase-0 tiles first): a CTA whose tiles
             // run short takes more, and the down tiles go out in the order their inputs complete
@@ -562,6 +641,23 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 const GemmProblem& P = a.p[ti.ph];
                 const CUtensorMap* tm = ti.ph ? &tmap_w1 : &tmap_w0;
                 const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256, n_blk = P.N / 128;
+                if constexpr (C::WRES) {
+                    // the unit's weight block, slab by slab, into the resident region as the last
+                    // token block of the previous unit frees each slab
+                    const uint8_t* sf_src = P.b_sf + ((static_cast<int64_t>(ti.g) * n_blk + ti.nb) * kb64) * SF_TILE;
+                    for (int kt = 0; kt < k_stages; ++kt) {
+                        if (!ptx::mbar_wait(&st.r_empty[kt], ((rph >> kt) & 1u) ^ 1u)) { set_abort(st, a.status); ok = false; break; }
+                        rph ^= 1u << kt;
+                        const int nat = min(4, kb64 - kt * 4);
+                        ptx::mbar_arrive_expect_tx(&st.r_full[kt], LY::W_BYTES + nat * SF_TILE);
+                        ptx::tma_load_3d(smem + LY::B_OFF + kt * LY::W_BYTES, tm, &st.r_full[kt], 0, ti.nb * W_ROWS,
+                                         ti.g * k_stages + kt);
+                        ptx::bulk_load(smem + LY::B_SF_OFF + kt * SF_STAGE, sf_src + static_cast<int64_t>(kt) * 4 * SF_TILE,
+                                       nat * SF_TILE, &st.r_full[kt]);
+                    }
+                    L = L_next;
+                    continue;
+                }
                 for (int sub = 0; ok && sub < n_sub(ti); ++sub) {
                     const int nb = C::ROWS ? sub : ti.nb;
                     // scale tiles of the tile's 128-row weight blocks: [G][N/128][K/64][512 bytes]
@@ -586,31 +682,31 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         }
     } else if (warp == 1) {
         // ================================ MMA issuer
-        if constexpr (C::RES) {
+        if constexpr (C::WRES) {
             if (lane == 0) {
-                // Resident units: per weight block, K-stage by K-stage, the weights' scale tile of
-                // each K-step into tensor memory and one 128 x 128 x 64 MMA reading the token block's
-                // slab kt from the resident region. The first weight block of a unit also waits for
-                // each slab's gather and copies its activation scales into tensor memory (kept for
-                // the unit's other weight blocks); the last one commits each slab free once its MMAs
-                // are issued, so the next unit's gather of that slab overlaps the remaining slabs.
+                // Weight-resident units: per token block of the run, K-stage by K-stage, the
+                // activations' scale tile of each K-step into tensor memory and one 128 x 128 x 64 MMA
+                // of the stage's activation rows against the resident slab kt. The first token block
+                // also waits for each weight slab and copies its scales into tensor memory (kept for
+                // the run's other blocks); the last one commits each slab free once its MMAs are
+                // issued, so the next unit's load of that slab overlaps the remaining slabs.
                 const uint32_t idesc = ptx::idesc_nvf4(C::MMA_M, C::MMA_N);
                 const uint32_t s0 = ptx::smem_u32(smem);
-                const uint64_t dw0 = ptx::sdesc_sw128(s0 + LY::OFF_W), dsfw0 = ptx::sdesc_sf(s0 + LY::OFF_SFW);
-                const uint64_t da0 = ptx::sdesc_sw128(s0 + LY::A_OFF), dsfa0 = ptx::sdesc_sf(s0 + LY::A_SF_OFF);
+                const uint64_t dact0 = ptx::sdesc_sw128(s0 + LY::OFF_ACT), dsfa0 = ptx::sdesc_sf(s0 + LY::OFF_SFACT);
+                const uint64_t dw0 = ptx::sdesc_sw128(s0 + LY::B_OFF), dsfw0 = ptx::sdesc_sf(s0 + LY::B_SF_OFF);
                 constexpr uint64_t kStageAdv = LY::STAGE_BYTES >> 4, kOpAdv = 32 >> 4, kSfAdv = SF_TILE >> 4;
-                constexpr uint64_t kSlabAdv = LY::A_SLAB >> 4, kSfSlabAdv = SF_STAGE >> 4;
+                constexpr uint64_t kSlabAdv = LY::W_BYTES >> 4, kSfSlabAdv = SF_STAGE >> 4;
                 int s = 0;
-                uint32_t ph = 0, lt = 0, aph = 0;  // aph: phase bit of each slab's gather barrier
+                uint32_t ph = 0, lt = 0, rph = 0;  // rph: phase bit of each slab's load barrier
                 bool ok = true;
                 TileCursor tc;
                 for (;;) {
                     const int L = tile_take(st, tc, total, true);
                     if (L >= total || aborted(st)) break;
-                    const int uph = L >= tiles0 ? 1 : 0;
-                    const int kK = a.p[uph].K;
+                    const TileInfo tu = tile_at(L);
+                    const int kK = a.p[tu.ph].K;
                     const int kb64 = kK / 64, k_stages = (kK + 255) / 256;
-                    const int nsub = a.p[uph].N / W_ROWS;
+                    const int nsub = tu.nbk;
                     for (int sub = 0; ok && sub < nsub; ++sub, ++lt) {
                         const uint32_t as = lt % C::ACC_BUFS, acc_ph = (lt / C::ACC_BUFS) & 1;
                         if (!ptx::mbar_wait(&st.acc_empty[as], acc_ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
@@ -619,21 +715,21 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         uint32_t acc = 0;
                         for (int kt = 0; kt < k_stages; ++kt) {
                             if (!ptx::mbar_wait(&st.full[s], ph)) { set_abort(st, a.status); ok = false; break; }
+                            ptx::fence_proxy_async_smem();  // the stage's rows came by cp.async (generic proxy)
                             if (sub == 0) {
-                                if (!ptx::mbar_wait(&st.a_full[kt], (aph >> kt) & 1u)) { set_abort(st, a.status); ok = false; break; }
-                                aph ^= 1u << kt;
-                                ptx::fence_proxy_async_smem();  // the slab came by cp.async (generic proxy)
+                                if (!ptx::mbar_wait(&st.r_full[kt], (rph >> kt) & 1u)) { set_abort(st, a.status); ok = false; break; }
+                                rph ^= 1u << kt;
                             }
                             const uint64_t so = static_cast<uint64_t>(s) * kStageAdv;
-                            const uint64_t sa = static_cast<uint64_t>(kt) * kSlabAdv;
-                            const uint32_t tsfw = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS;
+                            const uint64_t sw = static_cast<uint64_t>(kt) * kSlabAdv;
+                            const uint32_t tsfa = tmem + LY::SF_COL + s * LY::STAGE_SF_COLS;
                             const int nk = min(4, kb64 - kt * 4);
                             auto kstep = [&](int kk) {
-                                const uint32_t tw = tsfw + kk * LY::SFW_STEP_COLS;
-                                const uint32_t tsa = tmem + LY::SFA_COL + (kt * 4 + kk) * 4;
-                                ptx::tmem_cp_32x128b_x4(tw, dsfw0 + so + kk * kSfAdv);
-                                if (sub == 0) ptx::tmem_cp_32x128b_x4(tsa, dsfa0 + kt * kSfSlabAdv + kk * kSfAdv);
-                                ptx::mma_nvf4(d_tmem, da0 + sa + kk * kOpAdv, dw0 + so + kk * kOpAdv, idesc, tsa, tw, acc);
+                                const uint32_t ta = tsfa + kk * 4;
+                                const uint32_t tw = tmem + LY::RES_SF_COL + (kt * 4 + kk) * 4;
+                                ptx::tmem_cp_32x128b_x4(ta, dsfa0 + so + kk * kSfAdv);
+                                if (sub == 0) ptx::tmem_cp_32x128b_x4(tw, dsfw0 + kt * kSfSlabAdv + kk * kSfAdv);
+                                ptx::mma_nvf4(d_tmem, dact0 + so + kk * kOpAdv, dw0 + sw + kk * kOpAdv, idesc, ta, tw, acc);
                                 acc = 1;
                             };
                             if (nk == 4) {
@@ -643,7 +739,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                                 for (int kk = 0; kk < nk; ++kk) kstep(kk);
                             }
                             ptx::tc_commit(&st.empty[s]);
-                            if (sub == nsub - 1) ptx::tc_commit(&st.a_empty[kt]);
+                            if (sub == nsub - 1) ptx::tc_commit(&st.r_empty[kt]);
                             if (++s == C::STAGES) { s = 0; ph ^= 1; }
                         }
                         if (!ok) break;
@@ -692,7 +788,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                             ptx::tmem_cp_32x128b_x4(tw + j * 4, dsfw0 + so + kk * kSfAdv + j * (SF_STAGE >> 4));
                         uint32_t tsa;
                         if constexpr (C::ROWS) {
-                            tsa = tmem + LY::SFA_COL + kg * 4;
+                            tsa = tmem + LY::RES_SF_COL + kg * 4;
                             if (sub == 0) ptx::tmem_cp_32x128b_x4(tsa, dsfact0 + so + kk * kSfAdv);
                         } else {
                             tsa = tsfact + kk * 4;
@@ -774,112 +870,105 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         const uint8_t* sptr[NSR];
         uint32_t cvalid = 0, svalid = 0;
         int s = 0;
-        uint32_t ph = 0, a_ph = 0;  // a_ph: phase bit of each resident slab's free barrier
+        uint32_t ph = 0;
         bool ok = true;
         TileCursor tc;
         for (;;) {
             const int L = tile_take(st, tc, total, false);
             if (L >= total || !ok || aborted(st)) break;
-            const TileInfo ti = tile_at(L);
-            const GemmProblem& P = a.p[ti.ph];
+            const TileInfo tu = tile_at(L);
+            const GemmProblem& P = a.p[tu.ph];
             const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
             const int kb64 = P.K / 64, k_stages = (P.K + 255) / 256;
-            if (ti.ph == 1) {
-                // the down GEMM reads h: wait until every gate/up tile of this token block stored it
-                // (the stages already issued complete on their own meanwhile)
-                if constexpr (LY::PUBLISH) publish_all();
-                const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS) + ready_extra;
-                if (!spin_until(a.ready + ti.tbg, target, ready_limit_ns)) { set_abort(st, a.status); break; }
-            }
-            // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row (a launch
-            // that permutes itself has the gate/up rows in shared memory)
-            const int32_t* a_row = rs && ti.ph == 0 ? rs->row : P.a_row;
-            int64_t srcv[(RW + 31) / 32];
-#pragma unroll
-            for (int h = 0; h < (RW + 31) / 32; ++h) {
-                const int r = w2 * RW + h * 32 + lane;
-                const int64_t p = ti.row0 + r;
-                srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (a_row ? static_cast<int64_t>(a_row[p]) : p) : -1;
-            }
-            cvalid = 0;
-            svalid = 0;
-#pragma unroll
-            for (int i = 0; i < NCR; ++i) {
-                const int rl = i * 4 + (lane >> 3);  // row within this warp's slice (same word of srcv in all lanes)
-                const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
-                cptr[i] = src >= 0 ? P.a_codes + src * a_ld + chunk * 16 : P.a_codes;
-                if (src >= 0) cvalid |= 1u << i;
-            }
-#pragma unroll
-            for (int i = 0; i < NSR; ++i) {
-                const int rl = i * 8 + (lane >> 2);
-                const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
-                sptr[i] = src >= 0 ? P.a_sf + src * sf_ld + word * 4 : P.a_sf;
-                if (src >= 0) svalid |= 1u << i;
-            }
-            const uint8_t* sf_tiles = P.a_sf + static_cast<int64_t>(ti.tbg) * kb64 * SF_TILE;
+            const uint8_t* sf_tiles = nullptr;
             // (units: the activation scales go with the first weight block only; the MMA thread
-            // keeps them in tensor memory for the others. Resident units gather each K-slab once,
-            // into the resident region, when the MMA thread has freed it.)
-            for (int sub = 0; ok && sub < (C::RES ? 1 : n_sub(ti)); ++sub)
-            for (int kt = 0; kt < k_stages; ++kt) {
-                uint8_t* sact;
-                uint8_t* ssf;
-                if constexpr (C::RES) {
-                    if (!ptx::mbar_wait(&st.a_empty[kt], ((a_ph >> kt) & 1u) ^ 1u)) { set_abort(st, a.status); ok = false; break; }
-                    a_ph ^= 1u << kt;
-                    sact = smem + LY::A_OFF + kt * LY::A_SLAB;
-                    ssf = smem + LY::A_SF_OFF + kt * SF_STAGE;
-                } else {
-                    if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
-                    sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
-                    ssf = smem + s * LY::STAGE_BYTES + LY::OFF_SFACT;
-                }
-                const bool kin = static_cast<int64_t>(kt) * BK_BYTES + chunk * 16 < a_ld;
-#pragma unroll
-                for (int i = 0; i < NCR; ++i) {
-                    const int r = w2 * RW + i * 4 + (lane >> 3);
-                    const bool v = ((cvalid >> i) & 1u) && kin;
-                    ptx::cp_async_16(sact + r * 128 + ((chunk ^ (r & 7)) * 16), v ? cptr[i] + kt * BK_BYTES : P.a_codes, v);
-                }
-                if (C::ROWS && sub > 0) {
-                } else if (P.a_sf_tiled) {
-                    // the stage's (up to) 4 scale tiles, 32 lines x 16 bytes each, 2 copies per thread
-                    const int nat = min(4, kb64 - kt * 4);
-#pragma unroll
-                    for (int c = pt; c < 4 * 32; c += kNumActProducers) {
-                        const int j = c >> 5, line = c & 31;
-                        const bool v = j < nat;
-                        ptx::cp_async_16(ssf + j * SF_TILE + line * 16,
-                                         v ? sf_tiles + (static_cast<int64_t>(kt) * 4 + j) * SF_TILE + line * 16 : P.a_sf, v);
+            // keeps them in tensor memory for the others. Weight-resident units run through several
+            // token blocks, each with its own rows.)
+            for (int sub = 0; ok && sub < n_sub(tu); ++sub) {
+                const TileInfo ti = sub_tile(tu, sub);
+                if (sub == 0 || C::WRES) {
+                    if (ti.ph == 1) {
+                        // the down GEMM reads h: wait until every gate/up tile of this token block stored
+                        // it (the stages already issued complete on their own meanwhile)
+                        if constexpr (LY::PUBLISH) publish_all();
+                        const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS) + ready_extra;
+                        if (!spin_until(a.ready + ti.tbg, target, ready_limit_ns)) { set_abort(st, a.status); ok = false; break; }
                     }
-                } else {
-                    const bool kin_s = static_cast<int64_t>(kt) * 16 + word * 4 < sf_ld;
+                    // source row of tile rows w2*RW + lane (+ 32): one gather-index load per row (a
+                    // launch that permutes itself has the gate/up rows in shared memory)
+                    const int32_t* a_row = rs && ti.ph == 0 ? rs->row : P.a_row;
+                    int64_t srcv[(RW + 31) / 32];
+#pragma unroll
+                    for (int h = 0; h < (RW + 31) / 32; ++h) {
+                        const int r = w2 * RW + h * 32 + lane;
+                        const int64_t p = ti.row0 + r;
+                        srcv[h] = (h * 32 + lane < RW && r < ti.rows) ? (a_row ? static_cast<int64_t>(a_row[p]) : p) : -1;
+                    }
+                    cvalid = 0;
+                    svalid = 0;
+#pragma unroll
+                    for (int i = 0; i < NCR; ++i) {
+                        const int rl = i * 4 + (lane >> 3);  // row within this warp's slice (same word of srcv in all lanes)
+                        const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
+                        cptr[i] = src >= 0 ? P.a_codes + src * a_ld + chunk * 16 : P.a_codes;
+                        if (src >= 0) cvalid |= 1u << i;
+                    }
 #pragma unroll
                     for (int i = 0; i < NSR; ++i) {
-                        const int r = w2 * RW + i * 8 + (lane >> 2);
-                        const bool v = ((svalid >> i) & 1u) && kin_s;
-                        ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : P.a_sf, v);
+                        const int rl = i * 8 + (lane >> 2);
+                        const int64_t src = __shfl_sync(0xFFFFFFFFu, srcv[rl >> 5], rl & 31);
+                        sptr[i] = src >= 0 ? P.a_sf + src * sf_ld + word * 4 : P.a_sf;
+                        if (src >= 0) svalid |= 1u << i;
                     }
+                    sf_tiles = P.a_sf + static_cast<int64_t>(ti.tbg) * kb64 * SF_TILE;
                 }
-                if constexpr (C::RES) {
-                    ptx::cp_async_arrive_noinc(&st.a_full[kt]);
-                    continue;
-                } else if constexpr (LY::PUBLISH) {
-                    ptx::cp_async_commit();
-                    ++issued;
-                    ptx::cp_async_wait<LAG>();
-                    if (issued > published + LAG) {
-                        ptx::fence_proxy_async_smem();
-                        for (; published + LAG < issued; ++published) {
-                            ptx::mbar_arrive(&st.full[pub]);
-                            if (++pub == C::STAGES) pub = 0;
+                for (int kt = 0; kt < k_stages; ++kt) {
+                    if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                    uint8_t* sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
+                    uint8_t* ssf = smem + s * LY::STAGE_BYTES + LY::OFF_SFACT;
+                    const bool kin = static_cast<int64_t>(kt) * BK_BYTES + chunk * 16 < a_ld;
+#pragma unroll
+                    for (int i = 0; i < NCR; ++i) {
+                        const int r = w2 * RW + i * 4 + (lane >> 3);
+                        const bool v = ((cvalid >> i) & 1u) && kin;
+                        ptx::cp_async_16(sact + r * 128 + ((chunk ^ (r & 7)) * 16), v ? cptr[i] + kt * BK_BYTES : P.a_codes, v);
+                    }
+                    if (C::ROWS && sub > 0) {
+                    } else if (P.a_sf_tiled) {
+                        // the stage's (up to) 4 scale tiles, 32 lines x 16 bytes each, 2 copies per thread
+                        const int nat = min(4, kb64 - kt * 4);
+#pragma unroll
+                        for (int c = pt; c < 4 * 32; c += kNumActProducers) {
+                            const int j = c >> 5, line = c & 31;
+                            const bool v = j < nat;
+                            ptx::cp_async_16(ssf + j * SF_TILE + line * 16,
+                                             v ? sf_tiles + (static_cast<int64_t>(kt) * 4 + j) * SF_TILE + line * 16 : P.a_sf, v);
+                        }
+                    } else {
+                        const bool kin_s = static_cast<int64_t>(kt) * 16 + word * 4 < sf_ld;
+#pragma unroll
+                        for (int i = 0; i < NSR; ++i) {
+                            const int r = w2 * RW + i * 8 + (lane >> 2);
+                            const bool v = ((svalid >> i) & 1u) && kin_s;
+                            ptx::cp_async_4(ssf + word * SF_TILE + (r % 32) * 16 + (r / 32) * 4, v ? sptr[i] + kt * 16 : P.a_sf, v);
                         }
                     }
-                } else {
-                    ptx::cp_async_arrive_noinc(&st.full[s]);
+                    if constexpr (LY::PUBLISH) {
+                        ptx::cp_async_commit();
+                        ++issued;
+                        ptx::cp_async_wait<LAG>();
+                        if (issued > published + LAG) {
+                            ptx::fence_proxy_async_smem();
+                            for (; published + LAG < issued; ++published) {
+                                ptx::mbar_arrive(&st.full[pub]);
+                                if (++pub == C::STAGES) pub = 0;
+                            }
+                        }
+                    } else {
+                        ptx::cp_async_arrive_noinc(&st.full[s]);
+                    }
+                    if (++s == C::STAGES) { s = 0; ph ^= 1; }
                 }
-                if (++s == C::STAGES) { s = 0; ph ^= 1; }
             }
         }
         if constexpr (LY::PUBLISH) publish_all();
@@ -1040,8 +1129,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             if (L >= total || aborted(st)) break;
             const TileInfo tu = tile_at(L);
             for (int sub = 0; sub < n_sub(tu); ++sub, ++lt) {
-            TileInfo ti = tu;
-            if constexpr (C::ROWS) ti.nb = sub;
+            const TileInfo ti = sub_tile(tu, sub);
             const GemmProblem& P = a.p[ti.ph];
             const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
             // the tile's scales are loaded before waiting for its accumulator, hiding their latency:
@@ -1322,7 +1410,7 @@ int gemm_schedule_rows(int schedule)
         case kSchedWide: return Cfg<kModeWide>::ACT_ROWS;
         case kSchedWideNarrow: return Cfg<kModeWideNarrow>::ACT_ROWS;
         case kSchedWideRows: return Cfg<kModeWideRows>::ACT_ROWS;
-        case kSchedRowsRes: return Cfg<kModeRowsRes>::ACT_ROWS;
+        case kSchedWeightsResident: return Cfg<kModeWRes>::ACT_ROWS;
         default: return Cfg<kModeActM>::ACT_ROWS;
     }
 }
@@ -1376,8 +1464,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, 
 {
     if ((schedule == kSchedWide || schedule == kSchedWideNarrow || schedule == kSchedWideRows) && !gemm_wide_fits(a))
         schedule = kSchedActOnM;
-    if (schedule == kSchedRowsRes &&
-        (a.p[0].K > Cfg<kModeRowsRes>::MAX_K || (a.nphase > 1 && a.p[1].K > Cfg<kModeRowsRes>::MAX_K)))
+    if (schedule == kSchedWeightsResident &&
+        (a.p[0].K > Cfg<kModeWRes>::MAX_K || (a.nphase > 1 && a.p[1].K > Cfg<kModeWRes>::MAX_K)))
         schedule = kSchedActOnM;  // the resident region holds K <= 2048
     if (schedule == kSchedAuto) schedule = p_max <= 64 ? kSchedWeightsOnM : kSchedActOnM;
     switch (schedule) {
@@ -1388,7 +1476,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, int64_t p_max, int schedule, 
             if (a.p[0].K <= Cfg<kModeWideRows>::MAX_K && (a.nphase < 2 || a.p[1].K <= Cfg<kModeWideRows>::MAX_K))
                 return launch_t<kModeWideRows>(a, p_max, sms, stream);
             return launch_t<kModeWide>(a, p_max, sms, stream);
-        case kSchedRowsRes: return launch_t<kModeRowsRes>(a, p_max, sms, stream);
+        case kSchedWeightsResident: return launch_t<kModeWRes>(a, p_max, sms, stream);
         default: return launch_t<kModeActM>(a, p_max, sms, stream);
     }
 }

@@ -103,11 +103,11 @@ constexpr int kGemmMaxG = 1025;
 // 256 weight rows per tile (wide: fewer MMAs and scale copies per weight byte; needs N % 256 == 0,
 // else it falls back to activations on M). Auto picks weights-on-M when p_max <= 64.
 // Wide-narrow: the wide shape with 32-row token blocks and a fifth stage (groups of few rows).
-// Resident token-block units: a whole 128-row token block per CTA, its activations gathered once
-// into shared memory, 128-row weight blocks into a double-buffered accumulator (K <= 2048).
+// Weight-resident units: one 128-row weight block (all of K <= 2048) per CTA in shared memory, up to
+// 16 token blocks of its group streamed past it into a double-buffered accumulator.
 enum GemmSchedule : int {
     kSchedAuto = 0, kSchedActOnM = 1, kSchedWeightsOnM = 2, kSchedWide = 3, kSchedWideNarrow = 4, kSchedWideRows = 5,
-    kSchedRowsRes = 6
+    kSchedWeightsResident = 6
 };
 bool gemm_wide_fits(const GemmArgs& a);
 // whether a launch of p_max rows is large enough for token-block units (kSchedWideRows)

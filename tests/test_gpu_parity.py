@@ -326,17 +326,19 @@ def _gemm_case(seed, counts, H, I, N_kind):
     return dict(offsets=offsets, P=P, ac=ac, asf=asf, sa=sa, a_row=a_row, bc=bc, bs=bs, bsc=bsc, N=N, K=K)
 
 
-SCHEDS = ["act_on_m", "weights_on_m", "wide", "wide_rows", "rows_resident"]
+SCHEDS = ["act_on_m", "weights_on_m", "wide", "wide_rows", "weights_resident"]
 
 
 def _sched(moe, name):
     return {"act_on_m": moe.SCHED_ACT_ON_M, "weights_on_m": moe.SCHED_WEIGHTS_ON_M, "wide": moe.SCHED_WIDE,
-            "wide_rows": moe.SCHED_WIDE_ROWS, "rows_resident": moe.SCHED_ROWS_RESIDENT}[name]
+            "wide_rows": moe.SCHED_WIDE_ROWS, "weights_resident": moe.SCHED_WEIGHTS_RESIDENT}[name]
 
 
 @pytest.mark.parametrize("sched", SCHEDS)
-@pytest.mark.parametrize("counts", [[3, 0, 130, 1, 128, 257], [1] * 40, [700], [0, 0, 5], [33, 32, 31, 64, 65]])
+@pytest.mark.parametrize("counts", [[3, 0, 130, 1, 128, 257], [1] * 40, [700], [0, 0, 5], [33, 32, 31, 64, 65],
+                                    [5, 4100, 0, 2049]])
 def test_gemm_gate_up_f32(moe, counts, sched):
+    # (4100 rows = 33 blocks of 128: a weight-resident schedule takes them in runs of at most 16)
     c = _gemm_case(len(counts), counts, 256, 128, "gate_up")
     ref = oracle.grouped_gemm(c["ac"], c["asf"], c["sa"], c["offsets"], c["bc"], c["bs"], c["bsc"], a_row=c["a_row"])
     bcp, bsp = moe.moe_prepack_nvfp4(dev(c["bc"]), dev(c["bs"]), True)
