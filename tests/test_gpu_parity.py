@@ -117,17 +117,24 @@ def test_quantize_static_scale_edge_values(moe):
 # router
 # ------------------------------------------------------------------------------------------------
 
-def _check_route_values(w, g, lg, w_ref, g_ref, lg_ref):
+def _check_route_values(w, g, lg, w_ref, g_ref, lg_ref, ids=None, k=None):
     # The logits are FP32 sums (their order differs between the CUDA-core and tensor-core routers);
     # the renormalised softmax moves each weight by at most half the largest logit change (its
     # Jacobian rows sum to 2 p (1 - p) <= 1/2 in absolute value) and the sigmoid gate by a quarter
-    # of it, so the weights are held to the logits' own error plus FP32 rounding.
-    dl = float(np.max(np.abs(lg.cpu().numpy() - lg_ref)))
+    # of it, so against the oracle's own logits the weights are held to the logits' error plus FP32
+    # rounding. The routing arithmetic itself is held to 1e-6: the oracle's FP64 softmax and
+    # renormalisation of the kernel's OWN FP32 logits must give the same ids and weights.
+    lg = lg.cpu().numpy()
+    dl = float(np.max(np.abs(lg - lg_ref)))
     assert dl <= 1e-4, dl
     w = w.cpu().numpy()
     assert np.max(np.abs(w - w_ref)) <= dl + W_TOL
     assert np.max(np.abs(w.sum(1) - 1.0)) <= W_TOL
     assert np.max(np.abs(g.cpu().numpy() - g_ref)) <= 0.5 * dl + W_TOL
+    if ids is not None:
+        ids2, w2, _ = oracle.route_from_logits(lg.astype(np.float64), k)
+        np.testing.assert_array_equal(ids2, ids.cpu().numpy())
+        assert np.max(np.abs(w - w2)) <= W_TOL
 
 
 @pytest.mark.parametrize("config", ["tiny", "decode", "prefill4k"])
@@ -144,7 +151,7 @@ def test_route_topk(moe, config):
                          logit_bias=None if bias is None else dev(bias), prepacked=True)
     ids, w, g, lg = moe.moe_route_topk(bf16_dev(x), layer, want_logits=True)
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
-    _check_route_values(w, g, lg, w_ref, g_ref, lg_ref)
+    _check_route_values(w, g, lg, w_ref, g_ref, lg_ref, ids=ids, k=k)
 
 
 @pytest.mark.parametrize("config,T", [("tiny", 65), ("tiny", 130), ("decode", 300), ("decode", 2500)])
@@ -162,7 +169,7 @@ def test_route_topk_tensor_core_ragged(moe, config, T):
     ids, w, g, lg = moe.moe_route_topk(bf16_dev(x), layer, want_logits=True)
     moe.moe_read_device_status()
     np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
-    _check_route_values(w, g, lg, w_ref, g_ref, lg_ref)
+    _check_route_values(w, g, lg, w_ref, g_ref, lg_ref, ids=ids, k=k)
 
 
 @pytest.mark.parametrize("interleave", [0, 1])
