@@ -169,8 +169,9 @@ struct Lay {
     static_assert(STAGE_BYTES % 1024 == 0, "stages keep 1024-byte alignment");
 };
 
+// 16-byte aligned size: the exchange buffers placed right after it are accessed with 16-byte loads
 template <int kMode>
-struct Tail {
+struct alignas(16) Tail {
     uint64_t full[Cfg<kMode>::STAGES];
     uint64_t empty[Cfg<kMode>::STAGES];
     uint64_t acc_full[2];
@@ -208,6 +209,13 @@ struct RouteSmem {
     int32_t row[kRouteMaxAssign + kRouteMaxT];
     int32_t perm[kRouteMaxAssign];
 };
+
+template <int kMode>
+constexpr size_t smem_bytes();
+static_assert(sizeof(Tail<kModeWideNarrow>) % 16 == 0 && sizeof(Tail<kModeSwap>) % 16 == 0 &&
+                  sizeof(Tail<kModeActM>) % 16 == 0 && sizeof(Tail<kModeWRes>) % 16 == 0,
+              "exchange buffers after the tail stay 16-byte aligned");
+static_assert(Lay<kModeWideNarrow>::TAIL_OFF % 16 == 0 && Lay<kModeSwap>::TAIL_OFF % 16 == 0, "tail offset");
 
 template <int kMode>
 constexpr size_t smem_bytes()
