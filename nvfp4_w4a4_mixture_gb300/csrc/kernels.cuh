@@ -31,7 +31,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, int E, cons
                                     float* logits, int ld, int* status, cudaStream_t stream);
 
 // ---- permute.cu
-constexpr int kPermChunk = 512;  // assignments per warp-chunk
+constexpr int kPermChunk = 512;  // assignments per chunk (one CTA of the permutation kernels)
 inline int64_t perm_chunks(int64_t n) { return n <= 0 ? 1 : (n + kPermChunk - 1) / kPermChunk; }
 // offsets: [E+2]; hist: (perm_chunks(n) + 1) * E ints of scratch; ticket: zero between calls.
 cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int with_shared, int32_t* offsets,

@@ -1,14 +1,17 @@
 // permute.cu -- stable counting sort of the T*k (token, slot) assignments by expert id.
 //
-// The flat assignment list f = t*k + j is cut into warp-chunks of kPermChunk entries.
-//   1. histogram: each warp counts its chunk per expert (warp match: one shared-memory add per
-//      run of equal ids, no atomics) -> hist[expert][chunk];
+// The flat assignment list f = t*k + j is cut into chunks of kPermChunk entries, one CTA each; the
+// CTA's kPermWarps warps take kPermChunk / kPermWarps consecutive entries each.
+//   1. histogram: each warp counts its entries per expert (warp match: one shared-memory add per
+//      run of equal ids, no atomics), the CTA sums its warps -> hist[expert][chunk];
 //   2. row scan (one CTA per expert): exclusive scan of the expert's counts over the chunks, the
 //      expert's total to totals[expert]; the last CTA to finish (atomic ticket, no waiting) scans
 //      the totals over the experts -> expert offsets (the shared expert appended as group E);
-//   3. scatter: each warp walks its chunk in order; an entry's position is its expert's offset
-//      plus its chunk's base plus the number of earlier entries of the same expert in the chunk.
-//      Ascending f within every expert (stable), independent of scheduling: bit-exact.
+//   3. scatter: each warp counts its entries again, an exclusive scan over the CTA's warps gives
+//      every warp its base per expert (offset + chunk base + earlier warps' counts), and the warp
+//      walks its entries in order, an entry's position being that base plus the number of earlier
+//      entries of the same expert in the warp. Ascending f within every expert (stable),
+//      independent of scheduling: bit-exact.
 #include <cub/block/block_scan.cuh>
 
 #include "kernels.cuh"
@@ -16,6 +19,31 @@
 namespace moe {
 
 constexpr int kPermWarps = 8;
+constexpr int kPermWarpEntries = kPermChunk / kPermWarps;  // consecutive entries per warp
+static_assert(kPermChunk % (kPermWarps * 32) == 0, "whole warp passes");
+
+// Counts of this warp's entries per expert into my[0..E) (zeroed first); ids outside [0, E) are
+// dropped (and reported when status is given).
+__device__ __forceinline__ void warp_count(const int32_t* __restrict__ ids, int64_t beg, int64_t end, int E, int32_t* my,
+                                           int lane, int* status)
+{
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+    for (int64_t base = beg; base < end; base += 32) {
+        const int64_t i = base + lane;
+        int e = -1;
+        if (i < end) {
+            e = ids[i];
+            if (e < 0 || e >= E) {
+                if (status) record_status(status, kDevBadExpertId);
+                e = -1;
+            }
+        }
+        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
+        __syncwarp();
+    }
+}
 
 __global__ void __launch_bounds__(kPermWarps * 32)
     k_perm_hist(const int32_t* __restrict__ ids, int64_t n, int E, int64_t nchunks, int32_t* __restrict__ hist,
@@ -24,27 +52,16 @@ __global__ void __launch_bounds__(kPermWarps * 32)
     ptx::griddep_wait();  // inputs come from the launch before this one
     extern __shared__ int32_t cnt[];  // [kPermWarps][E]
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    int32_t* my = cnt + warp * E;
-    for (int e = lane; e < E; e += 32) my[e] = 0;
-    __syncwarp();
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp;
-    if (c >= nchunks) return;
-    const int64_t beg = c * kPermChunk, end = min(n, beg + kPermChunk);
-    for (int64_t base = beg; base < end; base += 32) {
-        const int64_t i = base + lane;
-        int e = -1;
-        if (i < end) {
-            e = ids[i];
-            if (e < 0 || e >= E) {
-                record_status(status, kDevBadExpertId);
-                e = -1;
-            }
-        }
-        const unsigned m = __match_any_sync(0xFFFFFFFFu, e);
-        if (e >= 0 && lane == __ffs(m) - 1) my[e] += __popc(m);
-        __syncwarp();
+    const int64_t c = blockIdx.x;
+    const int64_t beg = min(n, c * kPermChunk + warp * kPermWarpEntries), end = min(n, beg + kPermWarpEntries);
+    warp_count(ids, beg, end, E, cnt + warp * E, lane, status);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kPermWarps * 32) {
+        int32_t t = 0;
+#pragma unroll
+        for (int w = 0; w < kPermWarps; ++w) t += cnt[w * E + e];
+        hist[static_cast<int64_t>(e) * nchunks + c] = t;
     }
-    for (int e = lane; e < E; e += 32) hist[static_cast<int64_t>(e) * nchunks + c] = my[e];
 }
 
 constexpr int kScanThreads = 1024;
@@ -108,7 +125,7 @@ __global__ void __launch_bounds__(kPermWarps * 32)
                    int32_t* __restrict__ src_perm, int32_t* __restrict__ row_token)
 {
     ptx::griddep_wait();  // inputs come from the launch before this one
-    extern __shared__ int32_t base_s[];  // [kPermWarps][E]
+    extern __shared__ int32_t base_s[];  // [kPermWarps][E]: this warp's counts, then its bases
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // the shared-expert rows: row T*k + t holds token t
     if (row_token && with_shared) {
@@ -116,12 +133,22 @@ __global__ void __launch_bounds__(kPermWarps * 32)
              t += static_cast<int64_t>(gridDim.x) * blockDim.x)
             row_token[n + t] = static_cast<int32_t>(t);
     }
-    const int64_t c = static_cast<int64_t>(blockIdx.x) * kPermWarps + warp;
-    if (c >= nchunks) return;
+    const int64_t c = blockIdx.x;
+    const int64_t beg = min(n, c * kPermChunk + warp * kPermWarpEntries), end = min(n, beg + kPermWarpEntries);
     int32_t* my = base_s + warp * E;
-    for (int e = lane; e < E; e += 32) my[e] = __ldg(offsets + e) + hist[static_cast<int64_t>(e) * nchunks + c];
-    __syncwarp();
-    const int64_t beg = c * kPermChunk, end = min(n, beg + kPermChunk);
+    warp_count(ids, beg, end, E, my, lane, nullptr);
+    __syncthreads();
+    // each warp's base per expert: offset + the chunk's base + the counts of the earlier warps
+    for (int e = threadIdx.x; e < E; e += kPermWarps * 32) {
+        int32_t run = __ldg(offsets + e) + hist[static_cast<int64_t>(e) * nchunks + c];
+#pragma unroll
+        for (int w = 0; w < kPermWarps; ++w) {
+            const int32_t v = base_s[w * E + e];
+            base_s[w * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
     for (int64_t b = beg; b < end; b += 32) {
         const int64_t i = b + lane;
@@ -209,7 +236,7 @@ cudaError_t launch_permute(const int32_t* topk_ids, int T, int k, int E, int wit
                           with_shared, offsets, perm_src, src_perm, row_token, status);
     }
     const int64_t nchunks = perm_chunks(n);
-    const int blocks = static_cast<int>((nchunks + kPermWarps - 1) / kPermWarps);
+    const int blocks = static_cast<int>(nchunks);
     const size_t smem = static_cast<size_t>(kPermWarps) * E * sizeof(int32_t);
     int32_t* totals = hist + nchunks * E;
     cudaError_t e = launch_pdl(k_perm_hist, dim3(blocks), dim3(kPermWarps * 32), smem, stream, topk_ids, n, E, nchunks, hist,
