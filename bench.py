@@ -232,8 +232,9 @@ def launches_per_layer(c):
         return 3  # front half (quantize + route + permute), expert GEMMs, combine
     quant = 1 if T * H // 16 <= 4096 else 2
     perm = 1 if T * k <= 512 else 3
-    # the layer's counters zeroed, quantize, logits + top-k, permute, expert GEMMs (one launch), combine
-    return 1 + quant + 2 + perm + 1 + 1
+    # quantize (its first launch also zeroes the layer's counters), logits + top-k, permute, expert GEMMs
+    # (one launch), combine
+    return quant + 2 + perm + 1 + 1
 
 
 def distinct_experts(m, layer, x):

@@ -59,9 +59,10 @@ moe_status_t check_device()
 }
 
 struct WsLayout {
-    size_t hdr, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, perm_src, src_perm, row_token,
+    size_t hdr, amax_slots, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, perm_src, src_perm, row_token,
         hist, h_codes, h_sf, ready, y, total;
 };
+constexpr int kMaxAmaxSlots = 4096;  // >= layer_amax_slots(SM count) on any device this library runs on
 
 WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
 {
@@ -74,6 +75,7 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     };
     const int64_t n = T * k, P = T * k + T;
     L.hdr = take(sizeof(WsHeader));
+    L.amax_slots = take(kMaxAmaxSlots * 4);  // the layer quantizer's per-CTA maxima
     L.topk_ids = take(n * 4);
     L.topk_w = take(n * 4);
     L.shared_g = take(T * 4);
@@ -106,17 +108,6 @@ __global__ void k_stage_in(const uint4* __restrict__ x, uint4* __restrict__ xd, 
         xd[i] = x[i];
         if (r) rd[i] = r[i];
     }
-    ptx::griddep_launch_dependents();
-}
-
-// The layer's counters for the launches that follow (tensor-max scratch, token-block readiness and
-// the tile counter of the expert GEMMs), zeroed by a kernel rather than memsets so that every launch of
-// the layer overlaps the one before it; the previous launch may still use them until it completes.
-__global__ void k_zero_counters(unsigned* __restrict__ amax_bits, int32_t* __restrict__ ready, int n)
-{
-    ptx::griddep_wait();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *amax_bits = 0u;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) ready[i] = 0;
     ptx::griddep_launch_dependents();
 }
 
@@ -555,13 +546,12 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
         MOE_CUDA(mark(1), "event record");
         MOE_CUDA(mark(2), "event record");
     } else {
-        // the counters the launches below rely on, zeroed first by a kernel (no memset between two
-        // kernels: each launch overlaps the one before it, programmatic dependent launch)
-        MOE_CUDA(launch_pdl(k_zero_counters, dim3((n_ready + 1 + 255) / 256), dim3(256), 0, s, &hdr->amax_bits, P32(W.ready),
-                            n_ready + 1),
-                 "clear the layer's counters");
-        // W4A4: quantize the layer input once per token (dynamic tensor scale)
-        MOE_CUDA(launch_quantize(x, T, H, nullptr, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, &hdr->amax_bits, sms, s, true),
+        // W4A4: quantize the layer input once per token (dynamic tensor scale); the quantizer's first
+        // launch also zeroes the counters of the expert GEMMs (no memset between two kernels: each
+        // launch overlaps the one before it, programmatic dependent launch)
+        if (layer_amax_slots(sms) > kMaxAmaxSlots) return fail(MOE_ERR_UNSUPPORTED_DEVICE, "%d SMs: too many", sms);
+        MOE_CUDA(launch_quantize_layer(x, T, H, P8(W.x_codes), P8(W.x_sf), &hdr->s_x,
+                                       reinterpret_cast<uint32_t*>(base + W.amax_slots), P32(W.ready), n_ready + 1, sms, s),
                  "quantize");
         MOE_CUDA(mark(1), "event record");
         // router, softmax, top-k, shared gate

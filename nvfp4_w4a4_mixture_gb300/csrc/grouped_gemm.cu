@@ -1254,24 +1254,24 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     // gate/up bank's round lies in its gate or its up half); written 128 bytes per row
                     // and instruction through an in-warp transpose
                     static_assert(GPR == 4, "rounds of 64 columns");
-#pragma unroll
-                    for (int rd = 0; rd < NR; ++rd) {
-                        uint32_t v[GPR][16];
-                        load_round(rd, v);
-                        if (rd == NR - 1) release();
+                    auto round_col = [&](int rd, float& sc) {
                         const int c0 = half * CPW + rd * GPR * 16;  // first tile column of the round
-                        int col;
-                        float sb;
                         if (P.gate_up) {
                             const int cc = c0 & 127, upper = cc >= 64;
-                            col = (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
-                            sb = upper ? sb1 : sb0;
-                        } else {
-                            col = ti.nb * W_ROWS + c0;
-                            sb = sb0;
+                            sc = sa * (upper ? sb1 : sb0);
+                            return (upper ? P.N / 2 : 0) + (ti.nb * LY::WB + (c0 >> 7)) * 64 + (cc & 63);
                         }
-                        const float sc = sa * sb;
-                        if (P.epilogue == kEpiF32) {
+                        sc = sa * sb0;
+                        return ti.nb * W_ROWS + c0;
+                    };
+                    if (P.epilogue == kEpiF32) {
+#pragma unroll
+                        for (int rd = 0; rd < NR; ++rd) {
+                            uint32_t v[GPR][16];
+                            load_round(rd, v);
+                            if (rd == NR - 1) release();
+                            float sc;
+                            const int col = round_col(rd, sc);
                             // 64 FP32 = two rows of 128 bytes: chunk c = columns 4c .. 4c + 3
 #pragma unroll
                             for (int hh = 0; hh < 2; ++hh) {
@@ -1287,18 +1287,33 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                                 store_rows128(x, reinterpret_cast<uint8_t*>(static_cast<float*>(P.out) + po * P.N + col + hh * 32),
                                               valid, lane);
                             }
-                        } else {
-                            // 64 bf16 = one row of 128 bytes: chunk c = columns 8c .. 8c + 7
-                            uint4 x[8];
+                        }
+                    } else {
+                        // bf16: every round is packed (64 columns = 128 bytes: chunk c = columns 8c .. 8c + 7)
+                        // as soon as it is loaded, and the accumulator is freed once the last round is
+                        // in registers, before any transpose or store
+                        uint4 x[NR][8];
+#pragma unroll
+                        for (int rd = 0; rd < NR; ++rd) {
+                            uint32_t v[GPR][16];
+                            load_round(rd, v);
+                            if (rd == NR - 1) release();
+                            float sc;
+                            round_col(rd, sc);
 #pragma unroll
                             for (int c = 0; c < 8; ++c) {
                                 const int g = c >> 1, e = (c & 1) * 8;
-                                x[c] = make_uint4(pack_bf16x2(__uint_as_float(v[g][e]) * sc, __uint_as_float(v[g][e + 1]) * sc),
-                                                  pack_bf16x2(__uint_as_float(v[g][e + 2]) * sc, __uint_as_float(v[g][e + 3]) * sc),
-                                                  pack_bf16x2(__uint_as_float(v[g][e + 4]) * sc, __uint_as_float(v[g][e + 5]) * sc),
-                                                  pack_bf16x2(__uint_as_float(v[g][e + 6]) * sc, __uint_as_float(v[g][e + 7]) * sc));
+                                x[rd][c] = make_uint4(pack_bf16x2(__uint_as_float(v[g][e]) * sc, __uint_as_float(v[g][e + 1]) * sc),
+                                                      pack_bf16x2(__uint_as_float(v[g][e + 2]) * sc, __uint_as_float(v[g][e + 3]) * sc),
+                                                      pack_bf16x2(__uint_as_float(v[g][e + 4]) * sc, __uint_as_float(v[g][e + 5]) * sc),
+                                                      pack_bf16x2(__uint_as_float(v[g][e + 6]) * sc, __uint_as_float(v[g][e + 7]) * sc));
                             }
-                            store_rows128(x, reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(P.out) + po * P.N + col), valid, lane);
+                        }
+#pragma unroll
+                        for (int rd = 0; rd < NR; ++rd) {
+                            float sc;
+                            const int col = round_col(rd, sc);
+                            store_rows128(x[rd], reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(P.out) + po * P.N + col), valid, lane);
                         }
                     }
                 } else {

@@ -14,6 +14,11 @@ cudaError_t launch_quantize(const uint16_t* x, int64_t rows, int64_t K, const fl
                             bool amax_zeroed = false);
 cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
                                 uint8_t* sf, float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream);
+// The layer's quantizer (dynamic tensor scale): per-CTA maxima in slots (layer_amax_slots(sms) of
+// them), no atomics; it also zeroes zero[0 .. n_zero) for the launches that follow.
+int layer_amax_slots(int sms);
+cudaError_t launch_quantize_layer(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf, float* s_out,
+                                  uint32_t* slots, int32_t* zero, int n_zero, int sms, cudaStream_t stream);
 
 // ---- router.cu
 // logits: FP32 [T][E+1] (column E = shared-gate logit, no bias).

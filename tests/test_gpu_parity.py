@@ -555,7 +555,7 @@ def test_device_status_clean(moe):
 @pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 64), ("tiny", 65), ("tiny", 300), ("decode", 300)])
 def test_layer_launch_count(moe, name, T):
     # the kernels one layer call launches, as the CUDA activity trace lists them, against the count the
-    # benchmark reports: 3 for small batches (front half, expert GEMMs, combine), up to 10 otherwise
+    # benchmark reports: 3 for small batches (front half, expert GEMMs, combine), up to 9 otherwise
     from torch.autograd import DeviceType
     from torch.profiler import ProfilerActivity, profile
 
