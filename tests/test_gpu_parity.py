@@ -452,9 +452,10 @@ def test_layer_tiny(moe):
     assert err < 5e-3  # requantized codes agree, so the error is the bf16 rounding of y and out
 
 
-@pytest.mark.parametrize("T", [None, 3])
+@pytest.mark.parametrize("T", [None, 3, 1500])
 def test_layer_tiny_residual(moe, T):
-    # 64 tokens: separate front kernels, 3 tokens: the one-launch front half
+    # 64 tokens: separate front kernels, 3 tokens: the one-launch front half, 1500 tokens: the
+    # streaming combine (one CTA per SM, rows bulk-copied into shared memory)
     _check_layer(moe, I_.layer_case("tiny", seed=0 if T is None else 21, T=T), residual=True)
 
 
@@ -471,7 +472,7 @@ def test_layer_prefill16k_sampled(moe):
     _check_layer(moe, I_.layer_case("prefill16k", sample=8))
 
 
-@pytest.mark.parametrize("T", [1, 4, 5, 7, 8, 9, 63, 64, 65, 130])
+@pytest.mark.parametrize("T", [1, 4, 5, 7, 8, 9, 63, 64, 65, 130, 1023, 1024])
 def test_layer_tiny_token_counts(moe, T):
     # T <= 64 with T*k <= 512 takes the one-launch front half, larger T the separate kernels; the
     # front half stages 4 tokens per router pass up to T = 4 and 8 beyond, so 4/5, 7/8/9 and

@@ -54,12 +54,14 @@ def _run(moe, case):
     layer = gpu_layer(moe, case)
     T = case["T"]
     ws = moe.Workspace(layer.workspace_bytes(T))
-    moe.moe_layer_forward(layer, bf16_dev(case["x"]), ws=ws)
+    out = moe.moe_layer_forward(layer, bf16_dev(case["x"]), ws=ws)
     torch.cuda.synchronize()
     moe.moe_read_device_status(ws=ws)
     got = moe.layer_intermediates(layer, T, ws)
-    return {k: (v.float().cpu().numpy() if torch.is_tensor(v) and v.dtype == torch.bfloat16
-                else v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in got.items()}
+    got = {k: (v.float().cpu().numpy() if torch.is_tensor(v) and v.dtype == torch.bfloat16
+               else v.cpu().numpy() if torch.is_tensor(v) else v) for k, v in got.items()}
+    got["out"] = out.float().cpu().numpy()
+    return got
 
 
 def _scale_tile_bytes(h_sf_tiles, offsets, block_rows, positions, n_cols):
@@ -116,6 +118,7 @@ def _check_full(moe, case):
     T, E, k, I = case["T"], case["E"], case["k"], case["I"]
     b64 = None if case["bias"] is None else case["bias"].astype(np.float64)
     ref = oracle.layer_forward(case["x"], case["w_r"], k, case["gu"], case["dn"], case["s_mid"], bias=b64)
+    assert I_.rel_frobenius(got["out"], ref["out_f64"]) <= 2e-2
     _check_front(got, case, ref["topk_ids"], ref["logits"], ref["x_codes"], ref["x_sf"], ref["x_scale"])
     if got["permutation_in_workspace"]:
         np.testing.assert_array_equal(got["expert_offsets"], ref["offsets"])
@@ -129,11 +132,12 @@ def _check_full(moe, case):
     return got
 
 
-@pytest.mark.parametrize("T", [1, 4, 5, 64, 65])
+@pytest.mark.parametrize("T", [1, 4, 5, 64, 65, 1100])
 def test_layer_intermediates_tiny(moe, T):
     # T <= 32: one-launch front half + the expert GEMMs' own permutation (wide-narrow tiles);
     # T = 64: one-launch front half with the permutation stored (wide tiles); T = 65: separate
-    # quantize / tensor-core router / top-k / permute launches
+    # quantize / tensor-core router / top-k / permute launches; T = 1100: the CTA-chunk permutation
+    # over several chunks and the streaming combine
     got = _check_full(moe, I_.layer_case("tiny", seed=T, T=T))
     assert got["permutation_in_workspace"] == (T > 32 or not GEMM_PERMUTES)
 
