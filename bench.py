@@ -225,11 +225,20 @@ def one_launch_front(c):
     return c["T"] <= 64 and c["T"] * c["k"] <= 512 and c["E"] <= 1024
 
 
+def fused_route(c):
+    """Large batches with 512 experts route first, in one launch that also takes x's maximum, and the
+    quantizer's encoding pass follows (see csrc/api.cu)."""
+    return (not one_launch_front(c) and c["E"] == 512 and c["k"] <= 16 and c["T"] >= 12288 and c["H"] % 64 == 0
+            and c["H"] <= 8192)
+
+
 def launches_per_layer(c):
     """Kernels of the library launched by one layer forward (see csrc/api.cu)."""
     T, H, k = c["T"], c["H"], c["k"]
     if one_launch_front(c):
         return 3  # front half (quantize + route + permute), expert GEMMs, combine
+    if fused_route(c):
+        return 1 + 1 + 3 + 1 + 1  # router + top-k + max |x|, encoder, permute, expert GEMMs, combine
     quant = 1 if T * H // 16 <= 4096 else 2
     perm = 1 if T * k <= 512 else 3
     # quantize (its first launch also zeroes the layer's counters), logits + top-k, permute, expert GEMMs
@@ -482,6 +491,10 @@ def measure(m, name, K, W, args, d):
     if one_launch_front(c):
         # one launch covers the first three stages: events 1..3 follow it back to back
         stage_us = {"front": sum(stage_us.pop(n) for n in ("quantize", "route", "permute")), **stage_us}
+    elif fused_route(c):
+        # routing ran first: the first interval is the router's, the second the encoder's
+        first, second = stage_us.pop("quantize"), stage_us.pop("route")
+        stage_us = {"route (with max |x|)": first, "quantize (encode)": second, **stage_us}
 
     # ---- end to end through the public call: pinned host input -> layer -> pinned host output
     x_h = x.cpu().pin_memory()

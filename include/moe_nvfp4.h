@@ -131,6 +131,9 @@ moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, con
  *   x: bf16 [T][H]; uses L->w_router, L->logit_bias, L->H, L->E, L->k.
  *   topk_ids: int32 [T][k] (routing order: weight non-increasing); topk_w: FP32 [T][k];
  *   shared_g: nullable FP32 [T]; logits_out: nullable FP32 [T][E] (bias included).
+ *   With E = 512, k <= 16 and T >= 12288 the logits, top-k, weights and shared gate come from one
+ *   launch that holds all 512 logits of 128 tokens per CTA; the shared-gate logit is then a
+ *   sequential FP32 sum (the routed logits stay tensor-core sums).
  *   ws: >= moe_workspace_bytes(H, E, k, I, T).
  * ------------------------------------------------------------------------------------------- */
 moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int32_t* topk_ids,
@@ -223,7 +226,9 @@ moe_status_t moe_layer_forward(const moe_layer_t* L, const uint16_t* x, int T, c
  *   quantizer, [1] after it, [2] after routing (logits + top-k), [3] after the permutation, [4]
  *   after the expert GEMMs (gate/up + SwiGLU + requantisation + down, one launch), [5] after the
  *   combine. For small batches (T <= 64 and T*k <= 512) quantisation, routing and permutation run
- *   as one launch between events [0] and [1]; [2] and [3] then follow [1] directly.
+ *   as one launch between events [0] and [1]; [2] and [3] then follow [1] directly. For large
+ *   batches with E = 512 and k <= 16 (T >= 12288) routing runs first and also takes x's maximum:
+ *   [1] follows routing and [2] the quantizer (moe_layer_workspace_view reports route_first = 1).
  *   n_events: 0 (plain forward) or 6. The library creates and destroys no event.
  * ------------------------------------------------------------------------------------------- */
 moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x, int T, const uint16_t* residual,
@@ -289,6 +294,8 @@ moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const moe_layer_t*
  *                     byte (r % 32) * 16 + (r / 32) * 4 + c % 4 of tile c / 4
  *     y               bf16 [T*k + T][H]: the down projection of row (t, j) at row t*k + j (the
  *                     assignment order), of the shared expert for token t at row T*k + t
+ *     route_first     1 when the forward routes before it encodes x (the fused router of large
+ *                     batches), else 0
  *   bytes = moe_workspace_bytes(H, E, k, I, T). The view depends on the device (its SM count
  *   picks the tile schedule), so query it on the device that runs the forward.
  * ------------------------------------------------------------------------------------------- */
@@ -300,6 +307,7 @@ typedef struct {
     int64_t permutation_in_workspace, expert_offsets, perm_src, src_perm, row_token;
     int64_t h_codes, h_sf, h_block_rows;
     int64_t y;
+    int64_t route_first;
 } moe_layer_view_t;
 
 moe_status_t moe_layer_workspace_view(const moe_layer_t* L, int T, moe_layer_view_t* view);

@@ -45,7 +45,7 @@ class LayerView(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
         "bytes", "x_scale", "x_codes", "x_sf", "logits", "logits_ld", "topk_ids", "topk_w", "shared_g",
         "permutation_in_workspace", "expert_offsets", "perm_src", "src_perm", "row_token", "h_codes", "h_sf",
-        "h_block_rows", "y")]
+        "h_block_rows", "y", "route_first")]
 
 
 _lib = None
@@ -324,8 +324,9 @@ def layer_intermediates(layer, T, ws):
     """Views (no copies, no arithmetic) of the intermediate results that the last moe_layer_forward of
     T tokens left in workspace `ws`, at the offsets moe_layer_workspace_view reports. Read them once
     the forward's stream has passed it. Keys: x_scale, x_codes, x_sf, logits [T][E+1] (column E: the
-    shared-gate logit), topk_ids, topk_w, shared_g, h_codes, h_sf (tiles), y; with the permutation
-    in the workspace also expert_offsets, perm_src, src_perm, row_token."""
+    shared-gate logit), topk_ids, topk_w, shared_g, h_codes, h_sf (tiles), y, route_first (the fused
+    router ran before the encoder); with the permutation in the workspace also expert_offsets,
+    perm_src, src_perm, row_token."""
     v = moe_layer_workspace_view(layer, T)
     H, E, k, I = layer.H, layer.E, layer.k, layer.I
     buf = ws.tensor
@@ -349,6 +350,7 @@ def layer_intermediates(layer, T, ws):
         h_block_rows=int(v.h_block_rows),
         y=at(v.y, P * H * 2, torch.bfloat16, (P, H)),
         permutation_in_workspace=bool(v.permutation_in_workspace),
+        route_first=bool(v.route_first),
     )
     if v.permutation_in_workspace:
         out.update(expert_offsets=at(v.expert_offsets, (E + 2) * 4, torch.int32, (E + 2,)),

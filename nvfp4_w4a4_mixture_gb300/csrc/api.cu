@@ -213,6 +213,27 @@ bool pdl_enabled()
     return on;
 }
 
+CUresult encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                          const uint32_t* box, int swizzle_bytes)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
+    if (!fn || rank < 1 || rank > 5) return CUDA_ERROR_NOT_FOUND;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    const CUtensorMapSwizzle sw = swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                  : swizzle_bytes == 32 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                        : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                            uint32_t box1)
 {
@@ -310,6 +331,15 @@ moe_status_t moe_quantize_nvfp4_f32(const float* x, int64_t rows, int64_t K, con
 // Router logits into the workspace: tensor cores above kRouterTcMinT tokens (rows router_tc_ld(E)
 // apart), else the CUDA-core kernel with its fixed summation order (rows E + 1 apart).
 constexpr int kRouterTcMinT = 64;
+// From this many tokens (E = 512, k <= 16) routing runs as one launch that also takes x's maximum
+// (k_router_topk: one CTA per 128 tokens holds all 512 logits of its rows), and the activation
+// encoder follows it.
+constexpr int kFusedRouteMinT = 12288;
+
+static bool fused_route_for(int T, int H, int E, int k)
+{
+    return T >= kFusedRouteMinT && router_topk_fits(H, E, k);
+}
 
 // How moe_layer_forward runs a batch of T tokens: which front half, whether the expert GEMMs
 // build the permutation themselves, their tile schedule and token-block height, and the row
@@ -317,6 +347,7 @@ constexpr int kRouterTcMinT = 64;
 struct LayerPlan {
     bool one_launch_front;  // quantise + route (+ permute) in one launch (small batches)
     bool gemm_permutes;     // the expert GEMMs rank the ids in shared memory (offsets etc. not stored)
+    bool fused_route;       // routing (with x's maximum) in one launch before the activation encoder
     int sched;              // GemmSchedule of the expert-GEMM launch
     int block_rows;         // token rows per block of that schedule (h's scale tiles)
     int logits_ld;          // floats between two tokens' logits in the workspace
@@ -342,6 +373,7 @@ static LayerPlan layer_plan(int H, int E, int k, int I, int T, int sms)
     p.sched = wide ? (T <= 32 ? kSchedWideNarrow : gemm_rows_pays(P, sms) ? kSchedWideRows : kSchedWide)
                    : small ? kSchedWeightsOnM : kSchedActOnM;
     p.block_rows = gemm_schedule_rows(p.sched);
+    p.fused_route = !p.one_launch_front && fused_route_for(T, H, E, k) && router_topk_slots(T) <= kMaxAmaxSlots;
     p.logits_ld = (!p.one_launch_front && T > kRouterTcMinT) ? router_tc_ld(E) : E + 1;
     return p;
 }
@@ -367,6 +399,16 @@ moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int3
     MOE_TRY(check_device());
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* logits = reinterpret_cast<float*>(static_cast<char*>(ws) + W.logits);
+    if (fused_route_for(T, L->H, L->E, L->k)) {
+        MOE_CUDA(launch_router_topk(x, T, L->H, L->E, L->k, L->w_router, L->logit_bias, logits, ld, topk_ids, topk_w,
+                                    shared_g, nullptr, nullptr, 0, &reinterpret_cast<WsHeader*>(ws)->status, s),
+                 "router launch");
+        if (logits_out)
+            MOE_CUDA(cudaMemcpy2DAsync(logits_out, static_cast<size_t>(L->E) * 4, logits, static_cast<size_t>(ld) * 4,
+                                       static_cast<size_t>(L->E) * 4, static_cast<size_t>(T), cudaMemcpyDeviceToDevice, s),
+                     "logits copy");
+        return MOE_OK;
+    }
     MOE_CUDA(route_logits(x, T, L, logits, reinterpret_cast<WsHeader*>(ws), s), "router launch");
     MOE_CUDA(launch_topk(logits, T > kRouterTcMinT ? ld : L->E + 1, T, L->E, L->k, topk_ids, topk_w, shared_g, logits_out, s),
              "top-k launch");
@@ -545,6 +587,23 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
                  "front");
         MOE_CUDA(mark(1), "event record");
         MOE_CUDA(mark(2), "event record");
+    } else if (plan.fused_route) {
+        // routing first: logits, top-k, weights, shared gate and each CTA's max |x| in one launch
+        // (which also zeroes the expert GEMMs' counters), then the W4A4 encoding of x with the
+        // tensor scale reduced from those maxima
+        uint32_t* slots = reinterpret_cast<uint32_t*>(base + W.amax_slots);
+        MOE_CUDA(launch_router_topk(x, T, H, E, k, L->w_router, L->logit_bias, PF(W.logits), plan.logits_ld,
+                                    P32(W.topk_ids), PF(W.topk_w), PF(W.shared_g), slots, P32(W.ready), n_ready + 1,
+                                    &hdr->status, s),
+                 "router");
+        MOE_CUDA(mark(1), "event record");
+        MOE_CUDA(launch_quantize_from_slots(x, T, H, P8(W.x_codes), P8(W.x_sf), &hdr->s_x, slots, router_topk_slots(T),
+                                            sms, s),
+                 "quantize");
+        MOE_CUDA(mark(2), "event record");
+        MOE_CUDA(launch_permute(P32(W.topk_ids), T, k, E, 1, P32(W.offsets), P32(W.perm_src), P32(W.src_perm),
+                                P32(W.row_token), P32(W.hist), &hdr->perm_ticket, &hdr->status, s),
+                 "permute");
     } else {
         // W4A4: quantize the layer input once per token (dynamic tensor scale); the quantizer's first
         // launch also zeroes the counters of the expert GEMMs (no memset between two kernels: each
@@ -656,6 +715,7 @@ moe_status_t moe_layer_workspace_view(const moe_layer_t* L, int T, moe_layer_vie
     v.h_sf = static_cast<int64_t>(W.h_sf);
     v.h_block_rows = plan.block_rows;
     v.y = static_cast<int64_t>(W.y);
+    v.route_first = plan.fused_route ? 1 : 0;
     *view = v;
     return MOE_OK;
 }

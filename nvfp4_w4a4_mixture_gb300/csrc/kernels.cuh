@@ -17,6 +17,9 @@ cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const f
 // The layer's quantizer (dynamic tensor scale): per-CTA maxima in slots (layer_amax_slots(sms) of
 // them), no atomics; it also zeroes zero[0 .. n_zero) for the launches that follow.
 int layer_amax_slots(int sms);
+// The encoding pass alone, its tensor scale reduced from n_slots maxima written by an earlier launch.
+cudaError_t launch_quantize_from_slots(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf,
+                                       float* s_out, const uint32_t* slots, int n_slots, int sms, cudaStream_t stream);
 cudaError_t launch_quantize_layer(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf, float* s_out,
                                   uint32_t* slots, int32_t* zero, int n_zero, int sms, cudaStream_t stream);
 
@@ -34,6 +37,17 @@ cudaError_t launch_topk(const float* logits, int ld, int T, int E, int k, int32_
 int router_tc_ld(int E);
 cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, int E, const uint16_t* w_router, const float* bias,
                                     float* logits, int ld, int* status, cudaStream_t stream);
+
+// ---- router_fused.cu (large batches, E = 512: logits, top-k, weights, shared gate and max |x| in
+// one launch; one CTA per 128 tokens)
+// logits: FP32 [T][ld] (ld >= E + 1, ld % 4 == 0; column E = gate logit). amax_slots (nullable):
+// one max |x| per CTA, as float bits, ceil(T / 128) of them. zero (nullable): zero[0 .. n_zero)
+// is zeroed after the previous launch completes. A bounded wait that runs out sets kDevTimeoutRouter.
+bool router_topk_fits(int H, int E, int k);
+inline int router_topk_slots(int T) { return (T + 127) / 128; }
+cudaError_t launch_router_topk(const uint16_t* x, int T, int H, int E, int k, const uint16_t* w_router, const float* bias,
+                               float* logits, int ld, int32_t* topk_ids, float* topk_w, float* shared_g,
+                               uint32_t* amax_slots, int32_t* zero, int n_zero, int* status, cudaStream_t stream);
 
 // ---- permute.cu
 constexpr int kPermChunk = 512;  // assignments per chunk (one CTA of the permutation kernels)
@@ -151,6 +165,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 void set_last_error_detail(const char* msg);  // text returned by moe_last_error_detail()
 CUresult encode_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
                              uint32_t box_outer);
+CUresult encode_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                          const uint32_t* box, int swizzle_bytes);
 CUresult encode_tmap_3d_u8(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                            uint32_t box1);
 

@@ -257,6 +257,14 @@ cudaError_t launch_quantize_layer(const uint16_t* x, int64_t rows, int64_t K, ui
                       static_cast<const uint32_t*>(slots), grid_a, codes, sf, s_out);
 }
 
+cudaError_t launch_quantize_from_slots(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes, uint8_t* sf,
+                                       float* s_out, const uint32_t* slots, int n_slots, int sms, cudaStream_t stream)
+{
+    const int64_t nblocks = rows * K / 16;
+    return launch_pdl(k_quantize_slots, dim3(quant_grid(nblocks, sms)), dim3(kLayerAmaxThreads), 0, stream, x, nblocks,
+                      slots, n_slots, codes, sf, s_out);
+}
+
 cudaError_t launch_quantize_f32(const float* x, int64_t rows, int64_t K, const float* s_in, uint8_t* codes,
                                 uint8_t* sf, float* s_out, unsigned* amax_scratch, int sms, cudaStream_t stream)
 {

@@ -154,11 +154,12 @@ def test_route_topk(moe, config):
     _check_route_values(w, g, lg, w_ref, g_ref, lg_ref, ids=ids, k=k)
 
 
-@pytest.mark.parametrize("config,T", [("tiny", 65), ("tiny", 130), ("decode", 300), ("decode", 2500)])
+@pytest.mark.parametrize("config,T", [("tiny", 65), ("tiny", 130), ("decode", 300), ("decode", 2500), ("decode", 12365)])
 def test_route_topk_tensor_core_ragged(moe, config, T):
     # more than 64 tokens take the tensor-core router: token blocks of 128 and router-row tiles with
     # ragged edges (E + 1 = 17 and 513); the tile width follows the token count (64 rows while the
-    # CTAs fit one wave, then 96 — 2500 tokens — then 176)
+    # CTAs fit one wave, then 96 — 2500 tokens — then 176). From 12288 tokens with E = 512 the fused
+    # router holds all 512 logits of a 128-token block per CTA (12365: a ragged last block of 77)
     c = wl.CONFIGS[config]
     H, E, k = c["H"], c["E"], c["k"]
     w_r = wl.gen_router(T, E, H)
@@ -553,10 +554,12 @@ def test_device_status_clean(moe):
     moe.moe_read_device_status()
 
 
-@pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 64), ("tiny", 65), ("tiny", 300), ("decode", 300)])
+@pytest.mark.parametrize("name,T", [("tiny", 4), ("tiny", 64), ("tiny", 65), ("tiny", 300), ("decode", 300),
+                                    ("prefill4k", 4096), ("prefill16k", 16384)])
 def test_layer_launch_count(moe, name, T):
     # the kernels one layer call launches, as the CUDA activity trace lists them, against the count the
-    # benchmark reports: 3 for small batches (front half, expert GEMMs, combine), up to 9 otherwise
+    # benchmark reports: 3 for small batches (front half, expert GEMMs, combine), up to 9 otherwise (7
+    # with the fused router of 512 experts from 12288 tokens)
     from torch.autograd import DeviceType
     from torch.profiler import ProfilerActivity, profile
 

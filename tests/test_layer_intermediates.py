@@ -140,6 +140,7 @@ def test_layer_intermediates_tiny(moe, T):
     # over several chunks and the streaming combine
     got = _check_full(moe, I_.layer_case("tiny", seed=T, T=T))
     assert got["permutation_in_workspace"] == (T > 32 or not GEMM_PERMUTES)
+    assert not got["route_first"]
 
 
 def test_layer_intermediates_decode(moe):
@@ -177,6 +178,7 @@ def test_layer_intermediates_prefill_sampled(moe, config, sample):
     codes, sf, S = oracle.quantize_nvfp4(x)
     _check_front(got, case, ids, lg, codes, sf, S)
     assert got["permutation_in_workspace"]
+    assert got["route_first"] == (T >= 12288)  # 512 experts: the fused router, then the encoder
     off, ps, sp = oracle.permute(ids, E)
     np.testing.assert_array_equal(got["expert_offsets"], off)
     np.testing.assert_array_equal(got["perm_src"], ps)
