@@ -253,19 +253,6 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr)
     return d;
 }
 
-// The same for a K-major operand in the 64-byte swizzle layout: rows of 64 bytes, 8-row groups 512
-// bytes apart (the layout a SWIZZLE_64B TMA box writes), layout 4 = 64-byte swizzle.
-__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>(1u) << 16;
-    d |= static_cast<uint64_t>(512u >> 4) << 32;
-    d |= static_cast<uint64_t>(1u) << 46;
-    d |= static_cast<uint64_t>(4u) << 61;
-    return d;
-}
-
 // Descriptor of a 32-row x 16-byte block (no swizzle; 8-row x 16-byte core matrices 128 bytes
 // apart) for tcgen05.cp of scale factors.
 __device__ __forceinline__ uint64_t sdesc_sf(uint32_t saddr)
