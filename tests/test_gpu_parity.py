@@ -113,6 +113,56 @@ def test_quantize_static_scale_edge_values(moe):
         np.testing.assert_array_equal(codes.cpu().numpy(), c_ref)
 
 
+def _boundary_blocks(S, n_blocks, seed):
+    """FP32 blocks whose quotients v / d lie on and within 3 FP32 ulps of the E2M1 rounding boundaries
+    (midpoints and grid values), and whose amax / (6 S) lies on and near UE4M3 midpoints, for a static
+    tensor scale S."""
+    rng = np.random.default_rng(seed)
+    S = np.float32(S)
+    six_s = np.float32(np.float32(6.0) * S)
+    e2m1_edges = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    e4m3 = [1.0, 1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875, 2.0]
+
+    def step(v, k):
+        v = np.float32(v)
+        for _ in range(abs(k)):
+            v = np.nextafter(v, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+        return v
+
+    out = np.zeros((n_blocks, 16), np.float32)
+    for b in range(n_blocks):
+        lo = rng.integers(0, len(e4m3) - 1)
+        scale = np.float32(2.0 ** rng.integers(-6, 4))
+        if b % 2:
+            q = np.float32((e4m3[lo] + e4m3[lo + 1]) / 2) * scale  # an UE4M3 midpoint
+        else:
+            q = np.float32(e4m3[lo]) * scale
+        amax = step(np.float32(q * six_s), int(rng.integers(-3, 4)))
+        dsf = np.float32(q)  # the scale the block should get, up to the rounding being probed
+        d = np.float32(dsf * S)
+        out[b, 0] = amax * (1 if rng.random() < 0.5 else -1)
+        for i in range(1, 16):
+            m = e2m1_edges[rng.integers(0, len(e2m1_edges))]
+            v = step(np.float32(np.float32(m) * d), int(rng.integers(-3, 4)))
+            v = min(v, np.float32(abs(out[b, 0])))  # amax stays the block's maximum
+            out[b, i] = v * (1 if rng.random() < 0.5 else -1)
+        rng.shuffle(out[b])
+    return out
+
+
+@pytest.mark.parametrize("S,n_blocks", [(0.1, 3000), (0.013, 6000), (1.0 / 3.0, 300)])
+def test_quantize_codes_at_rounding_boundaries(moe, S, n_blocks):
+    # the encoder decides codes from products with a correctly rounded reciprocal and divides only
+    # when a quotient is within about 2^-20 of a rounding boundary: quotients placed on and a few
+    # ulps around every boundary must give the oracle's codes and scales bit for bit (3000 and 6000
+    # blocks take the two-launch quantizer, 300 the one-CTA one)
+    x = _boundary_blocks(S, n_blocks, seed=n_blocks).reshape(-1, 64)
+    c_ref, s_ref, _ = oracle.quantize_nvfp4(x, s_in=S)
+    codes, sf, _ = moe.moe_quantize_nvfp4(dev(x), s_in=dev(np.array([S], np.float32)))
+    np.testing.assert_array_equal(sf.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(codes.cpu().numpy(), c_ref)
+
+
 # ------------------------------------------------------------------------------------------------
 # router
 # ------------------------------------------------------------------------------------------------
