@@ -305,6 +305,28 @@ def test_route_topk_tied_groups(moe, E, n_tied, T):
     assert np.all(w.cpu().numpy() == np.float32(1.0 / k))
 
 
+@pytest.mark.parametrize("n_tied", [40, 200, 512])
+def test_route_topk_tied_groups_fused(moe, n_tied):
+    # the fused router of 512 experts (from 12288 tokens; 12365: a ragged last block): 40 equal logits
+    # fit a row's candidate list, 200 and 512 overflow it and the whole warp inserts from a second
+    # pass over the accumulator; the lowest ids among the tied experts win, in id order
+    E, H, k, T = 512, 256, 10, 12365
+    w_r, bias, tied = _tied_router(E + n_tied, E, H, n_tied)
+    if n_tied == E:
+        w_r[:E] = 0.0
+        bias[:] = 0.0
+    x = wl.gen_x(8, T, H)
+    ids_ref, _, _, _ = oracle.router(x, w_r, k, bias=bias.astype(np.float64))
+    np.testing.assert_array_equal(ids_ref, np.broadcast_to(tied[:k], (T, k)))
+    dummy = (torch.zeros(1, 1, 8, dtype=torch.uint8, device="cuda"),) * 2 + (torch.ones(1, 2, device="cuda"),)
+    layer = moe.MoeLayer(H, E, k, 128, bf16_dev(w_r), dummy, dummy, torch.ones(E + 1, device="cuda"),
+                         logit_bias=dev(bias), prepacked=True)
+    ids, w, _, _ = moe.moe_route_topk(bf16_dev(x), layer)
+    moe.moe_read_device_status()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.all(w.cpu().numpy() == np.float32(1.0 / k))
+
+
 @pytest.mark.parametrize("n_tied", [40, 70])
 def test_layer_decode_tied_router(moe, n_tied):
     # the one-launch front half (T = 4) on tied logits: its own top-k must pick the same experts
