@@ -79,7 +79,7 @@ typedef struct {
 typedef struct {
     int H, E, k, I;
     const uint16_t* w_router;   /* bf16 [E+1][H]; row E = shared-expert gate vector */
-    const float* logit_bias;    /* nullable, FP32 [E], added to the routed logits */
+    const float* logit_bias;    /* nullable, FP32 [E], 16-byte aligned, added to the routed logits */
     moe_nvfp4_bank_t w_gate_up; /* G = E+1, N = 2I, K = H, prepacked with gate/up interleave; gscale [E+1][2] (gate, up) */
     moe_nvfp4_bank_t w_down;    /* G = E+1, N = H, K = I, prepacked plain; gscale [E+1] */
     const float* s_mid;         /* FP32 [E+1]: static tensor scale of the intermediate h per expert */

@@ -392,7 +392,8 @@ moe_status_t moe_route_topk(const uint16_t* x, int T, const moe_layer_t* L, int3
     if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
     if (T == 0) return MOE_OK;  // an empty batch: nothing is read or written, the pointers may be NULL
     if (!x || !L->w_router || !topk_ids || !topk_w) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
-    if (!aligned(x, 16) || !aligned(L->w_router, 16)) return fail(MOE_ERR_MISALIGNED, "x and w_router must be 16-byte aligned");
+    if (!aligned(x, 16) || !aligned(L->w_router, 16) || (L->logit_bias && !aligned(L->logit_bias, 16)))
+        return fail(MOE_ERR_MISALIGNED, "x, w_router and logit_bias must be 16-byte aligned");
     const WsLayout W = ws_layout(L->H, L->E, L->k, L->I, T);
     const int ld = router_tc_ld(L->E);
     MOE_TRY(check_ws(ws, ws_bytes, W.logits + static_cast<size_t>(T) * ld * 4));
@@ -545,8 +546,9 @@ moe_status_t moe_layer_forward_profiled(const moe_layer_t* L, const uint16_t* x,
     if (T < 0) return fail(MOE_ERR_UNSUPPORTED_SHAPE, "T=%d < 0", T);
     if (T == 0 && n_events == 0) return MOE_OK;  // an empty batch: nothing is read or written, the pointers may be NULL
     if (!x || !out || !L->w_router || !L->s_mid) return fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
-    if (!aligned(x, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)) || !aligned(L->w_router, 16))
-        return fail(MOE_ERR_MISALIGNED, "x, out, residual and w_router must be 16-byte aligned");
+    if (!aligned(x, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)) || !aligned(L->w_router, 16) ||
+        (L->logit_bias && !aligned(L->logit_bias, 16)))
+        return fail(MOE_ERR_MISALIGNED, "x, out, residual, w_router and logit_bias must be 16-byte aligned");
     if (x == out) return fail(MOE_ERR_INVALID_ARG, "out must not alias x");
     MOE_TRY(check_bank(&L->w_gate_up, "w_gate_up"));
     MOE_TRY(check_bank(&L->w_down, "w_down"));

@@ -59,8 +59,9 @@ extern "C" moe_status_t moe_route_topk_noalloc(const uint16_t* x, int T, const m
     if (T > kNoallocMaxTokens)
         return noalloc_fail(MOE_ERR_UNSUPPORTED_SHAPE, "T > 64: the no-allocation router holds logits for at most 64 tokens");
     if (!x || !L->w_router || !topk_ids || !topk_w) return noalloc_fail(MOE_ERR_INVALID_ARG, "NULL tensor pointer");
-    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(L->w_router)) % 16)
-        return noalloc_fail(MOE_ERR_MISALIGNED, "x and w_router must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(L->w_router) | reinterpret_cast<uintptr_t>(L->logit_bias)) %
+        16)
+        return noalloc_fail(MOE_ERR_MISALIGNED, "x, w_router and logit_bias must be 16-byte aligned");
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();

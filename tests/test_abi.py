@@ -108,6 +108,9 @@ def test_layer_validation(L):
     assert f(ctypes.byref(bad), _fake(p), 4, None, _fake(p + 4096), ws, need, None) == MOE_ERR_UNSUPPORTED_SHAPE
     assert f(ctypes.byref(good), _fake(p), 4, None, _fake(p + 4096), ws, need - 256, None) == MOE_ERR_WORKSPACE_TOO_SMALL
     assert f(ctypes.byref(good), _fake(p + 8), 4, None, _fake(p + 4096), ws, need, None) == MOE_ERR_MISALIGNED
+    biased = m.LayerDesc(2048, 512, 10, 768, p, p + 4, bank, bank, p)  # the logit bias is read 16 bytes at a time
+    assert f(ctypes.byref(biased), _fake(p), 4, None, _fake(p + 4096), ws, need, None) == MOE_ERR_MISALIGNED
+    assert b"logit_bias" in L.moe_last_error_detail()
     assert f(ctypes.byref(good), _fake(p), 4, None, _fake(p), ws, need, None) == MOE_ERR_INVALID_ARG
     assert f(ctypes.byref(good), _fake(p), -1, None, _fake(p + 4096), ws, need, None) == MOE_ERR_UNSUPPORTED_SHAPE
     nullbank = m.NvFp4Bank(p, None, p)
