@@ -496,34 +496,79 @@ def measure(m, name, K, W, args, d):
         first, second = stage_us.pop("quantize"), stage_us.pop("route")
         stage_us = {"route (with max |x|)": first, "quantize (encode)": second, **stage_us}
 
-    # ---- end to end through the public call: pinned host input -> layer -> pinned host output
+    # ---- end to end through the public calls: pinned host input -> layer -> pinned host output.
+    # Small batches and the stack: one step at a time on one stream, L2 flushed before each step
+    # (outside its interval): moe_layer_forward_host (the library enqueues both copies and the layer)
+    # for one layer; the input copied in once, the layers, the last output copied back for a stack.
+    # Large batches (one layer, T >= 1024): two steps in flight on two streams, each with its own
+    # device buffers and workspace, as a serving loop runs them: a step's input copy and the previous
+    # step's output copy overlap the other step's kernels, and each step's layer waits for the
+    # previous step's layer (so the kernels of two steps never share the GPU); the interval covers all
+    # Ke steps, every one of which copies its input in and its output out inside it (no L2 flush: a
+    # step's expert weights, 0.4 GB and more at these sizes, exceed the 126 MB L2 by themselves).
     x_h = x.cpu().pin_memory()
-    out_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    n_str = 2 if (L == 1 and T >= 1024) else 1
+    out_h = [torch.empty(T, H, dtype=torch.bfloat16).pin_memory() for _ in range(n_str)]
     Ke = min(K, 1000)
-    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
-    x_dev = torch.empty_like(x)
-    # one layer: the library's host-buffer call (it enqueues both copies and the layer); a stack: the
-    # input copied in once, the layers on the device, the last output copied back
-    e2e_call = "moe_layer_forward_host" if L == 1 else "copy in + %d x moe_layer_forward + copy out" % L
-    ws_h = m.Workspace(m.moe_workspace_bytes_host(H, E, k, I, T)) if L == 1 else None
-    with torch.cuda.stream(stream):
+    x_dev = [torch.empty_like(x) for _ in range(n_str)]
+    streams = [stream] + [torch.cuda.Stream() for _ in range(n_str - 1)]
+    if n_str == 1:
+        e2e_call = "moe_layer_forward_host" if L == 1 else "copy in + %d x moe_layer_forward + copy out" % L
+        ws_h = m.Workspace(m.moe_workspace_bytes_host(H, E, k, I, T)) if L == 1 else None
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(Ke)]
+        with torch.cuda.stream(stream):
+            for i in range(Ke):
+                flush_l2()
+                ee[i][0].record(stream)
+                if L == 1:
+                    m.moe_layer_forward_host(layers[0], x_h, out=out_h[0], ws=ws_h)
+                else:
+                    x_dev[0].copy_(x_h, non_blocking=True)
+                    cur = x_dev[0]
+                    for li, lay in enumerate(layers):
+                        o = bufs[li % 2]
+                        m.moe_layer_forward(lay, cur, residual=cur, out=o, ws=ws)
+                        cur = o
+                    out_h[0].copy_(cur, non_blocking=True)
+                ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = d.max(statistics.mean(a.elapsed_time(b) for a, b in ee))
+        e2e_ws = [ws_h or ws]
+    else:
+        e2e_call = "copy in + moe_layer_forward + copy out, two steps in flight on two streams"
+        e2e_ws = [ws] + [m.Workspace(layers[0].workspace_bytes(T)) for _ in range(n_str - 1)]
+        out_dev = [torch.empty_like(x) for _ in range(n_str)]
+        layer_done = [torch.cuda.Event() for _ in range(n_str)]
+
+        def e2e_step(i):
+            j, jp = i % n_str, (i - 1) % n_str
+            sj = streams[j]
+            with torch.cuda.stream(sj):
+                x_dev[j].copy_(x_h, non_blocking=True)
+                if i > 0:
+                    sj.wait_event(layer_done[jp])  # the previous step's layer has finished
+                m.moe_layer_forward(layers[0], x_dev[j], out=out_dev[j], ws=e2e_ws[j])
+                layer_done[j].record(sj)
+                out_h[j].copy_(out_dev[j], non_blocking=True)
+
+        for i in range(W):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_side = [torch.cuda.Event() for _ in streams[1:]]
+        e_start.record(streams[0])
+        for sd in streams[1:]:
+            sd.wait_event(e_start)
         for i in range(Ke):
-            flush_l2()
-            ee[i][0].record(stream)
-            if L == 1:
-                m.moe_layer_forward_host(layers[0], x_h, out=out_h, ws=ws_h)
-            else:
-                x_dev.copy_(x_h, non_blocking=True)
-                cur = x_dev
-                for li, lay in enumerate(layers):
-                    o = bufs[li % 2]
-                    m.moe_layer_forward(lay, cur, residual=cur, out=o, ws=ws)
-                    cur = o
-                out_h.copy_(cur, non_blocking=True)
-            ee[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = d.max(statistics.mean(a.elapsed_time(b) for a, b in ee))
-    m.moe_read_device_status(ws_h or ws)
+            e2e_step(i)
+        for sd, ev in zip(streams[1:], e_side):
+            ev.record(sd)
+            streams[0].wait_event(ev)
+        e_end.record(streams[0])
+        torch.cuda.synchronize()
+        e2e_ms = d.max(e_start.elapsed_time(e_end) / Ke)
+    for w in e2e_ws:
+        m.moe_read_device_status(w)
 
     # ---- roofline of the dominant kernel (the expert GEMMs, one launch) and of the whole step
     hbm, bf16_burst, bf16_sus, peak_src = measured_peaks()
@@ -560,7 +605,8 @@ def measure(m, name, K, W, args, d):
         "stages_timed_by": "stream events at the stage boundaries, each step queued behind a spin kernel",
         "step_ms_median": statistics.median(step_ms),
         "e2e": {"value": d.world * T / (e2e_ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
-                "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms, "cuda_graph": False, "call": e2e_call},
+                "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms, "cuda_graph": False, "call": e2e_call,
+                "streams": n_str},
         "gpu_launches": K * L * launches_per_layer(c),
         "clocks": clk,
     }
