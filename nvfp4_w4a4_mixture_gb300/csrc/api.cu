@@ -62,7 +62,9 @@ struct WsLayout {
     size_t hdr, amax_slots, topk_ids, topk_w, shared_g, logits, x_codes, x_sf, offsets, perm_src, src_perm, row_token,
         hist, h_codes, h_sf, ready, y, total;
 };
-constexpr int kMaxAmaxSlots = 4096;  // >= layer_amax_slots(SM count) on any device this library runs on
+// per-CTA maxima of |x|: the layer quantizer's (layer_amax_slots(SM count) of them, far below this on
+// any device this library runs on) or the fused router's (one per 128 tokens: up to 524,288 tokens)
+constexpr int kMaxAmaxSlots = 4096;
 
 WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
 {
@@ -75,7 +77,7 @@ WsLayout ws_layout(int64_t H, int64_t E, int64_t k, int64_t I, int64_t T)
     };
     const int64_t n = T * k, P = T * k + T;
     L.hdr = take(sizeof(WsHeader));
-    L.amax_slots = take(kMaxAmaxSlots * 4);  // the layer quantizer's per-CTA maxima
+    L.amax_slots = take(kMaxAmaxSlots * 4);  // per-CTA maxima of |x| (quantizer or fused router)
     L.topk_ids = take(n * 4);
     L.topk_w = take(n * 4);
     L.shared_g = take(T * 4);
