@@ -33,6 +33,9 @@ CONFIGS = {
     "stack48": dict(H=2048, E=512, k=10, I=768, T=2048, router="uniform", layers=48),
     # the decode call through the same 48-layer stack: 4 tokens per layer, one graph for all layers
     "decode_stack48": dict(H=2048, E=512, k=10, I=768, T=4, router="uniform", layers=48),
+    # parity-size layer with the routed-expert count of the full layer and a batch that takes the
+    # fused router (12,288 tokens and more), ragged in its last 128-token block
+    "wide_router": dict(H=256, E=512, k=10, I=128, T=12365, router="uniform", layers=1),
 }
 
 CALIBRATION_FILE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),

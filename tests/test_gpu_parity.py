@@ -204,12 +204,14 @@ def test_route_topk(moe, config):
     _check_route_values(w, g, lg, w_ref, g_ref, lg_ref, ids=ids, k=k)
 
 
-@pytest.mark.parametrize("config,T", [("tiny", 65), ("tiny", 130), ("decode", 300), ("decode", 2500), ("decode", 12365)])
+@pytest.mark.parametrize("config,T", [("tiny", 65), ("tiny", 130), ("decode", 300), ("decode", 2500), ("decode", 12365),
+                                      ("wide_router", 20000)])
 def test_route_topk_tensor_core_ragged(moe, config, T):
     # more than 64 tokens take the tensor-core router: token blocks of 128 and router-row tiles with
     # ragged edges (E + 1 = 17 and 513); the tile width follows the token count (64 rows while the
     # CTAs fit one wave, then 96 — 2500 tokens — then 176). From 12288 tokens with E = 512 the fused
-    # router holds all 512 logits of a 128-token block per CTA (12365: a ragged last block of 77)
+    # router holds all 512 logits of a 128-token block per CTA (12365: a ragged last block of 77;
+    # 20000: 157 CTAs, more than one per SM)
     c = wl.CONFIGS[config]
     H, E, k = c["H"], c["E"], c["k"]
     w_r = wl.gen_router(T, E, H)

@@ -13,9 +13,12 @@ Bars:
   >= 99.9 %  the requantised intermediate h (codes and block scales), row by row in permuted order:
              for small batches the expert GEMMs build the permutation in shared memory, so h at
              the oracle's permuted positions also checks that permutation;
-  per row    y, the down projection of every assignment (t, j) in assignment order, within 5e-2 of
-             the oracle's row for expert ids[t][j] (a row computed in the wrong expert group is off
-             by about 1.4), and within 1e-2 over all rows.
+  per row    y, the down projection of every assignment (t, j) in assignment order, against the
+             oracle's row for expert ids[t][j]: within 1e-2 where the assignment's h row (codes and
+             scales) equals the oracle's, within 0.25 where one of its h codes differs (the
+             requantisation may differ in 0.1 % of codes; with I = 128 one differing code moves a row
+             by a few percent), and within 1e-2 over all rows. A row computed in the wrong expert
+             group is off by about 1.4.
 """
 import os
 
@@ -34,7 +37,8 @@ GEMM_PERMUTES = os.environ.get("MOE_NVFP4_GEMM_PERMUTE", "1")[:1] != "0"
 LOGIT_TOL = 1e-4
 W_TOL = 1e-6
 CODE_MATCH = 0.999
-Y_ROW_TOL = 5e-2
+Y_ROW_TOL = 1e-2      # rows whose h equals the oracle's
+Y_ROW_TOL_H = 0.25    # rows with a differing h code
 Y_TOL = 1e-2
 
 
@@ -97,18 +101,24 @@ def _check_front(got, case, ref_ids, ref_logits, ref_codes, ref_sf, ref_S):
 
 
 def _check_rows(got, ref, gpu_pos, ref_pos, gpu_assign, ref_assign, offsets, I):
-    """h at permuted rows (GPU positions vs the oracle's), y at assignment rows."""
+    """Entry i of the four index arrays is one assignment: its h row (permuted positions, the GPU's
+    and the oracle's) and its y row (the GPU's in assignment order, the oracle's)."""
     hc = nibbles(got["h_codes"][gpu_pos])
     hc_ref = nibbles(ref["h_codes"][ref_pos])
     match = float(np.mean(hc == hc_ref))
     assert match >= CODE_MATCH, match
     hs = _scale_tile_bytes(got["h_sf"], offsets, got["h_block_rows"], gpu_pos, I // 16)
-    smatch = float(np.mean(hs == ref["h_sf"][ref_pos]))
+    hs_ref = ref["h_sf"][ref_pos]
+    smatch = float(np.mean(hs == hs_ref))
     assert smatch >= CODE_MATCH, smatch
+    h_same = np.all(hc == hc_ref, axis=1) & np.all(hs == hs_ref, axis=1)
     y = got["y"][gpu_assign].astype(np.float64)
     y_ref = ref["y"][ref_assign]
     row_err = np.linalg.norm(y - y_ref, axis=1) / np.maximum(np.linalg.norm(y_ref, axis=1), 1e-30)
-    assert np.max(row_err) <= Y_ROW_TOL, (int(np.argmax(row_err)), float(np.max(row_err)))
+    if np.any(h_same):
+        e = row_err[h_same]
+        assert np.max(e) <= Y_ROW_TOL, (int(np.flatnonzero(h_same)[np.argmax(e)]), float(np.max(e)))
+    assert np.max(row_err) <= Y_ROW_TOL_H, (int(np.argmax(row_err)), float(np.max(row_err)))
     assert I_.rel_frobenius(y, y_ref) <= Y_TOL
 
 
@@ -126,9 +136,10 @@ def _check_full(moe, case):
         np.testing.assert_array_equal(got["src_perm"], ref["src_perm"])
         np.testing.assert_array_equal(got["row_token"], ref["row_token"])
     P = T * k + T
-    assign = np.arange(P)
-    ref_assign = np.concatenate([ref["src_perm"], np.arange(T * k, P)])  # y is in assignment order
-    _check_rows(got, ref, np.arange(P), np.arange(P), assign, ref_assign, ref["offsets"], I)
+    # assignment a: h at permuted position src_perm[a] (the shared rows at T*k + t in both orders),
+    # y at row a on the GPU (assignment order) and at that permuted position in the oracle's y
+    pos = np.concatenate([ref["src_perm"], np.arange(T * k, P)])
+    _check_rows(got, ref, pos, pos, np.arange(P), pos, ref["offsets"], I)
     return got
 
 
@@ -141,6 +152,14 @@ def test_layer_intermediates_tiny(moe, T):
     got = _check_full(moe, I_.layer_case("tiny", seed=T, T=T))
     assert got["permutation_in_workspace"] == (T > 32 or not GEMM_PERMUTES)
     assert not got["route_first"]
+
+
+def test_layer_intermediates_fused_router(moe):
+    # 512 experts and 12,365 tokens (H 256, I 128): the fused router first (logits, top-k, weights,
+    # shared gate and x's maximum), then the encoder, the permutation, the expert GEMMs and the
+    # combine; every token against the oracle, the last 128-token block ragged (77 tokens)
+    got = _check_full(moe, I_.layer_case("wide_router"))
+    assert got["route_first"] and got["permutation_in_workspace"]
 
 
 def test_layer_intermediates_decode(moe):
