@@ -24,6 +24,12 @@ def test_s_mid_tiny_reproduces(orc):
     assert _gen().s_mid_for_shape(256, 16, 2, 128) == _stored()["s_mid_tiny"]
 
 
+def test_s_mid_flash_reproduces(orc):
+    # the Flash-shaped layer's intermediate scale (H 2048, E 512, k 10, I 768; about a minute of
+    # oracle work: the touched experts' weights quantised, the gate/up GEMM and SwiGLU of 256 tokens)
+    assert _gen().s_mid_for_shape(2048, 512, 10, 768) == _stored()["s_mid_flash"]
+
+
 def test_hot_beta_gives_half_the_assignments(orc):
     # the stored bias gives the first 10 % of the 512 experts 50 % of the top-10 assignments of the
     # calibration batch (1024 tokens), and a slightly smaller bias gives them less
