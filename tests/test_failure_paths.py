@@ -79,7 +79,8 @@ def test_layer_parity_under_environment_switch(env):
     key, val = env.split("=")
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                         "tests/test_gpu_parity.py", "tests/test_layer_intermediates.py",
-                        "-k", "layer_tiny or layer_decode_full_size or intermediates_tiny or intermediates_decode"],
+                        "-k", "layer_tiny or layer_decode_full_size or intermediates_tiny or intermediates_decode"
+                              " or intermediates_fused_router"],
                        cwd=ROOT, env={**os.environ, key: val}, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
     assert " passed" in r.stdout
