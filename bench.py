@@ -51,7 +51,8 @@ METRIC = "MoE-layer tokens/s (NVFP4 W4A4) at 1 GB300; % of FP4-TC / HBM roofline
 DEFAULT_CONFIG = "prefill16k"
 EXTRA_CONFIGS = ("decode", "decode_stack48", "stack48")
 DEFAULT_STEPS = {"tiny": 2000, "decode": 5000, "prefill4k": 600, "prefill16k": 400, "stack48": 30,
-                 "decode_stack48": 200, "wide_router": 300}
+                 "decode_stack48": 200, "wide_router": 300, "max_hidden": 500, "max_inter": 500,
+                 "max_experts_k": 500}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense FP4 : BF16 tensor-core ratio

@@ -36,6 +36,10 @@ CONFIGS = {
     # parity-size layer with the routed-expert count of the full layer and a batch that takes the
     # fused router (12,288 tokens and more), ragged in its last 128-token block
     "wide_router": dict(H=256, E=512, k=10, I=128, T=12365, router="uniform", layers=1),
+    # parity cases at the shape limits: hidden size 8192, intermediate size 8192, 1024 experts with top-32
+    "max_hidden": dict(H=8192, E=16, k=2, I=128, T=70, router="uniform", layers=1),
+    "max_inter": dict(H=256, E=16, k=2, I=8192, T=70, router="uniform", layers=1),
+    "max_experts_k": dict(H=256, E=1024, k=32, I=128, T=70, router="uniform", layers=1),
 }
 
 CALIBRATION_FILE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),

@@ -162,6 +162,14 @@ def test_layer_intermediates_fused_router(moe):
     assert got["route_first"] and got["permutation_in_workspace"]
 
 
+@pytest.mark.parametrize("config", ["max_hidden", "max_inter", "max_experts_k"])
+def test_layer_intermediates_shape_limits(moe, config):
+    # the largest supported shapes on small batches (70 tokens, the separate front launches): H = 8192
+    # (router and gate/up K = 8192), I = 8192 (gate/up N = 16384, down K = 8192), E = 1024 with k = 32
+    got = _check_full(moe, I_.layer_case(config))
+    assert got["permutation_in_workspace"] and not got["route_first"]
+
+
 def test_layer_intermediates_decode(moe):
     # the benchmarked decode step: k_decode_front (quantise, logits, top-k), then the expert GEMMs
     # whose every CTA ranks the ids in shared memory
