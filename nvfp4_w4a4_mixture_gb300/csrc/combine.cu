@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     ptx::griddep_wait();  // y comes from the launch before this one
     if (warp == kStreamWarps) {
         if (lane == 0) {
-            int i = 0;
+            uint32_t i = 0;
             for (int t = blockIdx.x; t < T; t += gridDim.x, ++i) {
                 const int b = i % kStreamBufs;
                 const uint32_t ph = (i / kStreamBufs) & 1;
@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
                     ptx::bulk_load(buf + (k + 1) * row_bytes, residual + static_cast<int64_t>(t) * H,
                                    static_cast<uint32_t>(row_bytes), &full[b]);
             }
+            if (!ptx::ring_drain(full, kStreamBufs, i)) record_status(status, kDevTimeoutCombine);
         }
     } else {
         int i = 0;

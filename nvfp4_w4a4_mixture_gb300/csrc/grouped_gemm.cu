@@ -627,6 +627,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         if (lane == 0) {
             int s = 0;
             uint32_t ph = 0, rph = 0;  // rph: phase bit of each resident slab's free barrier
+            uint32_t fills = 0, rfilled = 0;  // stage fills issued; resident slabs ever filled
             bool ok = true;
             // tiles in the order the CTAs come for them (phase-0 tiles first): a CTA whose tiles
             // run short takes more, and the down tiles go out in the order their inputs complete
@@ -656,6 +657,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     for (int kt = 0; kt < k_stages; ++kt) {
                         if (!ptx::mbar_wait(&st.r_empty[kt], ((rph >> kt) & 1u) ^ 1u)) { set_abort(st, a.status); ok = false; break; }
                         rph ^= 1u << kt;
+                        rfilled |= 1u << kt;
                         const int nat = min(4, kb64 - kt * 4);
                         ptx::mbar_arrive_expect_tx(&st.r_full[kt], LY::W_BYTES + nat * SF_TILE);
                         ptx::tma_load_3d(smem + LY::B_OFF + kt * LY::W_BYTES, tm, &st.r_full[kt], 0, ti.nb * W_ROWS,
@@ -682,11 +684,18 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                             ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sf_src + static_cast<int64_t>(j) * kb64 * SF_TILE,
                                            nat * SF_TILE, &st.full[s]);
                         sf_src += 4 * SF_TILE;
+                        ++fills;
                         if (++s == C::STAGES) { s = 0; ph ^= 1; }
                     }
                 }
                 L = L_next;
             }
+            // no copy of this thread writes shared memory after the CTA exits: every stage's and
+            // resident slab's last fill has landed (at once on the normal path, where all were consumed)
+            bool drained = ptx::ring_drain(st.full, C::STAGES, fills);
+            for (int kt = 0; kt < 8; ++kt)
+                if ((rfilled >> kt) & 1u) drained = ptx::mbar_wait(&st.r_full[kt], ((rph >> kt) & 1u) ^ 1u) && drained;
+            if (!drained) set_abort(st, a.status);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer

@@ -77,6 +77,25 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
     }
 }
 
+// The tail of a thread that fills a ring of n stages in order (fill i goes to stage i % n and
+// completes phase i / n of full[i % n]): wait until the last fill of every stage has completed, so
+// that none of this thread's copies writes shared memory after the CTA exits. On the normal path
+// every fill has been consumed and this returns at once; after a timeout elsewhere a phase may lack
+// another thread's arrival, and the whole tail gives up after one kWaitLimitNs (false).
+__device__ __forceinline__ bool ring_drain(uint64_t* full, int n, uint32_t fills)
+{
+    const uint32_t round = fills / n;
+    const int next = static_cast<int>(fills % n);
+    const uint64_t t0 = globaltimer();
+    for (int j = 0; j < n && static_cast<uint32_t>(j) < fills; ++j) {
+        // the stage's last fill is in the current round (j < next) or the one before
+        const uint32_t parity = (j < next ? round : round - 1) & 1u;
+        while (!mbar_try_wait(full + j, parity))
+            if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------------------------------------
 // Programmatic dependent launch: a kernel launched with programmatic stream serialisation may start
 // before the previous kernel on the stream has finished. griddep_wait() blocks until that kernel has

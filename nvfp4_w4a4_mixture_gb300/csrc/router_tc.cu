@@ -79,9 +79,9 @@ __global__ void __launch_bounds__(kRtThreads, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            int s = 0;
+            int s = 0, kt = 0;
             uint32_t ph = 0;
-            for (int kt = 0; kt < n_k; ++kt) {
+            for (; kt < n_k; ++kt) {
                 if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { fail(); break; }
                 uint8_t* sb = smem + s * kRtStageBytes;
                 ptx::mbar_arrive_expect_tx(&st.full[s], kRtStageBytes);
@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kRtThreads, 1)
                 ptx::tma_load_2d(sb + kRtABytes, &tmap_w, &st.full[s], kt * 64, nt * kRtN);
                 if (++s == kRtStages) { s = 0; ph ^= 1; }
             }
+            if (!ptx::ring_drain(st.full, kRtStages, kt)) fail();
         }
     } else if (warp == 1) {
         if (lane == 0) {
