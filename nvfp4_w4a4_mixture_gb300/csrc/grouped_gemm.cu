@@ -69,14 +69,14 @@ template <>
 struct Cfg<kModeActM> {                    // activations on the MMA's M side, 128 weight rows on N
     static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 6, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = false, SPLIT = false;
     static constexpr int MAX_K = 16384;
 };
 template <>
 struct Cfg<kModeSwap> {                    // weights on the MMA's M side, 32 activation rows on N
     static constexpr int ACT_ROWS = 32, W_ROWS = 128, STAGES = 8, EPI_WARPS = 4, ACC_COLS = 32, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 32;
-    static constexpr bool SWAP = true, XCHG = false, ROWS = false, WRES = false;
+    static constexpr bool SWAP = true, XCHG = false, ROWS = false, WRES = false, SPLIT = false;
     static constexpr int MAX_K = 16384;
 };
 template <>
@@ -85,7 +85,8 @@ struct Cfg<kModeWide> {                    // activations on M, 256 weight rows 
     // one buffer only, so the epilogue frees it as soon as its rows are in registers
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = false;
+    // (two MMA threads here would each copy the activation scales every K-step: measured slower)
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = false, SPLIT = false;
     static constexpr int MAX_K = 16384;
 };
 
@@ -97,17 +98,18 @@ struct Cfg<kModeWideNarrow> {              // wide, for token blocks of at most 
     // finish it; four stages keep the ring as fast as five did
     static constexpr int ACT_ROWS = 32, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = true, ROWS = false, WRES = false;
+    static constexpr bool SWAP = false, XCHG = true, ROWS = false, WRES = false, SPLIT = false;
     static constexpr int MAX_K = 16384;
 };
 template <>
 struct Cfg<kModeWideRows> {                // wide tiles taken a whole token block at a time: one CTA runs
                                            // every weight block of the token block in turn, and the
                                            // activation scales of the whole K stay in tensor memory
-                                           // after the first (two scale copies per K-step, not three)
+                                           // after the first; two MMA threads, each issuing one
+                                           // weight scale copy and one 128 x 128 MMA per K-step
     static constexpr int ACT_ROWS = 128, W_ROWS = 256, STAGES = 4, EPI_WARPS = 8, ACC_COLS = 256, ACC_BUFS = 1;
     static constexpr int MMA_M = 128, MMA_N = 256;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = true, WRES = false;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = true, WRES = false, SPLIT = true;
     static constexpr int MAX_K = 2048;     // resident activation scales: 4 columns per 64 of K
 };
 template <>
@@ -118,7 +120,7 @@ struct Cfg<kModeWRes> {                    // weight-resident units: one expert'
                                            // accumulators, so the epilogue of one block overlaps the next
     static constexpr int ACT_ROWS = 128, W_ROWS = 128, STAGES = 3, EPI_WARPS = 8, ACC_COLS = 128, ACC_BUFS = 2;
     static constexpr int MMA_M = 128, MMA_N = 128;
-    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = true;
+    static constexpr bool SWAP = false, XCHG = false, ROWS = false, WRES = true, SPLIT = false;
     static constexpr int MAX_K = 2048;     // weight slabs (8 x 18 KB) and their scales (128 columns)
 };
 
@@ -143,6 +145,9 @@ struct Lay {
     static constexpr int B_SF_OFF = B_OFF + MAX_SLABS * W_BYTES;
     static constexpr int TAIL_OFF = B_SF_OFF + MAX_SLABS * WB * SF_STAGE;
     static constexpr int THREADS = 128 + 32 * C::EPI_WARPS;
+    // SPLIT: warp 0 is a second MMA thread (each owns 128 of the tile's 256 weight rows) and the
+    // first activation producer warp also loads the weights
+    static constexpr int MMA_THREADS = C::SPLIT ? 2 : 1;
     static constexpr int SF_COL = C::ACC_BUFS * C::ACC_COLS;  // first scale-factor column
     static constexpr int SFW_STEP_COLS = 4 * WB;               // weight scale columns per K-step
     // per stage: 4 K-steps of weight scales, and of activation scales unless they are resident
@@ -177,6 +182,7 @@ struct alignas(16) Tail {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t drain_b;     // SPLIT: the second MMA thread's operations finished
     uint64_t xchg_full;   // weights-on-M SwiGLU: up values written (64 arrivals)
     uint64_t xchg_empty;  // weights-on-M SwiGLU: up values consumed (64 arrivals)
     uint64_t r_full[8];   // resident weight slab loaded (TMA bytes)
@@ -520,22 +526,23 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(&st.full[s], C::WRES ? kNumActProducers : 1 + kNumActProducers);
-            ptx::mbar_init(&st.empty[s], 1);
+            ptx::mbar_init(&st.empty[s], LY::MMA_THREADS);  // one commit per MMA thread
         }
         for (int i = 0; i < LY::MAX_SLABS; ++i) {
             ptx::mbar_init(&st.r_full[i], 1);
             ptx::mbar_init(&st.r_empty[i], 1);
         }
         for (int s = 0; s < C::ACC_BUFS; ++s) {
-            ptx::mbar_init(&st.acc_full[s], 1);
+            ptx::mbar_init(&st.acc_full[s], LY::MMA_THREADS);
             ptx::mbar_init(&st.acc_empty[s], 32 * LY::ACC_READERS);
         }
         ptx::mbar_init(&st.drain, 1);
+        ptx::mbar_init(&st.drain_b, 1);
         ptx::mbar_init(&st.xchg_full, 64);
         ptx::mbar_init(&st.xchg_empty, 64);
         for (int i = 0; i < kTileRing; ++i) {
             ptx::mbar_init(&st.tile_full[i], 1);
-            ptx::mbar_init(&st.tile_empty[i], 2 + 1 + LY::EPI_ACTIVE);
+            ptx::mbar_init(&st.tile_empty[i], 2 + LY::MMA_THREADS + LY::EPI_ACTIVE);
         }
         st.abort = 0;
         ptx::fence_mbar_init();
@@ -622,7 +629,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         return ti;
     };
 
-    if (warp == 0) {
+    if (warp == 0 && !C::SPLIT) {
         // ================================ weight producer
         if (lane == 0) {
             int s = 0;
@@ -697,8 +704,8 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 if ((rfilled >> kt) & 1u) drained = ptx::mbar_wait(&st.r_full[kt], ((rph >> kt) & 1u) ^ 1u) && drained;
             if (!drained) set_abort(st, a.status);
         }
-    } else if (warp == 1) {
-        // ================================ MMA issuer
+    } else if (warp == 1 || (C::SPLIT && warp == 0)) {
+        // ================================ MMA issuer(s)
         if constexpr (C::WRES) {
             if (lane == 0) {
                 // Weight-resident units: per token block of the run, K-stage by K-stage, the
@@ -768,11 +775,22 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 if (!ptx::mbar_wait(&st.drain, 0)) set_abort(st, a.status);
             }
         } else if (lane == 0) {
-            const uint32_t idesc = ptx::idesc_nvf4(C::MMA_M, C::MMA_N);
+            // SPLIT: two MMA threads (warp 1: weight rows 0..127 of the tile, warp 0: rows 128..255), each issuing 128 x 128 x 64 MMAs into its half of the accumulator columns with
+            // its own weight scale copy per K-step. A thread's tensor-core operations run one after
+            // another, each taking about as long whatever its N, while two threads' operations overlap:
+            // one K-step of the 256-row tile took 355 cycles from one thread (two scale copies and a
+            // 128 x 256 MMA) and 204 from two (one copy and a 128 x 128 MMA each). Both threads copy
+            // the activation scales into the same columns (identical bytes); the columns are not
+            // rewritten before every operation that reads them has completed (stage slots: the empty
+            // barrier counts both threads' commits; resident unit scales: the accumulator barrier).
+            const int half = (C::SPLIT && warp != 1) ? 1 : 0;
+            constexpr int N_MMA = C::SPLIT ? C::MMA_N / 2 : C::MMA_N;
+            const uint32_t idesc = ptx::idesc_nvf4(C::MMA_M, N_MMA);
             // descriptors of stage 0; stage s adds s * STAGE_BYTES to the start address field and
             // K-step kk adds 32 bytes (operands) or one 512-byte scale tile
             const uint32_t s0 = ptx::smem_u32(smem);
-            const uint64_t dw0 = ptx::sdesc_sw128(s0 + LY::OFF_W), dact0 = ptx::sdesc_sw128(s0 + LY::OFF_ACT);
+            const uint64_t dw0 = ptx::sdesc_sw128(s0 + LY::OFF_W + half * N_MMA * BK_BYTES);
+            const uint64_t dact0 = ptx::sdesc_sw128(s0 + LY::OFF_ACT);
             const uint64_t dsfw0 = ptx::sdesc_sf(s0 + LY::OFF_SFW), dsfact0 = ptx::sdesc_sf(s0 + LY::OFF_SFACT);
             constexpr uint64_t kStageAdv = LY::STAGE_BYTES >> 4, kOpAdv = 32 >> 4, kSfAdv = SF_TILE >> 4;
             int s = 0;
@@ -790,19 +808,22 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                     const uint32_t as = lt % C::ACC_BUFS, aph = (lt / C::ACC_BUFS) & 1;
                     if (!ptx::mbar_wait(&st.acc_empty[as], aph ^ 1)) { set_abort(st, a.status); ok = false; break; }
                     ptx::tc_fence_after();
-                    const uint32_t d_tmem = tmem + as * C::ACC_COLS;
+                    const uint32_t d_tmem = tmem + as * C::ACC_COLS + half * N_MMA;
                     uint32_t acc = 0;
                     // one K-step: the scale tiles into tensor memory, then the MMA (the tensor pipe runs
-                    // them in issue order; the copies, not the MMA, bound its rate); the issuing
-                    // thread's own instruction count matters too, so full stages take a straight-line
-                    // path. A 256-row weight tile has two scale tiles per K-step: rows 128..255 go to the
-                    // next four columns. Units keep the activation scales of K-step kg in columns
-                    // SFA_COL + 4 kg, copied during the first weight block.
+                    // them in issue order); full stages take a straight-line path. Weight rows
+                    // 128..255 of a 256-row tile have their scale tile in the next four columns. Units
+                    // keep the activation scales of K-step kg in columns SFA_COL + 4 kg, copied during
+                    // the first weight block.
                     auto kstep = [&](uint64_t so, uint32_t tsfw, uint32_t tsfact, int kk, int kg) {
                         const uint32_t tw = tsfw + kk * LY::SFW_STEP_COLS;
+                        if constexpr (C::SPLIT) {
+                            ptx::tmem_cp_32x128b_x4(tw + half * 4, dsfw0 + so + kk * kSfAdv + half * (SF_STAGE >> 4));
+                        } else {
 #pragma unroll
-                        for (int j = 0; j < LY::WB; ++j)
-                            ptx::tmem_cp_32x128b_x4(tw + j * 4, dsfw0 + so + kk * kSfAdv + j * (SF_STAGE >> 4));
+                            for (int j = 0; j < LY::WB; ++j)
+                                ptx::tmem_cp_32x128b_x4(tw + j * 4, dsfw0 + so + kk * kSfAdv + j * (SF_STAGE >> 4));
+                        }
                         uint32_t tsa;
                         if constexpr (C::ROWS) {
                             tsa = tmem + LY::RES_SF_COL + kg * 4;
@@ -815,7 +836,7 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                         if (kSwap)
                             ptx::mma_nvf4(d_tmem, dw, dact, idesc, tw, tsa, acc);
                         else
-                            ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsa, tw, acc);
+                            ptx::mma_nvf4(d_tmem, dact, dw, idesc, tsa, tw + half * 4, acc);
                         acc = 1;
                     };
                     for (int kt = 0; kt < k_stages; ++kt) {
@@ -841,8 +862,9 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 if (!ok) break;
             }
             // every issued tensor-core operation finishes before TMEM is freed
-            ptx::tc_commit(&st.drain);
-            if (!ptx::mbar_wait(&st.drain, 0)) set_abort(st, a.status);
+            uint64_t* drain = half ? &st.drain_b : &st.drain;
+            ptx::tc_commit(drain);
+            if (!ptx::mbar_wait(drain, 0)) set_abort(st, a.status);
         }
     } else if (warp < 4) {
         // ================================ activation producers (row gather)
@@ -890,9 +912,34 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         uint32_t ph = 0;
         bool ok = true;
         TileCursor tc;
+        // SPLIT: lane 0 of the first producer warp is the weight producer too. It claims the tiles
+        // (in the order the CTAs come for them, phase-0 tiles first, so a CTA whose tiles run short
+        // takes more and the down tiles go out in the order their inputs complete), publishes each
+        // one before taking it back from the ring, and loads each stage's weight box and weight scale
+        // tiles once the stage is free.
+        const bool wprod = C::SPLIT && warp == 2 && lane == 0;
+        int Lw = blockIdx.x;
+        bool w_done = false;
+        TileCursor tcw;
+        uint32_t fills = 0;
         for (;;) {
+            if (wprod && !w_done) {
+                if (Lw > total) Lw = total;
+                if (!tile_publish(st, tcw, Lw)) {
+                    set_abort(st, a.status);
+                    w_done = true;
+                } else if (Lw >= total) {
+                    // this CTA's last tile is loading: the next launch may be scheduled (its CTAs
+                    // start as SMs free up; its dependent reads wait for this grid to complete)
+                    ptx::griddep_launch_dependents();
+                    w_done = true;
+                }
+            }
+            // the next claim's round trip overlaps this tile's stages
+            const int Lw_next = (wprod && !w_done) ? static_cast<int>(gridDim.x) + atomicAdd(a.tile_counter, 1) : total;
             const int L = tile_take(st, tc, total, false);
             if (L >= total || !ok || aborted(st)) break;
+            Lw = Lw_next;
             const TileInfo tu = tile_at(L);
             const GemmProblem& P = a.p[tu.ph];
             const int64_t a_ld = P.K / 2, sf_ld = P.K / 16;
@@ -941,6 +988,22 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 }
                 for (int kt = 0; kt < k_stages; ++kt) {
                     if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                    if (wprod) {
+                        // the weight box (TMA) and the weight scale tiles of this stage:
+                        // scale tiles are stored [G][N/128][K/64][512 bytes]
+                        const int nat = min(4, kb64 - kt * 4);
+                        uint8_t* sbase = smem + s * LY::STAGE_BYTES;
+                        ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + LY::WB * nat * SF_TILE);
+                        ptx::tma_load_3d(sbase + LY::OFF_W, ti.ph ? &tmap_w1 : &tmap_w0, &st.full[s], 0, ti.nb * W_ROWS,
+                                         ti.g * k_stages + kt);
+                        const uint8_t* sfw =
+                            P.b_sf + ((static_cast<int64_t>(ti.g) * (P.N / 128) + ti.nb * LY::WB) * kb64 + kt * 4) * SF_TILE;
+#pragma unroll
+                        for (int j = 0; j < LY::WB; ++j)
+                            ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sfw + static_cast<int64_t>(j) * kb64 * SF_TILE,
+                                           nat * SF_TILE, &st.full[s]);
+                        ++fills;
+                    }
                     uint8_t* sact = smem + s * LY::STAGE_BYTES + LY::OFF_ACT;
                     uint8_t* ssf = smem + s * LY::STAGE_BYTES + LY::OFF_SFACT;
                     const bool kin = static_cast<int64_t>(kt) * BK_BYTES + chunk * 16 < a_ld;
@@ -990,6 +1053,8 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
         }
         if constexpr (LY::PUBLISH) publish_all();
         ptx::cp_async_wait<0>();  // no copy outlives the role
+        // nor a weight load: every stage's last fill has landed
+        if (wprod && !ptx::ring_drain(st.full, C::STAGES, fills)) set_abort(st, a.status);
     } else if constexpr (C::XCHG) {
         // ================================ epilogue through shared memory (32-row token blocks)
         // The two warps of lane quarter 0 copy the tile's accumulator (rows 0..31) to shared memory
