@@ -511,6 +511,7 @@ __device__ __forceinline__ uint32_t encode16_rcp(const float (&v)[16], float S, 
 template <int kMode>
 __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
     k_grouped_gemm_nvf4(const __grid_constant__ CUtensorMap tmap_w0, const __grid_constant__ CUtensorMap tmap_w1,
+                        const __grid_constant__ CUtensorMap tmap_a0, const __grid_constant__ CUtensorMap tmap_a1,
                         const GemmArgs a)
 {
     using C = Cfg<kMode>;
@@ -950,6 +951,45 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
             // token blocks, each with its own rows.)
             for (int sub = 0; ok && sub < n_sub(tu); ++sub) {
                 const TileInfo ti = sub_tile(tu, sub);
+                if (C::SPLIT && a.a_tma[tu.ph]) {
+                    // contiguous activation rows with scales in token-block tiles: the weight-producing
+                    // lane loads each stage's 128 rows as one TMA box (rows past the end read as
+                    // zeros) and the stage's scale tiles as one bulk copy, with the weights
+                    if (sub == 0 && ti.ph == 1) {
+                        const int target = LY::READY_PER_TILE * (a.p[0].N / W_ROWS) + ready_extra;
+                        if (!spin_until(a.ready + ti.tbg, target, ready_limit_ns)) { set_abort(st, a.status); ok = false; break; }
+                        // h, stored by other threads' generic stores, is then read by this lane's copies
+                        if (wprod) ptx::fence_proxy_async_global();
+                    }
+                    const uint8_t* act_sf = P.a_sf + static_cast<int64_t>(ti.tbg) * kb64 * SF_TILE;
+                    for (int kt = 0; kt < k_stages; ++kt) {
+                        if (!ptx::mbar_wait(&st.empty[s], ph ^ 1)) { set_abort(st, a.status); ok = false; break; }
+                        if (wprod) {
+                            const int nat = min(4, kb64 - kt * 4);
+                            const bool sf_copy = !C::ROWS || sub == 0;
+                            uint8_t* sbase = smem + s * LY::STAGE_BYTES;
+                            ptx::mbar_arrive_expect_tx(&st.full[s], LY::W_BYTES + LY::WB * nat * SF_TILE + LY::ACT_BYTES +
+                                                                        (sf_copy ? nat * SF_TILE : 0));
+                            ptx::tma_load_3d(sbase + LY::OFF_W, ti.ph ? &tmap_w1 : &tmap_w0, &st.full[s], 0, ti.nb * W_ROWS,
+                                             ti.g * k_stages + kt);
+                            const uint8_t* sfw =
+                                P.b_sf + ((static_cast<int64_t>(ti.g) * (P.N / 128) + ti.nb * LY::WB) * kb64 + kt * 4) * SF_TILE;
+#pragma unroll
+                            for (int j = 0; j < LY::WB; ++j)
+                                ptx::bulk_load(sbase + LY::OFF_SFW + j * SF_STAGE, sfw + static_cast<int64_t>(j) * kb64 * SF_TILE,
+                                               nat * SF_TILE, &st.full[s]);
+                            ptx::tma_load_3d(sbase + LY::OFF_ACT, ti.ph ? &tmap_a1 : &tmap_a0, &st.full[s], kt * BK_BYTES,
+                                             static_cast<int32_t>(ti.row0), 0);
+                            if (sf_copy)
+                                ptx::bulk_load(sbase + LY::OFF_SFACT, act_sf + static_cast<int64_t>(kt) * 4 * SF_TILE,
+                                               nat * SF_TILE, &st.full[s]);
+                            ++fills;
+                        }
+                        ptx::mbar_arrive(&st.full[s]);  // this thread's arrival (it copied nothing)
+                        if (++s == C::STAGES) { s = 0; ph ^= 1; }
+                    }
+                    continue;
+                }
                 if (sub == 0 || C::WRES) {
                     if (ti.ph == 1) {
                         // the down GEMM reads h: wait until every gate/up tile of this token block stored
@@ -1533,6 +1573,21 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     if (a.nphase == 1) tmap[1] = tmap[0];
+    // contiguous activation rows of a phase (no gather index) with scales in token-block tiles come
+    // as TMA boxes of 128 rows x 128 bytes (token-block units with two MMA threads); a phase whose
+    // codes a box cannot address keeps the per-row copies
+    GemmArgs b = a;
+    CUtensorMap tmap_a[2] = {tmap[0], tmap[0]};
+    for (int i = 0; i < 2; ++i) {
+        b.a_tma[i] = 0;
+        if (!C::SPLIT || i >= a.nphase || a.p[i].a_row || !a.p[i].a_sf_tiled || a.route.topk_ids) continue;
+        const GemmProblem& P = a.p[i];
+        if (encode_tmap_3d_u8(&tmap_a[i], P.a_codes, static_cast<uint64_t>(P.K / 2), static_cast<uint64_t>(p_max), 1,
+                              BK_BYTES, C::ACT_ROWS) == CUDA_SUCCESS)
+            b.a_tma[i] = 1;
+        else
+            tmap_a[i] = tmap[0];
+    }
     const int64_t blocks_ub = (p_max + C::ACT_ROWS - 1) / C::ACT_ROWS + a.G;
     const int64_t tiles_ub = blocks_ub * (C::ROWS ? 1 : a.p[0].N / C::W_ROWS);
     const int grid = static_cast<int>(tiles_ub < sms ? (tiles_ub < 1 ? 1 : tiles_ub) : sms);
@@ -1541,7 +1596,7 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
     // grid is resident once earlier kernels on the SMs have drained (they never wait on this one);
     // the waits are bounded in any case and report a timeout in the status word.
     return launch_pdl(k_grouped_gemm_nvf4<kMode>, dim3(grid), dim3(Lay<kMode>::THREADS), smem_bytes<kMode>(), stream,
-                      tmap[0], tmap[1], a);
+                      tmap[0], tmap[1], tmap_a[0], tmap_a[1], b);
 }
 
 bool gemm_rows_pays(int64_t p_max, int sms)

@@ -115,6 +115,8 @@ struct GemmArgs {
     int32_t* tile_counter;    // tiles handed out beyond the first gridDim.x, zeroed before each launch
     int* status;
     const WsHeader* hooks;    // nullable: the workspace header whose test_* fields the waits read
+    int a_tma[2];             // set by the launcher: phase i's activation rows are contiguous and come
+                              // as TMA boxes (token-block units with two MMA threads only)
 };
 constexpr int kGemmMaxG = 1025;
 // Tile schedules: activations on the MMA's M side (128-row token blocks x 128 weight rows),

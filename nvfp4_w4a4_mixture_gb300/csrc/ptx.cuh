@@ -178,6 +178,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Order global memory this thread has observed (e.g. another CTA's stores, acquired through a flag)
+// before its later async-proxy (TMA, bulk copy) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ------------------------------------------------------------------------------------------------
