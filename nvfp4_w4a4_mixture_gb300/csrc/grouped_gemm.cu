@@ -776,9 +776,10 @@ __global__ void __launch_bounds__(Lay<kMode>::THREADS, 1)
                 if (!ptx::mbar_wait(&st.drain, 0)) set_abort(st, a.status);
             }
         } else if (lane == 0) {
-            // SPLIT: two MMA threads (warp 1: weight rows 0..127 of the tile, warp 0: rows 128..255), each issuing 128 x 128 x 64 MMAs into its half of the accumulator columns with
-            // its own weight scale copy per K-step. A thread's tensor-core operations run one after
-            // another, each taking about as long whatever its N, while two threads' operations overlap:
+            // SPLIT: two MMA threads (warp 1: weight rows 0..127 of the tile, warp 0: rows 128..255),
+            // each issuing 128 x 128 x 64 MMAs into its half of the accumulator columns with its own
+            // weight scale copy per K-step. A thread's tensor-core operations run one after another,
+            // each taking about as long whatever its N, while two threads' operations overlap:
             // one K-step of the 256-row tile took 355 cycles from one thread (two scale copies and a
             // 128 x 256 MMA) and 204 from two (one copy and a 128 x 128 MMA each). Both threads copy
             // the activation scales into the same columns (identical bytes); the columns are not
