@@ -35,6 +35,7 @@ cores, one bounded sample of the workload per step.
 """
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -253,10 +254,15 @@ def distinct_experts(m, layer, x):
 
 
 def gemm_sources_hash():
+    """Hash of the expert GEMM's sources with comments and blank space removed: a traffic record stays
+    valid across edits that do not change the code."""
     h = hashlib.sha256()
     for f in ("grouped_gemm.cu", "ptx.cuh", "common.cuh", "kernels.cuh"):
-        with open(os.path.join(ROOT, "nvfp4_w4a4_mixture_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "nvfp4_w4a4_mixture_gb300", "csrc", f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
