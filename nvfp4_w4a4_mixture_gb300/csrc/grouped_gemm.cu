@@ -1574,14 +1574,14 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
         if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     if (a.nphase == 1) tmap[1] = tmap[0];
-    // contiguous activation rows of a phase (no gather index) with scales in token-block tiles come
-    // as TMA boxes of 128 rows x 128 bytes (token-block units with two MMA threads); a phase whose
-    // codes a box cannot address keeps the per-row copies
+    // contiguous activation rows of a phase (no gather index) with scales in token-block tiles and
+    // whole 256-value K-stages come as TMA boxes of 128 rows x 128 bytes (token-block units with two
+    // MMA threads); a phase whose codes a box cannot address keeps the per-row copies
     GemmArgs b = a;
     CUtensorMap tmap_a[2] = {tmap[0], tmap[0]};
     for (int i = 0; i < 2; ++i) {
         b.a_tma[i] = 0;
-        if (!C::SPLIT || i >= a.nphase || a.p[i].a_row || !a.p[i].a_sf_tiled || a.route.topk_ids) continue;
+        if (!C::SPLIT || i >= a.nphase || a.p[i].a_row || !a.p[i].a_sf_tiled || a.route.topk_ids || a.p[i].K % 256) continue;
         const GemmProblem& P = a.p[i];
         if (encode_tmap_3d_u8(&tmap_a[i], P.a_codes, static_cast<uint64_t>(P.K / 2), static_cast<uint64_t>(p_max), 1,
                               BK_BYTES, C::ACT_ROWS) == CUDA_SUCCESS)
@@ -1602,10 +1602,12 @@ static cudaError_t launch_t(const GemmArgs& a, int64_t p_max, int sms, cudaStrea
 
 bool gemm_rows_pays(int64_t p_max, int sms)
 {
-    // Token-block units carry six (gate/up) or eight (down) weight blocks each: with fewer than about
-    // eight 128-row blocks per SM the last units leave SMs idle for longer than the saved scale
-    // copies gain (4k tokens: 305 vs 285 us; 16k tokens: 990 vs 1031 us for the expert GEMMs).
-    return p_max >= 8LL * sms * Cfg<kModeWideRows>::ACT_ROWS;
+    // Token-block units carry six (gate/up) or eight (down) weight blocks each, so with few 128-row
+    // blocks per SM the last units leave SMs idle longer. With one MMA thread that outweighed the
+    // saved scale copies below about eight blocks per SM (4k tokens: 305 vs 285 us). Their two MMA
+    // threads and TMA activation boxes now win from about one block per SM: 4k tokens 217 vs 245 us,
+    // 2,048 tokens 240 vs 262 us for the expert GEMMs.
+    return p_max >= 1LL * sms * Cfg<kModeWideRows>::ACT_ROWS;
 }
 
 bool gemm_wide_fits(const GemmArgs& a)
