@@ -253,12 +253,15 @@ def distinct_experts(m, layer, x):
     return int(ids.unique().numel())
 
 
-def gemm_sources_hash():
+GEMM_SOURCES = ("grouped_gemm.cu", "ptx.cuh", "common.cuh", "kernels.cuh")
+
+
+def gemm_sources_hash(csrc=os.path.join(ROOT, "nvfp4_w4a4_mixture_gb300", "csrc")):
     """Hash of the expert GEMM's sources with comments and blank space removed: a traffic record stays
     valid across edits that do not change the code."""
     h = hashlib.sha256()
-    for f in ("grouped_gemm.cu", "ptx.cuh", "common.cuh", "kernels.cuh"):
-        with open(os.path.join(ROOT, "nvfp4_w4a4_mixture_gb300", "csrc", f), encoding="utf-8") as fh:
+    for f in GEMM_SOURCES:
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
         text = re.sub(r"//[^\n]*", " ", text)

@@ -51,3 +51,19 @@ def test_roofline_picks_the_longer_time():
 def test_default_workload_is_the_largest_single_layer_config():
     assert bench.DEFAULT_CONFIG == "prefill16k"
     assert set(bench.EXTRA_CONFIGS) == {"decode", "decode_stack48", "stack48"}
+
+
+def test_traffic_hash_ignores_comments_but_not_code(tmp_path):
+    src = os.path.join(ROOT, "nvfp4_w4a4_mixture_gb300", "csrc")
+    for f in bench.GEMM_SOURCES:
+        with open(os.path.join(src, f), encoding="utf-8") as fh:
+            (tmp_path / f).write_text(fh.read(), encoding="utf-8")
+    base = bench.gemm_sources_hash(str(tmp_path))
+    assert base == bench.gemm_sources_hash()
+    k = tmp_path / "grouped_gemm.cu"
+    text = k.read_text(encoding="utf-8")
+    k.write_text("// a new comment line\n/* and a block\n   comment */\n" + text.replace(";", ";   ", 3), encoding="utf-8")
+    assert bench.gemm_sources_hash(str(tmp_path)) == base
+    k.write_text(text.replace("STAGES = 4", "STAGES = 3", 1), encoding="utf-8")
+    assert bench.gemm_sources_hash(str(tmp_path)) != base
+
