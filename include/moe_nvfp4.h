@@ -98,7 +98,8 @@ enum {
                                           * else activations on M) */
     MOE_GEMM_SCHED_WIDE_ROWS = 0x800,    /* wide tiles, each CTA taking a whole 128-row token block
                                           * through every weight block (the activation scales stay
-                                          * in tensor memory); K <= 2048, else wide */
+                                          * in tensor memory; two threads issue the MMAs, 128 weight
+                                          * rows each); K <= 2048, else wide */
     MOE_GEMM_SCHED_WEIGHTS_RESIDENT = 0x1000 /* one group's 128-row weight block (all of K) kept in shared
                                           * memory, its scales in tensor memory, while up to 16 of the
                                           * group's 128-row token blocks stream past it into two
